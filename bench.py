@@ -1,0 +1,396 @@
+"""MoE-layer throughput on GB300: tokens/s of one forward layer (router top-k,
+layout, pull dispatch, grouped SwiGLU FFN, weighted combine) through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+One JSON line on rank 0.  N > 1 runs under torch.distributed.run: every rank
+runs its own independent layer on its own batch of T tokens (the layer is
+per-token, so batches shard with no data-path collective: weak scaling); the
+time is the max over ranks and the value the tokens of all ranks / that time.
+Inputs are seeded synthetic tensors of the workload's shape (no dataset).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s fwd & fwd+bwd on 1 GB300; % of FP8 TC / HBM roofline"
+DEFAULT_WORKLOAD = "mixtral_bf16"
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["mok", "reference"], default="mok")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    return p.parse_args()
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, sm_max_default):
+        if self.proc is None or self.file is None:
+            return {"sm_mhz": None, "sm_max_mhz": sm_max_default, "reasons": ["unsampled"]}
+        self.file.flush()
+        with open(self.file.name) as f:
+            rows = [r.strip().split(",") for r in f if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else sm_max_default,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _layer_flops(w):
+    return 6.0 * w.S * w.d * w.F
+
+
+def _layer_bytes(w):
+    """Algorithmic HBM bytes of one forward: every byte the method must move once."""
+    e = 1 if w.dtype == "mxfp8" else 2
+    sc = 1 / 32 if w.dtype == "mxfp8" else 0
+    weights = w.E * 3 * w.F * w.d * (e + sc)
+    x = w.T * w.d * 2
+    xe = 2 * w.S * w.d * (e + sc)
+    h = 2 * w.S * w.F * (e + sc)
+    ystage = 2 * w.S * w.d * 2
+    out = w.T * w.d * 2
+    return weights + x + xe + h + ystage + out
+
+
+def run_reference(args):
+    """The oracle as it stands, timed on the host cores on a bounded token sample."""
+    rank, world, _ = _dist()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    from combine_top_routing_gb300 import inputs as I
+    from oracle import oracle as O
+    w = I.WORKLOADS[args.workload]
+    inp = I.make_inputs(w, device="cpu")
+    kind = O.SOFTMAX if w.router == "softmax" else O.SIGMOID
+
+    def bf(t):
+        return O.bf16_values(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+    ntok = args.cpu_sample_tokens or 2
+    rng = np.random.default_rng(0)
+    x = bf(inp["x"])
+    Wr = inp["Wr"].double().numpy()
+    bias = None if inp["bias"] is None else inp["bias"].double().numpy()
+    ge = lambda e: (bf(inp["Wg"][e]), bf(inp["Wu"][e]), bf(inp["Wd"][e]))
+
+    def step():
+        tok = np.sort(rng.choice(w.T, ntok, replace=False))
+        O.forward(x, Wr, bias, ge, E=w.E, k=w.k, kind=kind, mode=w.dtype, tokens=tok)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    cores = len(os.sched_getaffinity(0))
+    val = ntok / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "d_model": w.d, "experts": w.E, "top_k": w.k,
+                   "d_ff": w.F, "gemm_dtype": w.dtype, "sample_tokens_per_step": ntok},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{ntok} random tokens of {w.name} per step (full layer "
+                                   f"forward of those tokens, fp64 oracle)"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline(w, inp_gpu, budget_s=20.0):
+    """Oracle forward on a bounded token sample, on this host's cores."""
+    import numpy as np
+    import torch
+
+    from oracle import oracle as O
+    kind = O.SOFTMAX if w.router == "softmax" else O.SIGMOID
+
+    def bf(t):
+        return O.bf16_values(t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+
+    x = bf(inp_gpu["x"])
+    Wr = inp_gpu["Wr"].double().cpu().numpy()
+    bias = None if inp_gpu["bias"] is None else inp_gpu["bias"].double().cpu().numpy()
+    ge = lambda e: (bf(inp_gpu["Wg"][e]), bf(inp_gpu["Wu"][e]), bf(inp_gpu["Wd"][e]))
+    rng = np.random.default_rng(1)
+    ntok, total_tok, t_total = 2, 0, 0.0
+    while t_total < budget_s:
+        tok = np.sort(rng.choice(w.T, ntok, replace=False))
+        t0 = time.perf_counter()
+        O.forward(x, Wr, bias, ge, E=w.E, k=w.k, kind=kind, mode=w.dtype, tokens=tok)
+        t_total += time.perf_counter() - t0
+        total_tok += ntok
+        if t_total < budget_s / 4:
+            ntok *= 2
+    cores = len(os.sched_getaffinity(0))
+    return {"value": total_tok / t_total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{total_tok} random tokens of {w.name} through the fp64 oracle forward "
+                      f"({t_total:.1f} s of CPU work)"}
+
+
+def main():
+    args = _args()
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world, local = _dist()
+    import torch
+    import torch.distributed as dist
+
+    from combine_top_routing_gb300 import inputs as I
+    from combine_top_routing_gb300 import mok
+    from combine_top_routing_gb300.layer import MoELayer
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    w = I.WORKLOADS[args.workload]
+    inp = I.make_inputs(I.scaled(w, seed=w.seed + 1000 * rank), device="cuda")
+    layer = MoELayer(w, inp)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---------------- device-resident timed region
+    for _ in range(max(3, args.warmup)):
+        layer.forward()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    peaks, peak_src = _peaks()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            layer.forward()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    status = layer.status()
+    if status != 0:
+        raise RuntimeError(f"device status {mok.status_string(status)}")
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * w.T / (ms / 1e3)
+
+    # ---------------- the expert FFN (dominant kernels) timed alone, same stream
+    R = _route_for_ffn(layer)
+    ffn_iters = max(5, min(50, args.steps))
+    for _ in range(2):
+        _ffn(layer, R)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(ffn_iters):
+        _ffn(layer, R)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ffn_ms = e0.elapsed_time(e1) / ffn_iters
+    flops = _layer_flops(w)
+    ffn_tflops = flops / (ffn_ms / 1e3) / 1e12
+    bf16_peak = peaks.get("bf16_tflops", 1900.0)
+    peak_tc = bf16_peak * (2.0 if w.dtype == "mxfp8" else 1.0)
+
+    # ---------------- end to end through the C ABI with host buffers
+    x_host = torch.empty_like(inp["x"], device="cpu").pin_memory()
+    x_host.copy_(inp["x"].cpu())
+    out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    for _ in range(2):
+        _e2e_step(layer, x_host, out_host)
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(e2e_steps):
+        _e2e_step(layer, x_host, out_host)
+    s1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = s0.elapsed_time(s1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = world * w.T / (e2e_ms / 1e3)
+
+    base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        base = cpu_baseline(w, inp)
+
+    if rank == 0:
+        clocks = clk.summary(peaks.get("sm_max_mhz"))
+        launches_per_step = 10
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp8(e4m3+e8m0)/fp32-acc" if w.dtype == "mxfp8" else "bf16/fp32-acc",
+            "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "d_model": w.d, "experts": w.E,
+                       "top_k": w.k, "d_ff": w.F, "gemm_dtype": w.dtype,
+                       "router": w.router, "pass": "forward",
+                       "l2": "inputs larger than L2 (expert weights %.1f GB)" %
+                             (w.E * 3 * w.F * w.d * (1 if w.dtype == 'mxfp8' else 2) / 1e9),
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": ffn_tflops, "peak": peak_tc,
+                         "unit": "TFLOP/s", "frac": ffn_tflops / peak_tc, "traffic": None,
+                         "kernel": "k_gemm FFN1+FFN2 (expert_ffn)",
+                         "peak_source": f"{peak_src} bf16 burst"
+                                        + (" x2 for fp8" if w.dtype == "mxfp8" else ""),
+                         "ms_per_launch": ffn_ms},
+            "layer_roofline": {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
+                               "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /
+                                           peaks.get("hbm_gbs", 6800.0)},
+            "e2e": {"value": e2e_val, "unit": "tokens/s",
+                    "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": base,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _route_for_ffn(layer):
+    """Route once so that the FFN alone can be timed on fixed layout buffers."""
+    import torch
+    w = layer.w
+    class R:
+        pass
+    r = R()
+    dev = "cuda"
+    r.ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    r.gates = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    r.counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    r.offsets = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    r.pad_offsets = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    r.slot_pos = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    r.row_tok = torch.empty(w.S, dtype=torch.int32, device=dev)
+    r.row_j = torch.empty(w.S, dtype=torch.uint8, device=dev)
+    from combine_top_routing_gb300 import mok
+    from combine_top_routing_gb300.layer import scale_words
+    mok.route_layout(layer.cfg, layer.x_src, layer.W_r, layer.bias, r.ids, r.gates, None, None,
+                     r.counts, r.offsets, r.pad_offsets, r.slot_pos, r.row_tok, r.row_j, layer.ws)
+    rows = layer.rows_pad
+    if w.dtype == "mxfp8":
+        r.xe = torch.empty((rows, w.d), dtype=torch.uint8, device=dev)
+        r.xs = torch.empty(scale_words(rows, w.d), dtype=torch.int32, device=dev)
+    else:
+        r.xe = torch.empty((rows, w.d), dtype=torch.bfloat16, device=dev)
+        r.xs = None
+    mok.dispatch(layer.cfg, layer.x_src, r.ids, r.offsets, r.pad_offsets, r.row_tok, r.row_j,
+                 r.xe, r.xs)
+    r.ystage = torch.empty((w.T, w.k, w.d), dtype=torch.bfloat16, device=dev)
+    return r
+
+
+def _ffn(layer, r):
+    from combine_top_routing_gb300 import mok
+    mok.expert_ffn(layer.cfg, r.xe, r.xs, layer.wstruct, r.offsets, r.pad_offsets, r.row_tok,
+                   r.row_j, r.ystage, None, None, None, layer.ws)
+
+
+def _e2e_step(layer, x_host, out_host):
+    layer.x.copy_(x_host, non_blocking=True)
+    if len(layer.x_src) > 1:
+        n = len(layer.x_src)
+        rows = layer.x.shape[0] // n
+        for s, buf in enumerate(layer.x_src):
+            buf.copy_(layer.x[s * rows:(s + 1) * rows], non_blocking=True)
+    layer.forward()
+    out_host.copy_(layer.out, non_blocking=True)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,444 @@
+// mok_api.cu -- the C ABI of libmok.so (declared in include/mok.h): argument
+// checks, workspace carving, tensor-map encoding and the order of launches.
+// No entry point allocates, frees or synchronises the host, except
+// mok_get_device_status, which synchronises by contract.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "mok.h"
+#include "mok_internal.h"
+
+namespace mok {
+
+static constexpr size_t kAlign = 256;
+
+static size_t take(size_t *cursor, size_t bytes)
+{
+    const size_t off = (*cursor + kAlign - 1) / kAlign * kAlign;
+    *cursor = off + bytes;
+    return off;
+}
+
+int check_config(const mok_config *cfg, Dims *dm)
+{
+    if (!cfg) return MOK_ERR_INVALID_ARG;
+    const int T = cfg->T, d = cfg->d_model, E = cfg->n_experts, k = cfg->top_k, F = cfg->d_ff;
+    if (T < 1 || d < 1 || E < 1 || k < 1 || F < 1) return MOK_ERR_INVALID_ARG;
+    if (cfg->router != MOK_ROUTER_SOFTMAX && cfg->router != MOK_ROUTER_SIGMOID) return MOK_ERR_INVALID_ARG;
+    if (cfg->dtype != MOK_BF16 && cfg->dtype != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
+    if (cfg->n_sources < 1 || cfg->n_sources > MOK_MAX_SOURCES) return MOK_ERR_INVALID_ARG;
+    if (cfg->n_sources > 1 && !cfg->source_rows) return MOK_ERR_INVALID_ARG;
+    if (cfg->minibatch_rows != 0 && cfg->minibatch_rows != 64 && cfg->minibatch_rows != 128 &&
+        cfg->minibatch_rows != 256)
+        return MOK_ERR_INVALID_ARG;
+    if (cfg->gather_sm_fraction < 0.0f || cfg->gather_sm_fraction >= 1.0f) return MOK_ERR_INVALID_ARG;
+    if (E > MOK_MAX_EXPERTS || k > MOK_MAX_TOPK || k > E) return MOK_ERR_UNSUPPORTED;
+    if (d % 128 != 0 || F % 128 != 0) return MOK_ERR_UNSUPPORTED;
+    const int64_t S = static_cast<int64_t>(T) * k;
+    if (S + static_cast<int64_t>(E) * MOK_ROW_ALIGN > (int64_t{1} << 31) - 1) return MOK_ERR_UNSUPPORTED;
+    if (cfg->n_sources > 1) {
+        int64_t sum = 0;
+        for (int s = 0; s < cfg->n_sources; ++s) {
+            if (cfg->source_rows[s] < 1) return MOK_ERR_INVALID_ARG;
+            if (cfg->source_rows[s] % 128 != 0) return MOK_ERR_UNSUPPORTED;
+            sum += cfg->source_rows[s];
+        }
+        if (sum != T) return MOK_ERR_INVALID_ARG;
+    }
+    if (dm) {
+        dm->T = T;
+        dm->d = d;
+        dm->E = E;
+        dm->k = k;
+        dm->F = F;
+        dm->router = cfg->router;
+        dm->dtype = cfg->dtype;
+        dm->S = S;
+        dm->rows_pad = round_up(S + static_cast<int64_t>(E) * (MOK_ROW_ALIGN - 1), MOK_ROW_ALIGN);
+        dm->E_pad = static_cast<int>(round_up(E, 128));
+        dm->nchunks = static_cast<int>((S + kLayoutChunk - 1) / kLayoutChunk);
+    }
+    return MOK_OK;
+}
+
+void ctx_layout(const Dims &dm, mok_ctx_layout *c)
+{
+    size_t cur = 0;
+    const size_t S = static_cast<size_t>(dm.S);
+    c->ids = take(&cur, S * 4);
+    c->gates = take(&cur, S * 4);
+    c->sel_scores = take(&cur, S * 4);
+    c->counts = take(&cur, static_cast<size_t>(dm.E) * 4);
+    c->offsets = take(&cur, static_cast<size_t>(dm.E + 1) * 4);
+    c->pad_offsets = take(&cur, static_cast<size_t>(dm.E + 1) * 4);
+    c->slot_pos = take(&cur, S * 4);
+    c->row_tok = take(&cur, S * 4);
+    c->row_j = take(&cur, S);
+    c->logits = take(&cur, static_cast<size_t>(dm.T) * dm.E * 4);
+    const size_t rowsF = static_cast<size_t>(dm.rows_pad) * dm.F * 2;
+    c->a = take(&cur, rowsF);
+    c->b = take(&cur, rowsF);
+    c->h = take(&cur, rowsF);
+    c->ystage = take(&cur, S * dm.d * 2);
+    c->total = (cur + kAlign - 1) / kAlign * kAlign;
+}
+
+void fwd_ws_layout(const Dims &dm, FwdWs *w)
+{
+    size_t cur = 0;
+    const size_t esize = dm.dtype == MOK_MXFP8 ? 1 : 2;
+    w->status = take(&cur, 256);
+    w->chunk_counts = take(&cur, static_cast<size_t>(dm.nchunks) * dm.E * 4);
+    w->chunk_base = take(&cur, static_cast<size_t>(dm.nchunks) * dm.E * 4);
+    w->w3 = take(&cur, static_cast<size_t>(dm.E_pad) * 3 * dm.d * 2);
+    mok_ctx_layout c;
+    ctx_layout(dm, &c);
+    w->route = take(&cur, c.a);  // ids .. logits, same sub-layout as the saved context
+    w->xe = take(&cur, static_cast<size_t>(dm.rows_pad) * dm.d * esize);
+    w->xe_scales = take(&cur, dm.dtype == MOK_MXFP8 ? static_cast<size_t>(dm.rows_pad) * dm.d / 32 : 0);
+    w->h = take(&cur, static_cast<size_t>(dm.rows_pad) * dm.F * esize);
+    w->h_scales = take(&cur, dm.dtype == MOK_MXFP8 ? static_cast<size_t>(dm.rows_pad) * dm.F / 32 : 0);
+    w->ystage = take(&cur, static_cast<size_t>(dm.S) * dm.d * 2);
+    w->total = (cur + kAlign - 1) / kAlign * kAlign;
+}
+
+int make_sources(const mok_config *cfg, const Dims &dm, const void *const *x_src, Sources *s)
+{
+    if (!x_src) return MOK_ERR_INVALID_ARG;
+    s->n = cfg->n_sources;
+    int run = 0;
+    for (int i = 0; i < s->n; ++i) {
+        if (!x_src[i]) return MOK_ERR_INVALID_ARG;
+        s->ptr[i] = static_cast<const uint16_t *>(x_src[i]);
+        s->row_start[i] = run;
+        run += s->n == 1 ? dm.T : cfg->source_rows[i];
+    }
+    s->row_start[s->n] = run;
+    return MOK_OK;
+}
+
+int num_sms()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return 148;
+    if (!cached[dev]) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n > 0 ? n : 148;
+    }
+    return cached[dev];
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int encode_tmap_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner_elems,
+                   uint64_t rows, uint32_t box_inner, uint32_t box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15)) return 1;
+    const uint64_t esize = fp8 ? 1 : 2;
+    cuuint64_t dims[2] = {inner_elems, rows};
+    cuuint64_t strides[1] = {inner_elems * esize};
+    cuuint32_t box[2] = {box_inner, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : 1;
+}
+
+static uint64_t wait_ns(const mok_config *cfg)
+{
+    return cfg->wait_limit_ns ? cfg->wait_limit_ns : 2000000000ull;
+}
+
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA; }
+
+template <typename T>
+static T *at(void *base, size_t off)
+{
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(base) + off);
+}
+
+struct RouteOut {
+    int32_t *ids;
+    float *gates, *sel_scores, *logits;
+    int32_t *counts, *offsets, *pad_offsets, *slot_pos, *row_tok;
+    uint8_t *row_j;
+};
+
+static RouteOut route_in(void *base, const mok_ctx_layout &c)
+{
+    RouteOut r;
+    r.ids = at<int32_t>(base, c.ids);
+    r.gates = at<float>(base, c.gates);
+    r.sel_scores = at<float>(base, c.sel_scores);
+    r.logits = at<float>(base, c.logits);
+    r.counts = at<int32_t>(base, c.counts);
+    r.offsets = at<int32_t>(base, c.offsets);
+    r.pad_offsets = at<int32_t>(base, c.pad_offsets);
+    r.slot_pos = at<int32_t>(base, c.slot_pos);
+    r.row_tok = at<int32_t>(base, c.row_tok);
+    r.row_j = at<uint8_t>(base, c.row_j);
+    return r;
+}
+
+static int route_layout_impl(const mok_config *cfg, const Dims &dm, const Sources &src,
+                             const float *W_r, const float *bias, const RouteOut &o, void *ws,
+                             cudaStream_t st)
+{
+    FwdWs w;
+    fwd_ws_layout(dm, &w);
+    uint16_t *w3 = at<uint16_t>(ws, w.w3);
+    cudaError_t e = launch_router_split(W_r, dm.E, dm.E_pad, dm.d, w3, st);
+    if (e == cudaSuccess)
+        e = launch_router_gemm(dm, src, w3, bias, o.logits, at<uint32_t>(ws, w.status), wait_ns(cfg), st);
+    if (e == cudaSuccess) e = launch_topk(dm, o.logits, o.ids, o.gates, o.sel_scores, st);
+    if (e == cudaSuccess)
+        e = launch_layout(dm, o.ids, o.counts, o.offsets, o.pad_offsets, o.slot_pos, o.row_tok,
+                          o.row_j, at<int32_t>(ws, w.chunk_counts), at<int32_t>(ws, w.chunk_base), st);
+    return cuda_status(e);
+}
+
+}  // namespace mok
+
+using namespace mok;
+
+extern "C" {
+
+int64_t mok_max_padded_rows(const mok_config *cfg)
+{
+    Dims dm;
+    if (check_config(cfg, &dm) != MOK_OK) return 0;
+    return dm.rows_pad;
+}
+
+int mok_workspace_size(const mok_config *cfg, size_t *fwd_ws, size_t *saved_ctx, size_t *bwd_ws)
+{
+    Dims dm;
+    const int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    FwdWs w;
+    fwd_ws_layout(dm, &w);
+    mok_ctx_layout c;
+    ctx_layout(dm, &c);
+    if (fwd_ws) *fwd_ws = w.total;
+    if (saved_ctx) *saved_ctx = c.total;
+    if (bwd_ws) *bwd_ws = w.total;
+    return MOK_OK;
+}
+
+int mok_saved_ctx_layout(const mok_config *cfg, mok_ctx_layout *out)
+{
+    Dims dm;
+    const int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!out) return MOK_ERR_INVALID_ARG;
+    ctx_layout(dm, out);
+    return MOK_OK;
+}
+
+int mok_route_layout(const mok_config *cfg, const void *const *x_src, const float *W_r,
+                     const float *bias, int32_t *ids, float *gates, float *sel_scores,
+                     float *logits, int32_t *counts, int32_t *offsets, int32_t *pad_offsets,
+                     int32_t *slot_pos, int32_t *row_tok, uint8_t *row_j, void *ws, void *stream)
+{
+    Dims dm;
+    int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!W_r || !ids || !gates || !counts || !offsets || !pad_offsets || !slot_pos || !row_tok ||
+        !row_j || !ws)
+        return MOK_ERR_INVALID_ARG;
+    Sources src;
+    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    FwdWs w;
+    fwd_ws_layout(dm, &w);
+    mok_ctx_layout c;
+    ctx_layout(dm, &c);
+    RouteOut o;
+    o.ids = ids;
+    o.gates = gates;
+    o.sel_scores = sel_scores ? sel_scores : at<float>(ws, w.route + c.sel_scores);
+    o.logits = logits ? logits : at<float>(ws, w.route + c.logits);
+    o.counts = counts;
+    o.offsets = offsets;
+    o.pad_offsets = pad_offsets;
+    o.slot_pos = slot_pos;
+    o.row_tok = row_tok;
+    o.row_j = row_j;
+    return route_layout_impl(cfg, dm, src, W_r, bias, o, ws, static_cast<cudaStream_t>(stream));
+}
+
+int mok_dispatch(const mok_config *cfg, const void *const *x_src, const int32_t *ids,
+                 const int32_t *offsets, const int32_t *pad_offsets, const int32_t *row_tok,
+                 const uint8_t *row_j, void *xe, uint32_t *xe_scales, void *stream)
+{
+    Dims dm;
+    int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!ids || !offsets || !pad_offsets || !row_tok || !row_j || !xe) return MOK_ERR_INVALID_ARG;
+    if (dm.dtype == MOK_MXFP8 && !xe_scales) return MOK_ERR_INVALID_ARG;
+    Sources src;
+    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    return cuda_status(launch_dispatch(dm, src, ids, offsets, pad_offsets, row_tok, row_j, xe,
+                                       xe_scales, static_cast<cudaStream_t>(stream)));
+}
+
+int mok_expert_ffn(const mok_config *cfg, const void *xe, const uint32_t *xe_scales,
+                   const mok_weights *w, const int32_t *offsets, const int32_t *pad_offsets,
+                   const int32_t *row_tok, const uint8_t *row_j, void *ystage, void *saved_a,
+                   void *saved_b, void *saved_h, void *ws, void *stream)
+{
+    Dims dm;
+    int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!xe || !w || !offsets || !pad_offsets || !row_tok || !row_j || !ystage || !ws)
+        return MOK_ERR_INVALID_ARG;
+    const bool mx = dm.dtype == MOK_MXFP8;
+    if (mx && (!xe_scales || !w->q_gate || !w->q_up || !w->q_down || !w->s_gate || !w->s_up || !w->s_down))
+        return MOK_ERR_INVALID_ARG;
+    if (!mx && (!w->w_gate || !w->w_up || !w->w_down)) return MOK_ERR_INVALID_ARG;
+    FwdWs fw;
+    fwd_ws_layout(dm, &fw);
+    // per-expert counts follow from the dense offsets; derive them into ws
+    mok_ctx_layout c;
+    ctx_layout(dm, &c);
+    int32_t *counts = at<int32_t>(ws, fw.route + c.counts);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_counts_from_offsets(offsets, dm.E, counts, st);
+    if (e == cudaSuccess)
+        e = launch_ffn(dm, xe, xe_scales, w, counts, offsets, pad_offsets, row_tok, row_j,
+                       at<void>(ws, fw.h), mx ? at<uint32_t>(ws, fw.h_scales) : nullptr,
+                       static_cast<uint16_t *>(ystage), static_cast<uint16_t *>(saved_a),
+                       static_cast<uint16_t *>(saved_b), static_cast<uint16_t *>(saved_h),
+                       at<uint32_t>(ws, fw.status), wait_ns(cfg), st);
+    return cuda_status(e);
+}
+
+int mok_combine(const mok_config *cfg, const void *ystage, const float *gates, void *out,
+                void *stream)
+{
+    Dims dm;
+    const int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!ystage || !gates || !out) return MOK_ERR_INVALID_ARG;
+    return cuda_status(launch_combine(dm, static_cast<const uint16_t *>(ystage), gates,
+                                      static_cast<uint16_t *>(out), static_cast<cudaStream_t>(stream)));
+}
+
+int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float *W_r,
+                    const float *bias, const mok_weights *w, void *out, void *saved_ctx, void *ws,
+                    void *stream)
+{
+    Dims dm;
+    int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!W_r || !w || !out || !ws) return MOK_ERR_INVALID_ARG;
+    const bool mx = dm.dtype == MOK_MXFP8;
+    if (mx && (!w->q_gate || !w->q_up || !w->q_down || !w->s_gate || !w->s_up || !w->s_down))
+        return MOK_ERR_INVALID_ARG;
+    if (!mx && (!w->w_gate || !w->w_up || !w->w_down)) return MOK_ERR_INVALID_ARG;
+    Sources src;
+    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    FwdWs fw;
+    fwd_ws_layout(dm, &fw);
+    mok_ctx_layout c;
+    ctx_layout(dm, &c);
+    void *rbase = saved_ctx ? saved_ctx : at<void>(ws, fw.route);
+    RouteOut o = route_in(rbase, c);
+    uint16_t *ystage = saved_ctx ? at<uint16_t>(saved_ctx, c.ystage) : at<uint16_t>(ws, fw.ystage);
+    uint32_t *status = at<uint32_t>(ws, fw.status);
+    cudaError_t e = cudaMemsetAsync(status, 0, 4, st);
+    if (e != cudaSuccess) return MOK_ERR_CUDA;
+    rc = route_layout_impl(cfg, dm, src, W_r, bias, o, ws, st);
+    if (rc != MOK_OK) return rc;
+    e = launch_dispatch(dm, src, o.ids, o.offsets, o.pad_offsets, o.row_tok, o.row_j,
+                        at<void>(ws, fw.xe), mx ? at<uint32_t>(ws, fw.xe_scales) : nullptr, st);
+    if (e == cudaSuccess)
+        e = launch_ffn(dm, at<void>(ws, fw.xe), mx ? at<uint32_t>(ws, fw.xe_scales) : nullptr, w,
+                       o.counts, o.offsets, o.pad_offsets, o.row_tok, o.row_j, at<void>(ws, fw.h),
+                       mx ? at<uint32_t>(ws, fw.h_scales) : nullptr, ystage,
+                       saved_ctx ? at<uint16_t>(saved_ctx, c.a) : nullptr,
+                       saved_ctx ? at<uint16_t>(saved_ctx, c.b) : nullptr,
+                       saved_ctx ? at<uint16_t>(saved_ctx, c.h) : nullptr, status,
+                       wait_ns(cfg), st);
+    if (e == cudaSuccess) e = launch_combine(dm, ystage, o.gates, static_cast<uint16_t *>(out), st);
+    return cuda_status(e);
+}
+
+int mok_moe_backward(const mok_config *cfg, const void *const *x_src, const float *W_r,
+                     const void *saved_ctx, const void *dY, const mok_weights *w, void *dX,
+                     mok_weight_grads *dw, float *dgates, float *dlogits, float *dW_r, void *ws,
+                     void *stream)
+{
+    (void)x_src; (void)W_r; (void)saved_ctx; (void)dY; (void)w; (void)dX; (void)dw;
+    (void)dgates; (void)dlogits; (void)dW_r; (void)ws; (void)stream;
+    Dims dm;
+    const int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    return MOK_ERR_UNSUPPORTED;
+}
+
+int mok_quantize_mx(const void *src, int64_t batch, int64_t rows, int64_t K, int transpose,
+                    uint8_t *codes, uint32_t *scales, void *stream)
+{
+    if (!src || !codes || !scales || batch < 1 || rows < 1 || K < 1) return MOK_ERR_INVALID_ARG;
+    if (rows % 128 != 0 || K % 128 != 0) return MOK_ERR_UNSUPPORTED;
+    if (transpose != 0 && transpose != 1) return MOK_ERR_INVALID_ARG;
+    return cuda_status(launch_quant_mx(static_cast<const uint16_t *>(src), batch, rows, K, transpose,
+                                       codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int mok_reset_device_status(void *ws, void *stream)
+{
+    if (!ws) return MOK_ERR_INVALID_ARG;
+    return cuda_status(cudaMemsetAsync(ws, 0, 4, static_cast<cudaStream_t>(stream)));
+}
+
+int mok_get_device_status(const void *ws, void *stream)
+{
+    if (!ws) return MOK_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t v = 0;
+    if (cudaMemcpyAsync(&v, ws, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOK_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOK_ERR_CUDA;
+    return static_cast<int>(v);
+}
+
+const char *mok_status_string(int status)
+{
+    switch (status) {
+    case MOK_OK: return "MOK_OK";
+    case MOK_ERR_INVALID_ARG: return "MOK_ERR_INVALID_ARG";
+    case MOK_ERR_UNSUPPORTED: return "MOK_ERR_UNSUPPORTED";
+    case MOK_ERR_CUDA: return "MOK_ERR_CUDA";
+    case MOK_ERR_TIMEOUT: return "MOK_ERR_TIMEOUT";
+    default: return "MOK_ERR_UNKNOWN";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,91 @@
+// mok_internal.h -- declarations shared by the library's translation units:
+// the source-buffer table, workspace carving and kernel launchers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mok.h"
+
+namespace mok {
+
+// Largest source count the per-source tensor-map table of the router GEMM
+// carries in its kernel parameters (64 maps = 8 KB of parameters).
+constexpr int kMaxRouterSources = 64;
+
+// Token t lives in source s = the last s with row_start[s] <= t, at row
+// t - row_start[s].
+struct Sources {
+    const uint16_t *ptr[MOK_MAX_SOURCES];
+    int row_start[MOK_MAX_SOURCES + 1];
+    int n;
+};
+
+__host__ __device__ inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+
+// Byte layout of the forward workspace (all offsets 256-aligned).
+struct FwdWs {
+    size_t status;          // uint32 status word
+    size_t chunk_counts;    // int32 [nchunks, E]
+    size_t chunk_base;      // int32 [nchunks, E]
+    size_t w3;              // BF16 [E_pad, 3d]: router weights split hi/mid/lo
+    size_t route;           // start of the route outputs block (when no saved ctx)
+    size_t xe, xe_scales;   // expert-ordered activations (padded rows)
+    size_t h, h_scales;     // SwiGLU output (padded rows)
+    size_t ystage;          // BF16 [T, k, d] (when no saved ctx)
+    size_t total;
+};
+
+struct Dims {
+    int T, d, E, k, F;
+    int router, dtype;
+    int64_t S;              // T * k
+    int64_t rows_pad;       // padded expert-ordered rows bound
+    int E_pad;              // E rounded up to 128 (router GEMM N)
+    int nchunks;            // layout chunks of kLayoutChunk slots
+};
+
+constexpr int kLayoutChunk = 1024;
+
+int check_config(const mok_config *cfg, Dims *dm);
+void fwd_ws_layout(const Dims &dm, FwdWs *w);
+void ctx_layout(const Dims &dm, mok_ctx_layout *c);
+int make_sources(const mok_config *cfg, const Dims &dm, const void *const *x_src, Sources *s);
+
+// ---- launchers (return cudaSuccess or the launch error) ----
+cudaError_t launch_router_split(const float *Wr, int E, int E_pad, int d, uint16_t *w3,
+                                cudaStream_t st);
+cudaError_t launch_router_gemm(const Dims &dm, const Sources &src, const uint16_t *w3,
+                               const float *bias, float *logits, uint32_t *status,
+                               uint64_t wait_ns, cudaStream_t st);
+cudaError_t launch_topk(const Dims &dm, const float *logits, int32_t *ids, float *gates,
+                        float *sel_scores, cudaStream_t st);
+cudaError_t launch_layout(const Dims &dm, const int32_t *ids, int32_t *counts, int32_t *offsets,
+                          int32_t *pad_offsets, int32_t *slot_pos, int32_t *row_tok,
+                          uint8_t *row_j, int32_t *chunk_counts, int32_t *chunk_base,
+                          cudaStream_t st);
+cudaError_t launch_counts_from_offsets(const int32_t *offsets, int E, int32_t *counts,
+                                       cudaStream_t st);
+cudaError_t launch_dispatch(const Dims &dm, const Sources &src, const int32_t *ids,
+                            const int32_t *offsets, const int32_t *pad_offsets,
+                            const int32_t *row_tok, const uint8_t *row_j, void *xe,
+                            uint32_t *xe_scales, cudaStream_t st);
+cudaError_t launch_combine(const Dims &dm, const uint16_t *ystage, const float *gates,
+                           uint16_t *out, cudaStream_t st);
+cudaError_t launch_quant_mx(const uint16_t *src, int64_t batch, int64_t rows, int64_t K,
+                            int transpose, uint8_t *codes, uint32_t *scales, cudaStream_t st);
+cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales,
+                       const mok_weights *w, const int32_t *counts, const int32_t *offsets,
+                       const int32_t *pad_offsets, const int32_t *row_tok,
+                       const uint8_t *row_j, void *h, uint32_t *h_scales, uint16_t *ystage,
+                       uint16_t *saved_a, uint16_t *saved_b, uint16_t *saved_h,
+                       uint32_t *status, uint64_t wait_ns, cudaStream_t st);
+
+int num_sms();
+// Encodes a 2-D tiled tensor map with 128-byte swizzle; returns 0 on success.
+int encode_tmap_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner_elems,
+                   uint64_t rows, uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace mok

@@ -1,0 +1,258 @@
+// mok_move.cu -- HBM-bound row movement: A3 pull dispatch (with fused MXFP8
+// quantisation), A6 final weighted combine, and the MXFP8 quantiser.
+//
+// [kucoin] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+// NVL72" (kucoin.com flash, Arabic).  §02: dispatch is a pull -- the expert
+// side reads each token it needs from (source, position in source) and places
+// it in its own expert order; MXFP8 activation quantisation is fused into
+// dispatch so no separate quantise pass touches HBM.  §03: the measured layer
+// ends with the final weighted combine.
+//
+// All kernels move 16-byte vectors per lane with rows spread over warps; a
+// warp owns whole rows so reads and writes are fully coalesced.
+#include <cuda_bf16.h>
+
+#include "mok_internal.h"
+#include "mok_ptx.cuh"
+
+namespace mok {
+
+// Word index of (k-group g, row r) in the MX scale tile layout of a matrix
+// with `rows` rows (see mok.h).
+__device__ __forceinline__ int64_t mx_word_index(int64_t g, int64_t r, int64_t rows)
+{
+    return (g * (rows >> 7) + (r >> 7)) * 128 + (r & 31) * 4 + ((r & 127) >> 5);
+}
+
+__device__ __forceinline__ const uint16_t *source_row(const Sources &src, int t, int d)
+{
+    int lo = 0, hi = src.n;  // last s with row_start[s] <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (src.row_start[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    return src.ptr[lo] + static_cast<int64_t>(t - src.row_start[lo]) * d;
+}
+
+// One warp quantises one 256-element stretch of a row: lane l converts
+// elements [8l, 8l+8), lanes 4b..4b+3 share MX block b, the amax is reduced
+// over those four lanes, and lanes 0 and 16 write the scale words of the two
+// 128-wide k-groups.  A 128-element tail passes nvalid = 16: every lane takes
+// part in the shuffles, lanes 16..31 write nothing.
+__device__ __forceinline__ void mx_quant_stretch(const uint4 raw, int lane, int nvalid,
+                                                 uint8_t *codes_row, int64_t col0,
+                                                 uint32_t *scales, int64_t scale_row,
+                                                 int64_t scale_rows)
+{
+    float f[8];
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+        f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int x = mx_scale_exp(amax);
+    const float inv = mx_inv_scale(x);
+    uint2 out;
+    out.x = pack_e4m3x2(f[0] * inv, f[1] * inv) | (pack_e4m3x2(f[2] * inv, f[3] * inv) << 16);
+    out.y = pack_e4m3x2(f[4] * inv, f[5] * inv) | (pack_e4m3x2(f[6] * inv, f[7] * inv) << 16);
+    if (lane < nvalid) *reinterpret_cast<uint2 *>(codes_row + col0 + 8 * lane) = out;
+    // scale byte of block (lane/4) sits at byte (lane/4) % 4 of its k-group word
+    uint32_t word = static_cast<uint32_t>(x + 127) << (8 * ((lane >> 2) & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    word |= __shfl_xor_sync(0xffffffffu, word, 8);
+    if ((lane & 15) == 0 && lane < nvalid) {
+        const int64_t g = (col0 + 8 * lane) >> 7;
+        scales[mx_word_index(g, scale_row, scale_rows)] = word;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// A3 dispatch.  Dense layout row p holds slot (t = row_tok[p], j = row_j[p]) of
+// expert e = ids[t*k+j]; it is written to padded row pad_offsets[e] + p -
+// offsets[e].  One warp per row, grid-stride over rows.
+// ---------------------------------------------------------------------------
+template <bool MX>
+__global__ void __launch_bounds__(256) k_dispatch(const Sources src, int64_t S, int d, int k,
+                                                  const int32_t *__restrict__ ids,
+                                                  const int32_t *__restrict__ offsets,
+                                                  const int32_t *__restrict__ pad_offsets,
+                                                  const int32_t *__restrict__ row_tok,
+                                                  const uint8_t *__restrict__ row_j, void *xe,
+                                                  uint32_t *__restrict__ xe_scales,
+                                                  int64_t rows_pad)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t p = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); p < S;
+         p += warps) {
+        const int t = row_tok[p];
+        const int e = ids[static_cast<int64_t>(t) * k + row_j[p]];
+        const int64_t q = pad_offsets[e] + (p - offsets[e]);
+        const uint4 *in = reinterpret_cast<const uint4 *>(source_row(src, t, d));
+        if (!MX) {
+            uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xe) + q * d);
+            for (int c = lane; c < d / 8; c += 32) out[c] = __ldg(in + c);
+        } else {
+            uint8_t *codes_row = static_cast<uint8_t *>(xe) + q * d;
+            for (int c0 = 0; c0 < d; c0 += 256) {
+                const int nvalid = d - c0 >= 256 ? 32 : 16;
+                const uint4 raw = lane < nvalid ? __ldg(in + (c0 >> 3) + lane) : make_uint4(0, 0, 0, 0);
+                mx_quant_stretch(raw, lane, nvalid, codes_row, c0, xe_scales, q, rows_pad);
+            }
+        }
+    }
+}
+
+cudaError_t launch_dispatch(const Dims &dm, const Sources &src, const int32_t *ids,
+                            const int32_t *offsets, const int32_t *pad_offsets,
+                            const int32_t *row_tok, const uint8_t *row_j, void *xe,
+                            uint32_t *xe_scales, cudaStream_t st)
+{
+    const int threads = 256;
+    const int64_t need = (dm.S + 7) / 8;
+    const int blocks = static_cast<int>(need < 32 * num_sms() ? need : 32 * num_sms());
+    if (dm.dtype == MOK_MXFP8)
+        k_dispatch<true><<<blocks, threads, 0, st>>>(src, dm.S, dm.d, dm.k, ids, offsets,
+                                                     pad_offsets, row_tok, row_j, xe, xe_scales,
+                                                     dm.rows_pad);
+    else
+        k_dispatch<false><<<blocks, threads, 0, st>>>(src, dm.S, dm.d, dm.k, ids, offsets,
+                                                      pad_offsets, row_tok, row_j, xe, xe_scales,
+                                                      dm.rows_pad);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// A6 combine: out[t, c] = bf16( fold_j fmaf(g_tj, y_tj[c], acc) ), acc from 0,
+// j = 0..k-1 in order.  One thread per 8 columns of one token.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ ystage,
+                                                 const float *__restrict__ gates, int T, int k,
+                                                 int d, uint16_t *__restrict__ out)
+{
+    const int64_t vec_per_tok = d / 8;
+    const int64_t n = static_cast<int64_t>(T) * vec_per_tok;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / vec_per_tok;
+        const int64_t c = i % vec_per_tok;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const float g = __ldg(gates + t * k + j);
+            const uint4 y = __ldg(reinterpret_cast<const uint4 *>(ystage + (t * k + j) * d) + c);
+            const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[2 * q] = fmaf(g, bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
+                acc[2 * q + 1] = fmaf(g, bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
+            }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4 *>(out + t * d)[c] = o;
+    }
+}
+
+cudaError_t launch_combine(const Dims &dm, const uint16_t *ystage, const float *gates,
+                           uint16_t *out, cudaStream_t st)
+{
+    const int64_t n = static_cast<int64_t>(dm.T) * (dm.d / 8);
+    const int threads = 256;
+    const int64_t need = (n + threads - 1) / threads;
+    const int blocks = static_cast<int>(need < 64 * num_sms() ? need : 64 * num_sms());
+    k_combine<<<blocks, threads, 0, st>>>(ystage, gates, dm.T, dm.k, dm.d, out);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 quantiser of BF16 matrices (weights and backward operands).
+// transpose = 0: rows of [rows, K] along K; one warp per row.
+// transpose = 1: the transpose [K, rows] along rows; a 256 x 32 tile of the
+// source goes through shared memory so that reads and writes stay coalesced.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_quant_rows(const uint16_t *__restrict__ src, int64_t R,
+                                                    int64_t K, uint8_t *__restrict__ codes,
+                                                    uint32_t *__restrict__ scales)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t r = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); r < R;
+         r += warps) {
+        const uint4 *in = reinterpret_cast<const uint4 *>(src + r * K);
+        for (int64_t c0 = 0; c0 < K; c0 += 256) {
+            const int nvalid = K - c0 >= 256 ? 32 : 16;
+            const uint4 raw = lane < nvalid ? __ldg(in + (c0 >> 3) + lane) : make_uint4(0, 0, 0, 0);
+            mx_quant_stretch(raw, lane, nvalid, codes + r * K, c0, scales, r, R);
+        }
+    }
+}
+
+// Source matrix b: [rows, K] BF16 at src + b*rows*K; output row (b*K + c) is
+// source column c, quantised along the source rows.
+__global__ void __launch_bounds__(256) k_quant_cols(const uint16_t *__restrict__ src, int64_t rows,
+                                                    int64_t K, uint8_t *__restrict__ codes,
+                                                    uint32_t *__restrict__ scales, int64_t R_out)
+{
+    __shared__ uint16_t tile[32][256 + 8];
+    const int64_t b = blockIdx.z;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 32;   // source columns -> output rows
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 256;  // source rows -> output columns
+    const uint16_t *s = src + b * rows * K;
+    // load 256 source rows x 32 columns: each thread reads 8 columns (16 bytes)
+    const int64_t nrows = rows - r0 < 256 ? rows - r0 : 256;
+    for (int i = threadIdx.x; i < 256 * 4; i += blockDim.x) {
+        const int rr = i >> 2, cc = (i & 3) * 8;
+        const uint4 v = rr < nrows
+                            ? __ldg(reinterpret_cast<const uint4 *>(s + (r0 + rr) * K + c0 + cc))
+                            : make_uint4(0, 0, 0, 0);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            tile[cc + 2 * q][rr] = static_cast<uint16_t>(w[q] & 0xFFFFu);
+            tile[cc + 2 * q + 1][rr] = static_cast<uint16_t>(w[q] >> 16);
+        }
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int oc = warp; oc < 32; oc += blockDim.x >> 5) {
+        const int64_t orow = b * K + c0 + oc;
+        uint4 raw;
+        const uint16_t *t = &tile[oc][8 * lane];
+        raw.x = t[0] | (static_cast<uint32_t>(t[1]) << 16);
+        raw.y = t[2] | (static_cast<uint32_t>(t[3]) << 16);
+        raw.z = t[4] | (static_cast<uint32_t>(t[5]) << 16);
+        raw.w = t[6] | (static_cast<uint32_t>(t[7]) << 16);
+        mx_quant_stretch(raw, lane, nrows >= 256 ? 32 : 16, codes + orow * rows, r0, scales, orow,
+                         R_out);
+    }
+}
+
+cudaError_t launch_quant_mx(const uint16_t *src, int64_t batch, int64_t rows, int64_t K,
+                            int transpose, uint8_t *codes, uint32_t *scales, cudaStream_t st)
+{
+    if (!transpose) {
+        const int64_t R = batch * rows;
+        const int64_t need = (R + 7) / 8;
+        const int blocks = static_cast<int>(need < 32 * num_sms() ? need : 32 * num_sms());
+        k_quant_rows<<<blocks, 256, 0, st>>>(src, R, K, codes, scales);
+    } else {
+        dim3 grid(static_cast<unsigned>(K / 32), static_cast<unsigned>((rows + 255) / 256),
+                  static_cast<unsigned>(batch));
+        k_quant_cols<<<grid, 256, 0, st>>>(src, rows, K, codes, scales, batch * K);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mok

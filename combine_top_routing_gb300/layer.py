@@ -1,0 +1,74 @@
+"""A convenience owner of the device buffers one MoE layer call needs.
+
+The library never allocates; this class allocates the caller-side buffers
+(workspace, saved context, outputs, MXFP8 weight copies) with torch and
+calls the C ABI through ``mok``.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import mok
+from .inputs import Workload, split_sources
+
+
+def scale_words(rows: int, K: int) -> int:
+    """32-bit words of an MX scale tile-layout buffer for a [rows, K] matrix."""
+    return rows * K // 128
+
+
+class MoELayer:
+    def __init__(self, w: Workload, inputs: dict, *, training: bool = False, device="cuda",
+                 **cfg_kw):
+        self.w = w
+        self.cfg = mok.Config.from_workload(w, **cfg_kw)
+        self.device = torch.device(device)
+        fwd, ctx, bwd = mok.workspace_size(self.cfg)
+        self.ws = torch.empty(fwd, dtype=torch.uint8, device=self.device)
+        self.ctx = torch.empty(ctx, dtype=torch.uint8, device=self.device) if training else None
+        self.ctx_layout = mok.saved_ctx_layout(self.cfg)
+        self.rows_pad = mok.max_padded_rows(self.cfg)
+        x = inputs["x"]
+        self.x = x
+        self.x_src = split_sources(x, w.n_sources) if w.n_sources > 1 else [x]
+        self.W_r = inputs["Wr"]
+        self.bias = inputs.get("bias")
+        self.weights = {"w_gate": inputs["Wg"], "w_up": inputs["Wu"], "w_down": inputs["Wd"]}
+        if w.dtype == "mxfp8":
+            self.quantize_weights()
+        self.wstruct = mok.weights_struct(self.weights)
+        self.out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=self.device)
+
+    def quantize_weights(self, transposed: bool = False, stream=None):
+        w, E, F, d = self.w, self.w.E, self.w.F, self.w.d
+        dev = self.device
+        q = self.weights
+        for name, src, rows, K in (("gate", q["w_gate"], F, d), ("up", q["w_up"], F, d),
+                                   ("down", q["w_down"], d, F)):
+            codes = torch.empty((E, rows, K), dtype=torch.uint8, device=dev)
+            scales = torch.empty(scale_words(E * rows, K), dtype=torch.int32, device=dev)
+            mok.quantize_mx(src, E, rows, K, 0, codes, scales, stream)
+            q["q_" + name], q["s_" + name] = codes, scales
+            if transposed:
+                codes_t = torch.empty((E, K, rows), dtype=torch.uint8, device=dev)
+                scales_t = torch.empty(scale_words(E * K, rows), dtype=torch.int32, device=dev)
+                mok.quantize_mx(src, E, rows, K, 1, codes_t, scales_t, stream)
+                q["qt_" + name], q["st_" + name] = codes_t, scales_t
+        self.wstruct = mok.weights_struct(q)
+
+    def forward(self, stream=None):
+        mok.moe_forward(self.cfg, self.x_src, self.W_r, self.bias, self.wstruct, self.out,
+                        self.ctx, self.ws, stream)
+        return self.out
+
+    def status(self, stream=None) -> int:
+        return mok.get_device_status(self.ws, stream)
+
+    # -- views into the saved context (training) ------------------------------
+    def ctx_view(self, field: str, dtype, shape):
+        off = getattr(self.ctx_layout, field)
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.tensor([], dtype=dtype).element_size()
+        return self.ctx[off:off + nbytes].view(dtype).view(shape)

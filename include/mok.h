@@ -1,0 +1,247 @@
+/*
+ * mok.h -- C ABI of libmok.so: one Mixture-of-Experts layer, forward and
+ * backward, on one GB300 (sm_103a).
+ *
+ * What the layer computes follows three news pages on Cursor's
+ * "Mixture-of-Kittens" (MoK) MoE kernel; they give prose, not formulas:
+ *   [kucoin] "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+ *            NVL72" (kucoin.com flash, Arabic), sections 01, 02, 03;
+ *   [miku]   "Mixture of kittens: how Cursor opened a kernel that speeds up
+ *            AI training by up to 2.4x" (miku-ai.ru);
+ *   [qvib]   "Mixture-of-Kittens (MoK) open source" (qvib.pro news).
+ * [kucoin] §03 names the steps of the measured layer: routing, the expert
+ * FFN, combine and the final weighted combine; §01 adds per-expert counts and
+ * placement (layout) before the grouped GEMM; §02 gives pull dispatch / push
+ * combine (and the reverse pair in backward) and MXFP8 quantisation fused into
+ * dispatch, the grouped GEMM and SwiGLU.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are caller-owned device memory; pointers marked
+ *     "host" are read before the call returns.  The library never allocates,
+ *     never frees and never synchronises the host inside a call: work is
+ *     enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *   - Return value: MOK_OK, or a host-detectable error code (nothing was
+ *     enqueued).  Errors found on the device (a bounded wait that ran out)
+ *     land in the status word of the workspace; read them with
+ *     mok_get_device_status.
+ *   - Notation: T tokens, d = d_model, E experts, k = top_k, F = d_ff,
+ *     S = T*k slots.  BF16 values are stored as raw 16-bit patterns.
+ *   - Expert-ordered row buffers (xe, h, saved a/b/h, dy/dx rows) use the
+ *     PADDED layout: expert e owns rows [pad_offsets[e], pad_offsets[e] +
+ *     counts[e]) and pad_offsets[e+1] - pad_offsets[e] = counts[e] rounded up
+ *     to MOK_ROW_ALIGN; the rows in between are padding with unspecified
+ *     contents.  A buffer of mok_max_padded_rows(cfg) rows always suffices.
+ *   - MXFP8 tensors are E4M3 codes (one byte each, row-major [rows, K]) plus
+ *     E8M0 scales (one byte per 32 consecutive elements along K) in the MX
+ *     SCALE TILE LAYOUT: for rows a multiple of 128 and K a multiple of 128,
+ *     the 32-bit word of (k-group g = K/128 index, row r) sits at word index
+ *        (g * rows/128 + r/128) * 128 + (r % 32) * 4 + (r % 128) / 32
+ *     and its byte b (0..3, little-endian) is the scale of K-block 4g + b.
+ *     Total size rows * K / 32 bytes.
+ */
+#ifndef MOK_H
+#define MOK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MOK_OK = 0,
+    MOK_ERR_INVALID_ARG = 1,   /* null pointer, size out of range, bad enum */
+    MOK_ERR_UNSUPPORTED = 2,   /* shape the kernels do not handle (see mok_config) */
+    MOK_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+    MOK_ERR_TIMEOUT = 4        /* device: a bounded wait gave up */
+};
+
+enum { MOK_ROUTER_SOFTMAX = 0, MOK_ROUTER_SIGMOID = 1 };
+enum { MOK_BF16 = 0, MOK_MXFP8 = 1 };
+
+#define MOK_ROW_ALIGN 128      /* expert segment alignment of row buffers */
+#define MOK_MAX_SOURCES 64     /* simulated expert-parallel source buffers */
+#define MOK_MAX_EXPERTS 1024
+#define MOK_MAX_TOPK 8
+
+/*
+ * Layer configuration.  Supported: 1 <= T, 1 <= E <= MOK_MAX_EXPERTS,
+ * 1 <= k <= min(E, MOK_MAX_TOPK), d and F multiples of 128 (the MXFP8 block
+ * of 32 and the 128-wide tiles), S + 128 E < 2^31, and for n_sources > 1 every
+ * source_rows[s] a multiple of 128 (one router row tile never spans two
+ * sources).  Anything else returns MOK_ERR_UNSUPPORTED.
+ */
+typedef struct {
+    int T, d_model, n_experts, top_k, d_ff;
+    int router;                    /* MOK_ROUTER_SOFTMAX | MOK_ROUTER_SIGMOID */
+    int dtype;                     /* MOK_BF16 | MOK_MXFP8 (expert GEMM operands) */
+    int n_sources;                 /* 1: x is one [T,d] buffer; >1: token t lives in
+                                      source s at row r, sources in token order */
+    const int *source_rows;        /* host [n_sources] rows per source (NULL if 1) */
+    int minibatch_rows;            /* rows per hand-off chunk of the fused forward:
+                                      64 | 128 | 256 (0 = 128) */
+    float gather_sm_fraction;      /* SMs given to the gather/combine role in the
+                                      fused forward (0 = automatic) */
+    size_t ring_bytes;             /* token ring of the fused forward (0 = no cap) */
+    unsigned long long wait_limit_ns; /* device spin give-up (0 = 2 s) */
+} mok_config;
+
+/* Expert weights.  Masters are BF16; the MXFP8 copies are made by
+ * mok_quantize_mx from the masters (forward blocking along each forward
+ * GEMM's K; "_t" copies are the transposes blocked along the backward dgrad
+ * GEMMs' K).  Unused members may be NULL. */
+typedef struct {
+    const void *w_gate;            /* device BF16 [E, F, d] */
+    const void *w_up;              /* device BF16 [E, F, d] */
+    const void *w_down;            /* device BF16 [E, d, F] */
+    const uint8_t *q_gate, *q_up, *q_down;     /* device E4M3, same shapes */
+    const uint32_t *s_gate, *s_up, *s_down;    /* device scales, tile layout */
+    const uint8_t *qt_gate, *qt_up;            /* device E4M3 [E, d, F] (W_g^T, W_u^T) */
+    const uint8_t *qt_down;                    /* device E4M3 [E, F, d] (W_d^T) */
+    const uint32_t *st_gate, *st_up, *st_down; /* device scales of the transposes */
+} mok_weights;
+
+typedef struct {
+    void *d_gate;                  /* device BF16 [E, F, d] */
+    void *d_up;                    /* device BF16 [E, F, d] */
+    void *d_down;                  /* device BF16 [E, d, F] */
+} mok_weight_grads;
+
+/* Byte offsets of the fields of the forward's saved context (for backward and
+ * for inspection).  All offsets are 256-byte aligned. */
+typedef struct {
+    size_t ids, gates, sel_scores, counts, offsets, pad_offsets, slot_pos,
+           row_tok, row_j, logits, a, b, h, ystage, total;
+} mok_ctx_layout;
+
+/* Upper bound on padded expert-ordered rows: S + E*(MOK_ROW_ALIGN-1),
+ * rounded up to MOK_ROW_ALIGN.  Returns 0 on a bad config. */
+int64_t mok_max_padded_rows(const mok_config *cfg);
+
+/* Workspace sizes in bytes: fwd_ws for mok_moe_forward and the step calls,
+ * saved_ctx for the forward's saved context, bwd_ws for mok_moe_backward.
+ * Any output pointer may be NULL. */
+int mok_workspace_size(const mok_config *cfg, size_t *fwd_ws, size_t *saved_ctx,
+                       size_t *bwd_ws);
+
+/* Offsets of the saved-context fields for this config. */
+int mok_saved_ctx_layout(const mok_config *cfg, mok_ctx_layout *out);
+
+/*
+ * A1 + A2: router top-k and layout ([kucoin] §01: the router decides each
+ * token's experts at every step; the layout counts tokens per expert and
+ * places one expert's tokens together for the grouped GEMM).
+ *   logits = x W_r^T (+ bias); scores = softmax over E (MOK_ROUTER_SOFTMAX)
+ *   or sigmoid; top-k by logit, ties to the lower expert id, slot j = 0 the
+ *   largest; gates = chosen scores / their sum.  Layout = stable counting
+ *   sort of slot t*k+j by expert.
+ * x_src      host array [n_sources] of device BF16 [source_rows[s], d]
+ * W_r        device fp32 [E, d];  bias device fp32 [E] or NULL
+ * ids        device int32 [T, k];   gates device fp32 [T, k]
+ * sel_scores device fp32 [T, k] chosen scores (softmax or sigmoid), or NULL
+ * logits     device fp32 [T, E] or NULL
+ * counts     device int32 [E];  offsets, pad_offsets device int32 [E+1]
+ * slot_pos   device int32 [T, k] dense row of slot (t, j)
+ * row_tok    device int32 [S];  row_j device uint8 [S]  (dense rows)
+ * ws         device workspace of at least fwd_ws bytes
+ */
+int mok_route_layout(const mok_config *cfg, const void *const *x_src, const float *W_r,
+                     const float *bias, int32_t *ids, float *gates, float *sel_scores,
+                     float *logits, int32_t *counts, int32_t *offsets,
+                     int32_t *pad_offsets, int32_t *slot_pos, int32_t *row_tok,
+                     uint8_t *row_j, void *ws, void *stream);
+
+/*
+ * A3: pull dispatch ([kucoin] §02: the expert side reads the tokens it needs
+ * by (source, position in source) and lays them out in its own expert order;
+ * MXFP8 quantisation fused into dispatch).  Row pad_offsets[e] + i of xe is
+ * token row_tok[offsets[e] + i].  BF16: xe is BF16 [rows, d].  MXFP8: xe is
+ * E4M3 [rows, d] and xe_scales the tile-layout scales (rows =
+ * mok_max_padded_rows).  ids/offsets/pad_offsets/row_tok as produced by
+ * mok_route_layout.
+ */
+int mok_dispatch(const mok_config *cfg, const void *const *x_src, const int32_t *ids,
+                 const int32_t *offsets, const int32_t *pad_offsets,
+                 const int32_t *row_tok, const uint8_t *row_j, void *xe,
+                 uint32_t *xe_scales, void *stream);
+
+/*
+ * A4 + A5: per-expert SwiGLU FFN as grouped GEMMs on the tensor cores
+ * ([kucoin] §01: grouped GEMM over organised input; §02: MXFP8 fused into
+ * the grouped GEMM and SwiGLU; push combine: each result goes straight to
+ * its token).  a = xe W_g^T, b = xe W_u^T (fp32 accumulate), h = silu(a) b
+ * stored as BF16 (BF16) or MXFP8 along F (MXFP8), y = h W_d^T stored as
+ * BF16 into ystage[row_tok[p], row_j[p]].
+ * ystage   device BF16 [T, k, d]
+ * saved_a, saved_b, saved_h  device BF16 [rows, F] (padded layout) or NULL
+ * ws       device workspace (fwd_ws bytes) holding h
+ */
+int mok_expert_ffn(const mok_config *cfg, const void *xe, const uint32_t *xe_scales,
+                   const mok_weights *w, const int32_t *offsets,
+                   const int32_t *pad_offsets, const int32_t *row_tok,
+                   const uint8_t *row_j, void *ystage, void *saved_a, void *saved_b,
+                   void *saved_h, void *ws, void *stream);
+
+/*
+ * A6: final weighted combine ([kucoin] §03).  out[t] = BF16 of the fp32
+ * fused multiply-add fold over j = 0..k-1 of gates[t,j] * ystage[t,j],
+ * starting from 0 -- a fixed order, so results are bit-reproducible.
+ * ystage device BF16 [T,k,d]; gates device fp32 [T,k]; out device BF16 [T,d].
+ */
+int mok_combine(const mok_config *cfg, const void *ystage, const float *gates,
+                void *out, void *stream);
+
+/*
+ * The whole forward layer: route_layout, dispatch, expert FFN and combine,
+ * enqueued back to back on one stream with no host round trip.
+ * saved_ctx: device buffer of saved_ctx bytes (training) or NULL (inference).
+ */
+int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float *W_r,
+                    const float *bias, const mok_weights *w, void *out, void *saved_ctx,
+                    void *ws, void *stream);
+
+/*
+ * Backward of mok_moe_forward ([kucoin] §01: backward runs two more rounds
+ * of communication in reverse; §02: pull reverse-combine, push
+ * reverse-dispatch).  Gradients of L = <dY, out>:
+ *   dy_slot = g dY[t] (BF16), dgates = <dY[t], y_tj>; dh = dy W_d; SwiGLU
+ *   backward with the saved a, b; dx_slot = da W_g + db W_u; dW_d = dy^T h,
+ *   dW_g = da^T xe, dW_u = db^T xe per expert (BF16); dlogits through the
+ *   renormalised top-k gates; dW_r = dlogits^T x; dX = sum_j dx_slot +
+ *   dlogits W_r (BF16).
+ * dY device BF16 [T,d]; dX device BF16 [T,d]; dgates device fp32 [T,k];
+ * dlogits device fp32 [T,E] or NULL; dW_r device fp32 [E,d].
+ */
+int mok_moe_backward(const mok_config *cfg, const void *const *x_src, const float *W_r,
+                     const void *saved_ctx, const void *dY, const mok_weights *w,
+                     void *dX, mok_weight_grads *dw, float *dgates, float *dlogits,
+                     float *dW_r, void *ws, void *stream);
+
+/*
+ * MXFP8 quantiser (OCP MX v1.0: scale X = clamp(floor(log2 amax) - 8, -127,
+ * 127), E8M0 byte X + 127, elements E4M3 round-to-nearest-even of v / 2^X,
+ * saturating at +-448).  src is `batch` BF16 matrices [rows, K], rows and K
+ * multiples of 128.  transpose = 0: blocks run along K; codes [batch, rows, K],
+ * scales in tile layout for a matrix of batch*rows rows and K columns.
+ * transpose = 1: each matrix is transposed first; codes [batch, K, rows],
+ * scales for batch*K rows and `rows` columns.
+ */
+int mok_quantize_mx(const void *src, int64_t batch, int64_t rows, int64_t K,
+                    int transpose, uint8_t *codes, uint32_t *scales, void *stream);
+
+/* Clears the device status word of a workspace (enqueued on stream). */
+int mok_reset_device_status(void *ws, void *stream);
+
+/* Synchronises `stream` and returns the device status word of `ws`:
+ * MOK_OK or MOK_ERR_TIMEOUT (a bounded device wait gave up). */
+int mok_get_device_status(const void *ws, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *mok_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOK_H */

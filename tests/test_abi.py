@@ -1,0 +1,99 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/mok.h declares, and rejects bad configurations on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from combine_top_routing_gb300 import mok
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "mok.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mok_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_expected_entry_points():
+    names = _declared()
+    for want in ("mok_route_layout", "mok_dispatch", "mok_expert_ffn", "mok_combine",
+                 "mok_moe_forward", "mok_moe_backward", "mok_workspace_size",
+                 "mok_status_string", "mok_get_device_status"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = mok.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert set(_declared()) <= set(mok.EXPORTS)
+
+
+def _cfg(**kw):
+    base = dict(T=256, d_model=256, n_experts=8, top_k=2, d_ff=256, router=0, dtype=0)
+    base.update(kw)
+    return mok.Config(**base)
+
+
+def test_workspace_size_valid_and_monotone():
+    small = mok.workspace_size(_cfg())
+    big = mok.workspace_size(_cfg(T=4096))
+    assert all(s > 0 for s in small)
+    assert all(b > s for b, s in zip(big, small))
+    assert mok.max_padded_rows(_cfg()) == 512 + 8 * 128
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(T=0), mok.MOK_ERR_INVALID_ARG),
+    (dict(top_k=9, n_experts=16), mok.MOK_ERR_UNSUPPORTED),
+    (dict(top_k=4, n_experts=2), mok.MOK_ERR_UNSUPPORTED),
+    (dict(n_experts=2048), mok.MOK_ERR_UNSUPPORTED),
+    (dict(d_model=200), mok.MOK_ERR_UNSUPPORTED),
+    (dict(d_ff=100), mok.MOK_ERR_UNSUPPORTED),
+    (dict(router=5), mok.MOK_ERR_INVALID_ARG),
+    (dict(dtype=7), mok.MOK_ERR_INVALID_ARG),
+    (dict(minibatch_rows=100), mok.MOK_ERR_INVALID_ARG),
+    (dict(gather_sm_fraction=1.5), mok.MOK_ERR_INVALID_ARG),
+])
+def test_bad_configs_rejected_on_host(kw, code):
+    with pytest.raises(mok.MokError) as ei:
+        mok.workspace_size(_cfg(**kw))
+    assert ei.value.code == code
+
+
+def test_sources_must_cover_tokens_in_128_row_pieces():
+    with pytest.raises(mok.MokError) as ei:
+        mok.workspace_size(_cfg(T=512, n_sources=4, source_rows=[128, 128, 128, 256]))
+    assert ei.value.code == mok.MOK_ERR_INVALID_ARG
+    with pytest.raises(mok.MokError) as ei:
+        mok.workspace_size(_cfg(T=400, n_sources=2, source_rows=[200, 200]))
+    assert ei.value.code == mok.MOK_ERR_UNSUPPORTED
+    assert mok.workspace_size(_cfg(T=512, n_sources=4, source_rows=[128] * 4))[0] > 0
+
+
+def test_null_pointers_rejected_before_any_launch():
+    L = mok.lib()
+    cfg = _cfg()
+    rc = L.mok_combine(cfg.ref, None, None, None, None)
+    assert rc == mok.MOK_ERR_INVALID_ARG
+    rc = L.mok_quantize_mx(None, 1, 128, 128, 0, None, None, None)
+    assert rc == mok.MOK_ERR_INVALID_ARG
+    rc = L.mok_get_device_status(None, None)
+    assert rc == mok.MOK_ERR_INVALID_ARG
+
+
+def test_status_strings():
+    assert mok.status_string(0) == "MOK_OK"
+    assert mok.status_string(4) == "MOK_ERR_TIMEOUT"
+    assert mok.status_string(99) == "MOK_ERR_UNKNOWN"
+
+
+def test_saved_ctx_layout_is_aligned_and_ordered():
+    lay = mok.saved_ctx_layout(_cfg())
+    fields = [f for f, _ in mok.MokCtxLayout._fields_]
+    offs = [getattr(lay, f) for f in fields]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs)
