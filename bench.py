@@ -38,7 +38,19 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
+    p.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
+                   help="override a workload field (e.g. T=2048, E=32) for profiling runs")
     return p.parse_args()
+
+
+def _workload(args):
+    from combine_top_routing_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload]
+    over = {}
+    for item in args.set:
+        k, v = item.split("=", 1)
+        over[k] = type(getattr(w, k))(v)
+    return I.scaled(w, **over) if over else w
 
 
 def _dist():
@@ -140,7 +152,7 @@ def run_reference(args):
 
     from combine_top_routing_gb300 import inputs as I
     from oracle import oracle as O
-    w = I.WORKLOADS[args.workload]
+    w = _workload(args)
     inp = I.make_inputs(w, device="cpu")
     kind = O.SOFTMAX if w.router == "softmax" else O.SIGMOID
 
@@ -228,7 +240,7 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    w = I.WORKLOADS[args.workload]
+    w = _workload(args)
     inp = I.make_inputs(I.scaled(w, seed=w.seed + 1000 * rank), device="cuda")
     layer = MoELayer(w, inp)
     stream = torch.cuda.current_stream()

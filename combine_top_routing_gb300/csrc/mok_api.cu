@@ -56,7 +56,7 @@ int check_config(const mok_config *cfg, Dims *dm)
         dm->router = cfg->router;
         dm->dtype = cfg->dtype;
         dm->S = S;
-        dm->rows_pad = round_up(S + static_cast<int64_t>(E) * (MOK_ROW_ALIGN - 1), MOK_ROW_ALIGN);
+        dm->rows_pad = round_up(S + static_cast<int64_t>(E) * (MOK_ROW_ALIGN - 1), 256);
         dm->E_pad = static_cast<int>(round_up(E, 128));
         dm->nchunks = static_cast<int>((S + kLayoutChunk - 1) / kLayoutChunk);
     }
@@ -101,6 +101,37 @@ void fwd_ws_layout(const Dims &dm, FwdWs *w)
     w->h = take(&cur, static_cast<size_t>(dm.rows_pad) * dm.F * esize);
     w->h_scales = take(&cur, dm.dtype == MOK_MXFP8 ? static_cast<size_t>(dm.rows_pad) * dm.F / 32 : 0);
     w->ystage = take(&cur, static_cast<size_t>(dm.S) * dm.d * 2);
+    w->total = (cur + kAlign - 1) / kAlign * kAlign;
+}
+
+void bwd_ws_layout(const Dims &dm, BwdWs *w)
+{
+    size_t cur = 0;
+    const bool mx = dm.dtype == MOK_MXFP8;
+    const size_t R = static_cast<size_t>(dm.rows_pad), d = dm.d, F = dm.F;
+    const size_t esize = mx ? 1 : 2;
+    w->status = take(&cur, 256);
+    w->dy = take(&cur, R * d * 2);
+    w->dy_q = take(&cur, mx ? R * d : 0);
+    w->dy_s = take(&cur, mx ? R * d / 32 : 0);
+    w->da = take(&cur, R * F * 2);
+    w->db = take(&cur, R * F * 2);
+    w->da_q = take(&cur, mx ? R * F : 0);
+    w->db_q = take(&cur, mx ? R * F : 0);
+    w->da_s = take(&cur, mx ? R * F / 32 : 0);
+    w->db_s = take(&cur, mx ? R * F / 32 : 0);
+    w->dx = take(&cur, R * d * 2);
+    w->dyT = take(&cur, d * R * esize);
+    w->hT = take(&cur, F * R * esize);
+    w->daT = take(&cur, F * R * esize);
+    w->dbT = take(&cur, F * R * esize);
+    w->xT = take(&cur, d * R * esize);
+    w->dyT_s = take(&cur, mx ? d * R / 32 : 0);
+    w->hT_s = take(&cur, mx ? F * R / 32 : 0);
+    w->daT_s = take(&cur, mx ? F * R / 32 : 0);
+    w->dbT_s = take(&cur, mx ? F * R / 32 : 0);
+    w->xT_s = take(&cur, mx ? d * R / 32 : 0);
+    w->dl_sel = take(&cur, static_cast<size_t>(dm.S) * 4);
     w->total = (cur + kAlign - 1) / kAlign * kAlign;
 }
 
@@ -245,9 +276,11 @@ int mok_workspace_size(const mok_config *cfg, size_t *fwd_ws, size_t *saved_ctx,
     fwd_ws_layout(dm, &w);
     mok_ctx_layout c;
     ctx_layout(dm, &c);
+    BwdWs bw;
+    bwd_ws_layout(dm, &bw);
     if (fwd_ws) *fwd_ws = w.total;
     if (saved_ctx) *saved_ctx = c.total;
-    if (bwd_ws) *bwd_ws = w.total;
+    if (bwd_ws) *bwd_ws = bw.total;
     return MOK_OK;
 }
 
@@ -395,12 +428,101 @@ int mok_moe_backward(const mok_config *cfg, const void *const *x_src, const floa
                      mok_weight_grads *dw, float *dgates, float *dlogits, float *dW_r, void *ws,
                      void *stream)
 {
-    (void)x_src; (void)W_r; (void)saved_ctx; (void)dY; (void)w; (void)dX; (void)dw;
-    (void)dgates; (void)dlogits; (void)dW_r; (void)ws; (void)stream;
     Dims dm;
-    const int rc = check_config(cfg, &dm);
+    int rc = check_config(cfg, &dm);
     if (rc != MOK_OK) return rc;
-    return MOK_ERR_UNSUPPORTED;
+    if (!W_r || !saved_ctx || !dY || !w || !dX || !dw || !dw->d_gate || !dw->d_up || !dw->d_down ||
+        !dgates || !dW_r || !ws)
+        return MOK_ERR_INVALID_ARG;
+    const bool mx = dm.dtype == MOK_MXFP8;
+    if (mx && (!w->qt_gate || !w->qt_up || !w->qt_down || !w->st_gate || !w->st_up || !w->st_down))
+        return MOK_ERR_INVALID_ARG;
+    if (!mx && (!w->wt_gate || !w->wt_up || !w->wt_down)) return MOK_ERR_INVALID_ARG;
+    Sources src;
+    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    mok_ctx_layout c;
+    ctx_layout(dm, &c);
+    BwdWs bw;
+    bwd_ws_layout(dm, &bw);
+    void *ctx = const_cast<void *>(saved_ctx);
+    RouteOut o = route_in(ctx, c);
+    BwdBufs b;
+    b.dy = at<uint16_t>(ws, bw.dy);
+    b.dy_q = at<uint8_t>(ws, bw.dy_q);
+    b.dy_s = at<uint32_t>(ws, bw.dy_s);
+    b.saved_a = at<uint16_t>(ctx, c.a);
+    b.saved_b = at<uint16_t>(ctx, c.b);
+    b.saved_h = at<uint16_t>(ctx, c.h);
+    b.da = at<uint16_t>(ws, bw.da);
+    b.db = at<uint16_t>(ws, bw.db);
+    b.da_q = at<uint8_t>(ws, bw.da_q);
+    b.db_q = at<uint8_t>(ws, bw.db_q);
+    b.da_s = at<uint32_t>(ws, bw.da_s);
+    b.db_s = at<uint32_t>(ws, bw.db_s);
+    b.dx = at<uint16_t>(ws, bw.dx);
+    b.dyT = at<void>(ws, bw.dyT);
+    b.hT = at<void>(ws, bw.hT);
+    b.daT = at<void>(ws, bw.daT);
+    b.dbT = at<void>(ws, bw.dbT);
+    b.xT = at<void>(ws, bw.xT);
+    b.dyT_s = at<uint32_t>(ws, bw.dyT_s);
+    b.hT_s = at<uint32_t>(ws, bw.hT_s);
+    b.daT_s = at<uint32_t>(ws, bw.daT_s);
+    b.dbT_s = at<uint32_t>(ws, bw.dbT_s);
+    b.xT_s = at<uint32_t>(ws, bw.xT_s);
+    b.dl_sel = at<float>(ws, bw.dl_sel);
+    uint32_t *status = at<uint32_t>(ws, bw.status);
+    const uint64_t wns = wait_ns(cfg);
+    cudaError_t e = cudaMemsetAsync(status, 0, 4, st);
+    // B1 reverse combine (+ gate and chosen-logit gradients)
+    if (e == cudaSuccess)
+        e = launch_rev_combine(dm, static_cast<const uint16_t *>(dY), o.gates, o.sel_scores, o.ids,
+                               o.slot_pos, o.offsets, o.pad_offsets, at<uint16_t>(ctx, c.ystage), b,
+                               dgates, dlogits, st);
+    // B2 + B3 dgrad GEMMs
+    if (e == cudaSuccess) e = launch_dgrad(dm, b, w, o.counts, o.pad_offsets, status, wns, st);
+    // B4 wgrad operands (token dimension innermost) and GEMMs
+    if (e == cudaSuccess)
+        e = launch_transpose_rows(dm, b.dy, nullptr, dm.d, o.counts, o.offsets, o.pad_offsets,
+                                  o.row_tok, b.dyT, b.dyT_s, st);
+    if (e == cudaSuccess)
+        e = launch_transpose_rows(dm, b.saved_h, nullptr, dm.F, o.counts, o.offsets, o.pad_offsets,
+                                  o.row_tok, b.hT, b.hT_s, st);
+    if (e == cudaSuccess)
+        e = launch_transpose_rows(dm, b.da, nullptr, dm.F, o.counts, o.offsets, o.pad_offsets,
+                                  o.row_tok, b.daT, b.daT_s, st);
+    if (e == cudaSuccess)
+        e = launch_transpose_rows(dm, b.db, nullptr, dm.F, o.counts, o.offsets, o.pad_offsets,
+                                  o.row_tok, b.dbT, b.dbT_s, st);
+    if (e == cudaSuccess)
+        e = launch_transpose_rows(dm, nullptr, &src, dm.d, o.counts, o.offsets, o.pad_offsets,
+                                  o.row_tok, b.xT, b.xT_s, st);
+    if (e == cudaSuccess)
+        e = launch_wgrad(dm, b.dyT, b.dyT_s, dm.d, b.hT, b.hT_s, dm.F, o.pad_offsets,
+                         static_cast<uint16_t *>(dw->d_down), status, wns, st);
+    if (e == cudaSuccess)
+        e = launch_wgrad(dm, b.daT, b.daT_s, dm.F, b.xT, b.xT_s, dm.d, o.pad_offsets,
+                         static_cast<uint16_t *>(dw->d_gate), status, wns, st);
+    if (e == cudaSuccess)
+        e = launch_wgrad(dm, b.dbT, b.dbT_s, dm.F, b.xT, b.xT_s, dm.d, o.pad_offsets,
+                         static_cast<uint16_t *>(dw->d_up), status, wns, st);
+    // B5 reverse dispatch (+ router dX), B6 router weight gradient
+    if (e == cudaSuccess)
+        e = launch_rev_dispatch(dm, o.ids, o.slot_pos, o.offsets, o.pad_offsets, b.dx, b.dl_sel, W_r,
+                                static_cast<uint16_t *>(dX), st);
+    if (e == cudaSuccess)
+        e = launch_router_wgrad(dm, src, o.offsets, o.row_tok, o.row_j, b.dl_sel, dW_r, st);
+    return cuda_status(e);
+}
+
+int mok_transpose_bf16(const void *src, int64_t batch, int64_t rows, int64_t K, void *dst,
+                       void *stream)
+{
+    if (!src || !dst || batch < 1 || rows < 1 || K < 1) return MOK_ERR_INVALID_ARG;
+    return cuda_status(launch_transpose_bf16(static_cast<const uint16_t *>(src), batch, rows, K,
+                                             static_cast<uint16_t *>(dst),
+                                             static_cast<cudaStream_t>(stream)));
 }
 
 int mok_quantize_mx(const void *src, int64_t batch, int64_t rows, int64_t K, int transpose,

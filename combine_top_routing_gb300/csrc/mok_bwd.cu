@@ -1,0 +1,347 @@
+// mok_bwd.cu -- the HBM-bound steps of the backward layer.
+//
+// [kucoin] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+// NVL72" (kucoin.com flash, Arabic).  §01: training runs two more rounds of
+// exchange in the reverse direction; §02: backward uses a pull
+// reverse-combine (each slot pulls dY of its token) and a push
+// reverse-dispatch (each slot's input gradient goes back to its token).
+//
+//   k_rev_combine    B1 + B6 (gate part): dy_slot = bf16(g dY[t]) into the
+//                    padded expert-ordered rows (and MXFP8 along d), dgates =
+//                    <dY[t], y_tj>, dlogits of the chosen experts;
+//   k_transpose_rows wgrad operands: a padded row buffer (or x gathered by
+//                    token) transposed to [X, rows] with padding rows zeroed,
+//                    BF16 or MXFP8 along the token dimension;
+//   k_rev_dispatch   B5 + router dX: dX[t] = sum_j dx_slot + sum_j dl_j W_r[e_j];
+//   k_router_wgrad   B6: dW_r[e] = sum over e's rows of dl * x[t].
+// Every reduction runs in a fixed order (no atomics), so results are
+// bit-reproducible.
+#include <cuda_bf16.h>
+
+#include "mok_internal.h"
+#include "mok_ptx.cuh"
+
+namespace mok {
+
+// padded row of slot (t, j)
+__device__ __forceinline__ int64_t slot_row(const int32_t *ids, const int32_t *slot_pos,
+                                            const int32_t *offsets, const int32_t *pad_offsets,
+                                            int64_t i)
+{
+    const int e = ids[i];
+    return pad_offsets[e] + (slot_pos[i] - offsets[e]);
+}
+
+// ---------------------------------------------------------------------------
+// B1: one warp per token.  Lane l owns columns [8l + 256 i, +8).
+// ---------------------------------------------------------------------------
+template <bool MX>
+__global__ void __launch_bounds__(256) k_rev_combine(
+    int T, int d, int k, int E, int kind, const uint16_t *__restrict__ dY,
+    const float *__restrict__ gates, const float *__restrict__ sel_scores,
+    const int32_t *__restrict__ ids, const int32_t *__restrict__ slot_pos,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_offsets,
+    const uint16_t *__restrict__ ystage, uint16_t *__restrict__ dy_rows, uint8_t *__restrict__ dy_q,
+    uint32_t *__restrict__ dy_s, int64_t rows_pad, float *__restrict__ dgates,
+    float *__restrict__ dlogits, float *__restrict__ dl_sel)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const uint4 *dyrow = reinterpret_cast<const uint4 *>(dY + static_cast<int64_t>(t) * d);
+    float dg[MOK_MAX_TOPK];
+    for (int j = 0; j < k; ++j) {
+        const int64_t i = static_cast<int64_t>(t) * k + j;
+        const float g = gates[i];
+        const int64_t q = slot_row(ids, slot_pos, offsets, pad_offsets, i);
+        const uint4 *yrow = reinterpret_cast<const uint4 *>(ystage + i * d);
+        float dot = 0.0f;
+        for (int c0 = 0; c0 < d; c0 += 256) {
+            const int nvalid = d - c0 >= 256 ? 32 : 16;
+            uint4 out = make_uint4(0, 0, 0, 0);
+            if (lane < nvalid) {
+                const uint4 a = __ldg(dyrow + (c0 >> 3) + lane);
+                const uint4 y = __ldg(yrow + (c0 >> 3) + lane);
+                const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+                const uint32_t yv[4] = {y.x, y.y, y.z, y.w};
+                uint32_t ov[4];
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {
+                    const float d0 = bf16_bits_to_float(av[q2] & 0xFFFFu);
+                    const float d1 = bf16_bits_to_float(av[q2] >> 16);
+                    dot = fmaf(d0, bf16_bits_to_float(yv[q2] & 0xFFFFu), dot);
+                    dot = fmaf(d1, bf16_bits_to_float(yv[q2] >> 16), dot);
+                    ov[q2] = pack_bf16x2(g * d0, g * d1);
+                }
+                out = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+                reinterpret_cast<uint4 *>(dy_rows + q * d)[(c0 >> 3) + lane] = out;
+            }
+            if (MX) mx_quant_stretch(out, lane, nvalid, dy_q + q * d, c0, dy_s, q, rows_pad);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        dg[j] = dot;
+    }
+    // gradients through the renormalised top-k gates to the chosen logits
+    float G = 0.0f, ssum = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        G += dg[j] * gates[static_cast<int64_t>(t) * k + j];
+        ssum += sel_scores[static_cast<int64_t>(t) * k + j];
+    }
+    float dl[MOK_MAX_TOPK];
+    int sel[MOK_MAX_TOPK];
+    for (int j = 0; j < k; ++j) {
+        const int64_t i = static_cast<int64_t>(t) * k + j;
+        sel[j] = ids[i];
+        if (kind == MOK_ROUTER_SOFTMAX) {
+            dl[j] = gates[i] * (dg[j] - G);
+        } else {
+            const float s = sel_scores[i];
+            dl[j] = (dg[j] - G) / ssum * s * (1.0f - s);
+        }
+        if (lane == 0) {
+            dgates[i] = dg[j];
+            dl_sel[i] = dl[j];
+        }
+    }
+    if (dlogits) {
+        for (int e = lane; e < E; e += 32) {
+            float v = 0.0f;
+            for (int j = 0; j < k; ++j)
+                if (sel[j] == e) v = dl[j];
+            dlogits[static_cast<int64_t>(t) * E + e] = v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// wgrad operands: out[c, q] = in[q, c] for the padded rows q of one 256-row
+// tile, zero where q is a padding row; GATHER reads row q from the token it
+// holds (x via the sources) instead of from a row buffer.
+// ---------------------------------------------------------------------------
+template <bool MX, bool GATHER>
+__global__ void __launch_bounds__(256) k_transpose_rows(
+    const uint16_t *__restrict__ in, Sources src, int C, int E, const int32_t *__restrict__ counts,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_offsets,
+    const int32_t *__restrict__ row_tok, int64_t rows_pad, void *out, uint32_t *__restrict__ out_s)
+{
+    __shared__ uint16_t tile[32][256 + 8];
+    __shared__ int32_t s_pad[MOK_MAX_EXPERTS + 1];
+    const int64_t q0 = static_cast<int64_t>(blockIdx.y) * 256;
+    const int c0 = blockIdx.x * 32;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) s_pad[e] = pad_offsets[e];
+    __syncthreads();
+    if (q0 >= s_pad[E]) return;  // beyond the last expert segment: never read
+    for (int i = threadIdx.x; i < 256 * 4; i += blockDim.x) {
+        const int rr = i >> 2, cc = (i & 3) * 8;
+        const int64_t q = q0 + rr;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (q < s_pad[E]) {
+            int lo = 0, hi = E;  // expert segment holding q
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (s_pad[mid] <= q) lo = mid;
+                else hi = mid;
+            }
+            const int64_t local = q - s_pad[lo];
+            if (local < counts[lo]) {
+                const uint16_t *row;
+                if (GATHER) row = source_row(src, row_tok[offsets[lo] + local], C);
+                else row = in + q * C;
+                v = __ldg(reinterpret_cast<const uint4 *>(row + c0 + cc));
+            }
+        }
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q2 = 0; q2 < 4; ++q2) {
+            tile[cc + 2 * q2][rr] = static_cast<uint16_t>(w[q2] & 0xFFFFu);
+            tile[cc + 2 * q2 + 1][rr] = static_cast<uint16_t>(w[q2] >> 16);
+        }
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int oc = warp; oc < 32; oc += blockDim.x >> 5) {
+        const int64_t orow = c0 + oc;
+        const uint16_t *tp = &tile[oc][8 * lane];
+        uint4 raw;
+        raw.x = tp[0] | (static_cast<uint32_t>(tp[1]) << 16);
+        raw.y = tp[2] | (static_cast<uint32_t>(tp[3]) << 16);
+        raw.z = tp[4] | (static_cast<uint32_t>(tp[5]) << 16);
+        raw.w = tp[6] | (static_cast<uint32_t>(tp[7]) << 16);
+        if (MX) {
+            mx_quant_stretch(raw, lane, 32, static_cast<uint8_t *>(out) + orow * rows_pad, q0, out_s,
+                             orow, C);
+        } else {
+            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + orow * rows_pad + q0)[lane] = raw;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// B5: dX[t] = bf16( sum_j dx_rows[slot row] + sum_j dl_tj W_r[e_tj] ), both
+// sums in j order in fp32.  One warp per token.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_rev_dispatch(
+    int T, int d, int k, const int32_t *__restrict__ ids, const int32_t *__restrict__ slot_pos,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_offsets,
+    const uint16_t *__restrict__ dx_rows, const float *__restrict__ dl_sel,
+    const float *__restrict__ W_r, uint16_t *__restrict__ dX)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    for (int c0 = lane * 8; c0 < d; c0 += 256) {
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int64_t q = slot_row(ids, slot_pos, offsets, pad_offsets, static_cast<int64_t>(t) * k + j);
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(dx_rows + q * d + c0));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc[2 * i] += bf16_bits_to_float(w[i] & 0xFFFFu);
+                acc[2 * i + 1] += bf16_bits_to_float(w[i] >> 16);
+            }
+        }
+        for (int j = 0; j < k; ++j) {
+            const int64_t i = static_cast<int64_t>(t) * k + j;
+            const float dl = dl_sel[i];
+            const float4 *wr = reinterpret_cast<const float4 *>(W_r + static_cast<int64_t>(ids[i]) * d + c0);
+            const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
+            acc[0] = fmaf(dl, w0.x, acc[0]);
+            acc[1] = fmaf(dl, w0.y, acc[1]);
+            acc[2] = fmaf(dl, w0.z, acc[2]);
+            acc[3] = fmaf(dl, w0.w, acc[3]);
+            acc[4] = fmaf(dl, w1.x, acc[4]);
+            acc[5] = fmaf(dl, w1.y, acc[5]);
+            acc[6] = fmaf(dl, w1.z, acc[6]);
+            acc[7] = fmaf(dl, w1.w, acc[7]);
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        *reinterpret_cast<uint4 *>(dX + static_cast<int64_t>(t) * d + c0) = o;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// B6: dW_r[e, c] = sum over e's dense rows p (in order) of dl(p) x[t(p), c].
+// Block (column chunk of 256, expert e); thread per column.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_router_wgrad(
+    Sources src, int d, int k, const int32_t *__restrict__ offsets,
+    const int32_t *__restrict__ row_tok, const uint8_t *__restrict__ row_j,
+    const float *__restrict__ dl_sel, float *__restrict__ dW_r)
+{
+    const int e = blockIdx.y;
+    const int c = blockIdx.x * 256 + threadIdx.x;
+    const int p0 = offsets[e], p1 = offsets[e + 1];
+    float acc = 0.0f;
+    for (int p = p0; p < p1; ++p) {
+        const int t = row_tok[p];
+        const float dl = dl_sel[static_cast<int64_t>(t) * k + row_j[p]];
+        if (c < d) acc = fmaf(dl, bf16_bits_to_float(source_row(src, t, d)[c]), acc);
+    }
+    if (c < d) dW_r[static_cast<int64_t>(e) * d + c] = acc;
+}
+
+// ---------------------------------------------------------------------------
+// BF16 transpose of `batch` matrices [rows, K] -> [K, rows] (weights for the
+// BF16 backward GEMMs).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_transpose_bf16(const uint16_t *__restrict__ src,
+                                                        int64_t rows, int64_t K,
+                                                        uint16_t *__restrict__ dst)
+{
+    __shared__ uint16_t tile[32][33];
+    const int64_t b = blockIdx.z;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, k0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const uint16_t *s = src + b * rows * K;
+    uint16_t *o = dst + b * rows * K;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+    for (int i = ty; i < 32; i += 8)
+        if (r0 + i < rows && k0 + tx < K) tile[i][tx] = s[(r0 + i) * K + k0 + tx];
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8)
+        if (k0 + i < K && r0 + tx < rows) o[(k0 + i) * rows + r0 + tx] = tile[tx][i];
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_rev_combine(const Dims &dm, const uint16_t *dY, const float *gates,
+                               const float *sel_scores, const int32_t *ids,
+                               const int32_t *slot_pos, const int32_t *offsets,
+                               const int32_t *pad_offsets, const uint16_t *ystage,
+                               const BwdBufs &b, float *dgates, float *dlogits, cudaStream_t st)
+{
+    const int blocks = (dm.T + 7) / 8;
+    if (dm.dtype == MOK_MXFP8)
+        k_rev_combine<true><<<blocks, 256, 0, st>>>(dm.T, dm.d, dm.k, dm.E, dm.router, dY, gates,
+                                                   sel_scores, ids, slot_pos, offsets, pad_offsets,
+                                                   ystage, b.dy, b.dy_q, b.dy_s, dm.rows_pad, dgates,
+                                                   dlogits, b.dl_sel);
+    else
+        k_rev_combine<false><<<blocks, 256, 0, st>>>(dm.T, dm.d, dm.k, dm.E, dm.router, dY, gates,
+                                                    sel_scores, ids, slot_pos, offsets, pad_offsets,
+                                                    ystage, b.dy, nullptr, nullptr, dm.rows_pad,
+                                                    dgates, dlogits, b.dl_sel);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_rows(const Dims &dm, const uint16_t *in, const Sources *src, int C,
+                                  const int32_t *counts, const int32_t *offsets,
+                                  const int32_t *pad_offsets, const int32_t *row_tok, void *out,
+                                  uint32_t *out_s, cudaStream_t st)
+{
+    dim3 grid(static_cast<unsigned>(C / 32), static_cast<unsigned>(dm.rows_pad / 256));
+    const bool mx = dm.dtype == MOK_MXFP8;
+    Sources empty_src = {};
+    const Sources &s = src ? *src : empty_src;
+    if (mx && src)
+        k_transpose_rows<true, true><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets, pad_offsets,
+                                                          row_tok, dm.rows_pad, out, out_s);
+    else if (mx)
+        k_transpose_rows<true, false><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets, pad_offsets,
+                                                           row_tok, dm.rows_pad, out, out_s);
+    else if (src)
+        k_transpose_rows<false, true><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets, pad_offsets,
+                                                           row_tok, dm.rows_pad, out, out_s);
+    else
+        k_transpose_rows<false, false><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets,
+                                                            pad_offsets, row_tok, dm.rows_pad, out, out_s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rev_dispatch(const Dims &dm, const int32_t *ids, const int32_t *slot_pos,
+                                const int32_t *offsets, const int32_t *pad_offsets,
+                                const uint16_t *dx_rows, const float *dl_sel, const float *W_r,
+                                uint16_t *dX, cudaStream_t st)
+{
+    k_rev_dispatch<<<(dm.T + 7) / 8, 256, 0, st>>>(dm.T, dm.d, dm.k, ids, slot_pos, offsets,
+                                                   pad_offsets, dx_rows, dl_sel, W_r, dX);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_wgrad(const Dims &dm, const Sources &src, const int32_t *offsets,
+                                const int32_t *row_tok, const uint8_t *row_j, const float *dl_sel,
+                                float *dW_r, cudaStream_t st)
+{
+    dim3 grid(static_cast<unsigned>((dm.d + 255) / 256), static_cast<unsigned>(dm.E));
+    k_router_wgrad<<<grid, 256, 0, st>>>(src, dm.d, dm.k, offsets, row_tok, row_j, dl_sel, dW_r);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_bf16(const uint16_t *src, int64_t batch, int64_t rows, int64_t K,
+                                  uint16_t *dst, cudaStream_t st)
+{
+    dim3 grid(static_cast<unsigned>((K + 31) / 32), static_cast<unsigned>((rows + 31) / 32),
+              static_cast<unsigned>(batch));
+    k_transpose_bf16<<<grid, 256, 0, st>>>(src, rows, K, dst);
+    return cudaGetLastError();
+}
+
+}  // namespace mok

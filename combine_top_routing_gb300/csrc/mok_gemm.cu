@@ -2,29 +2,37 @@
 //
 // [kucoin] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
 // NVL72" (kucoin.com flash, Arabic).  §01: the grouped GEMM needs each
-// expert's tokens organised together before it can feed the tensor cores;
-// §02: MXFP8 activation quantisation is fused into the grouped GEMM and
-// SwiGLU, and combine is a push -- each result goes straight to the token it
-// came from.
+// expert's tokens organised together before it can feed the tensor cores,
+// and backward runs the exchange again in reverse; §02: MXFP8 activation
+// quantisation is fused into the grouped GEMM and SwiGLU, and combine is a
+// push -- each result goes straight to the token it came from.
 //
 // One persistent kernel template, one CTA per SM, 6 warps:
 //   warp 0      TMA producer: A tile (128 rows) and B tile (128 or 256 rows)
-//               of 128 bytes along K per stage, plus MX scale tiles, into a
-//               4-stage shared-memory ring (mbarrier full/empty pairs);
+//               of 128 bytes along K per stage, plus MX scale tiles (bulk
+//               copies), into a 4-stage shared-memory ring (mbarrier
+//               full/empty pairs);
 //   warp 1      allocates TMEM and issues tcgen05.mma from one thread into a
 //               128 x N fp32 accumulator (N = 256 or 128);
 //   warps 2..5  epilogue: each thread owns one accumulator row (its TMEM
 //               lane) and runs the mode's epilogue straight from registers.
-// Modes:
-//   ROUTER  plain GEMM x . [W_hi | W_mid | W_lo]^T over the token rows of each
-//           source buffer (A's K wraps three times), fp32 logits (+ bias);
+// Modes (C = A B^T, both operands K-major):
+//   ROUTER  x . [W_hi | W_mid | W_lo]^T over the token rows of each source
+//           buffer (A's K wraps three times); fp32 logits (+ bias);
 //   FFN1    per expert, B = 128 rows of W_g and the same 128 rows of W_u, so
 //           one tile holds a and b for 128 columns of F: h = silu(a) b, stored
 //           BF16 or MXFP8 (blocks of 32 along F, quantised in registers);
-//   FFN2    per expert, y = h W_d^T stored BF16 into ystage[token, j].
-// Tiles are ordered expert by expert, N-tile by N-tile, with the expert's row
+//   FFN2    per expert, y = h W_d^T stored BF16 into ystage[token, j];
+//   DGRAD2  per expert, dh = dy W_d (B = W_d^T rows); SwiGLU backward with the
+//           saved a, b in the epilogue -> da, db (BF16, and MXFP8 along F);
+//   DGRAD1  per expert, dx = da W_g + db W_u as one K = 2F loop over
+//           (da, W_g^T) then (db, W_u^T); BF16 rows;
+//   WGRAD   per expert, dW = A^T B over the expert's token rows: A and B are
+//           the transposed operands [X, rows] whose K range is the expert's
+//           padded row segment; BF16 out, zeros for an expert without rows.
+// Tiles are ordered group by group, N-tile by N-tile, with the group's row
 // tiles innermost, and dealt round-robin to the CTAs: concurrently running
-// CTAs share B tiles and the expert's rows through L2.
+// CTAs share B tiles and the group's rows through L2.
 #include <cuda_bf16.h>
 
 #include <mutex>
@@ -47,7 +55,7 @@ constexpr int kSfbBytes = 1024;           // 256 rows x 4 scale bytes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 256;          // scale columns: 16 per stage after the accumulator
 
-enum { MODE_ROUTER = 0, MODE_FFN1 = 1, MODE_FFN2 = 2 };
+enum { MODE_ROUTER = 0, MODE_FFN1, MODE_FFN2, MODE_DGRAD2, MODE_DGRAD1, MODE_WGRAD };
 
 template <int NA>
 struct AMaps {
@@ -59,20 +67,22 @@ struct AMaps {
 };
 
 struct GemmArgs {
-    int E;                  // groups (experts); router: 1
+    int E;                  // groups (experts); router: sources
     const int32_t *counts;
     const int32_t *offsets;
     const int32_t *pad_offsets;
     int n_tiles;            // N tiles per group
     int BN;                 // MMA N: 128 or 256
-    int k_stages;           // K / (128 bytes)
-    int a_k_stages;         // K stages of A before it wraps (router), else k_stages
+    int k_stages;           // K / (128 bytes) (not WGRAD)
+    int a_k_stages;         // router: K stages of A before it wraps
+    int ks_half;            // DGRAD1: K stages of each of the two segments
     int b_rows_per_group;   // rows of B per expert
-    // MX scales (tile layout)
-    const uint32_t *sfa;
-    int64_t sfa_rows;
-    const uint32_t *sfb0, *sfb1;
-    int64_t sfb_rows;
+    int m_rows;             // WGRAD: output rows per expert (multiple of 128)
+    // MX scales (tile layout) of A maps 0/1 and B maps 0/1
+    const uint32_t *sfa[2];
+    int64_t sfa_rows[2];
+    const uint32_t *sfb[2];
+    int64_t sfb_rows[2];
     // epilogue
     int F, d, k_top, T;
     float *logits;
@@ -85,6 +95,13 @@ struct GemmArgs {
     uint16_t *ystage;
     const int32_t *row_tok;
     const uint8_t *row_j;
+    // backward
+    const uint16_t *in_a, *in_b;     // DGRAD2: saved a, b
+    uint16_t *out_da, *out_db;       // DGRAD2: BF16 da, db
+    uint8_t *q_da, *q_db;            // DGRAD2 (MX): codes of da, db along F
+    uint32_t *s_da, *s_db;           // DGRAD2 (MX): their scales
+    uint16_t *out_rows;              // DGRAD1: dx rows; WGRAD: dW [E * m_rows, N]
+    int64_t out_ld;                  // WGRAD: columns of dW
     uint32_t *status;
     uint64_t wait_ns;
 };
@@ -148,10 +165,76 @@ __device__ __forceinline__ void store_bf16x32(uint16_t *dst, const float *v)
     }
 }
 
-template <int MODE, bool MX, int NA>
+__device__ __forceinline__ void load_bf16x32(const uint16_t *src, float *v)
+{
+    const uint4 *p = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 w = p[q];
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[8 * q + 2 * i] = bf16_bits_to_float(u[i] & 0xFFFFu);
+            v[8 * q + 2 * i + 1] = bf16_bits_to_float(u[i] >> 16);
+        }
+    }
+}
+
+// 32 fp32 values -> one MX block: 32 E4M3 codes at dst (16-byte aligned);
+// returns the E8M0 scale byte.
+__device__ __forceinline__ uint32_t quant_mx32(const float *v, uint8_t *dst)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int x = mx_scale_exp(amax);
+    const float inv = mx_inv_scale(x);
+    uint4 *o = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const float *s = v + 16 * q;
+        uint4 w;
+        w.x = pack_e4m3x2(s[0] * inv, s[1] * inv) | (pack_e4m3x2(s[2] * inv, s[3] * inv) << 16);
+        w.y = pack_e4m3x2(s[4] * inv, s[5] * inv) | (pack_e4m3x2(s[6] * inv, s[7] * inv) << 16);
+        w.z = pack_e4m3x2(s[8] * inv, s[9] * inv) | (pack_e4m3x2(s[10] * inv, s[11] * inv) << 16);
+        w.w = pack_e4m3x2(s[12] * inv, s[13] * inv) | (pack_e4m3x2(s[14] * inv, s[15] * inv) << 16);
+        o[q] = w;
+    }
+    return static_cast<uint32_t>(x + 127);
+}
+
+__device__ __forceinline__ int64_t scale_word(int64_t x_elem, int64_t row, int64_t rows)
+{
+    return ((x_elem >> 7) * (rows >> 7) + (row >> 7)) * 128;
+}
+
+__device__ __forceinline__ int64_t scale_word_row(int64_t g, int64_t r, int64_t rows)
+{
+    return (g * (rows >> 7) + (r >> 7)) * 128 + (r & 31) * 4 + ((r & 127) >> 5);
+}
+
+template <int MODE>
+__device__ __forceinline__ int group_row_tiles(const AMaps<MODE == MODE_ROUTER ? 64 : 2> &am,
+                                               const GemmArgs &a, int g)
+{
+    if constexpr (MODE == MODE_ROUTER) return am.mt_start[g + 1] - am.mt_start[g];
+    else if constexpr (MODE == MODE_WGRAD) return a.m_rows / kBM;
+    else return (a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM;
+}
+
+template <int MODE, bool MX>
+__device__ __forceinline__ int tile_k_stages(const GemmArgs &a, int g)
+{
+    if constexpr (MODE == MODE_WGRAD)
+        return (a.pad_offsets[g + 1] - a.pad_offsets[g]) / (MX ? 128 : 64);
+    else return a.k_stages;
+}
+
+template <int MODE, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm(const __grid_constant__ AMaps<NA> am, const __grid_constant__ CUtensorMap tmB0,
-           const __grid_constant__ CUtensorMap tmB1, const GemmArgs a)
+    k_gemm(const __grid_constant__ AMaps<MODE == MODE_ROUTER ? 64 : 2> am,
+           const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+           const GemmArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -183,7 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        for (int i = 0; i < (MODE == MODE_ROUTER ? am.n : 1); ++i) prefetch_tmap(&am.m[i]);
+        const int na = MODE == MODE_ROUTER ? am.n : (MODE == MODE_DGRAD1 ? 2 : 1);
+        for (int i = 0; i < na; ++i) prefetch_tmap(&am.m[i]);
         prefetch_tmap(&tmB0);
         prefetch_tmap(&tmB1);
     }
@@ -196,12 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int per = (groups + 31) / 32;
         const int g0 = lane * per;
         int local = 0;
-        for (int g = g0; g < g0 + per && g < groups; ++g) {
-            int mt;
-            if (MODE == MODE_ROUTER) mt = am.mt_start[g + 1] - am.mt_start[g];
-            else mt = (a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM;
-            local += mt * a.n_tiles;
-        }
+        for (int g = g0; g < g0 + per && g < groups; ++g)
+            local += group_row_tiles<MODE>(am, a, g) * a.n_tiles;
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -211,10 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int run = incl - local;
         for (int g = g0; g < g0 + per && g < groups; ++g) {
             prefix[g] = run;
-            int mt;
-            if (MODE == MODE_ROUTER) mt = am.mt_start[g + 1] - am.mt_start[g];
-            else mt = (a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM;
-            run += mt * a.n_tiles;
+            run += group_row_tiles<MODE>(am, a, g) * a.n_tiles;
         }
         if (lane == 31) prefix[groups] = incl;
     }
@@ -224,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const int total = prefix[groups];
     const int BN = a.BN;
-    constexpr int kElemsPerStage = MX ? 128 : 64;
+    constexpr int kE = MX ? 128 : 64;  // elements per 128-byte K stage
 
     if (warp == 0) {
         if (lane == 0) {
@@ -234,40 +311,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                                          (MX ? kSfaBytes + (BN / 128) * 512 : 0);
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
                 const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
-                int a_row, b_row, ai = 0;
-                if (MODE == MODE_ROUTER) {
-                    ai = tl.group;
-                    a_row = tl.m_blk * kBM;
-                    b_row = tl.n_blk * BN;
-                } else {
-                    a_row = a.pad_offsets[tl.group] + tl.m_blk * kBM;
-                    b_row = tl.group * a.b_rows_per_group + tl.n_blk * (MODE == MODE_FFN1 ? 128 : BN);
-                }
-                for (int ks = 0; ks < a.k_stages; ++ks) {
+                const int g = tl.group;
+                const int kst = tile_k_stages<MODE, MX>(a, g);
+                for (int ks = 0; ks < kst; ++ks) {
+                    // coordinates of this stage: A map / (x, y), B maps / (x, y0, y1)
+                    int ai = 0, xa, ya, bi0 = 0, bi1 = 0, xb, yb0, yb1;
+                    if constexpr (MODE == MODE_ROUTER) {
+                        ai = g;
+                        xa = (ks % a.a_k_stages) * kE;
+                        ya = tl.m_blk * kBM;
+                        xb = ks * kE;
+                        yb0 = tl.n_blk * BN;
+                        yb1 = yb0 + 128;
+                    } else if constexpr (MODE == MODE_FFN1) {
+                        xa = ks * kE;
+                        ya = a.pad_offsets[g] + tl.m_blk * kBM;
+                        xb = ks * kE;
+                        yb0 = g * a.b_rows_per_group + tl.n_blk * 128;
+                        yb1 = yb0;
+                        bi1 = 1;
+                    } else if constexpr (MODE == MODE_DGRAD1) {
+                        const int seg = ks >= a.ks_half;
+                        const int kk = ks - seg * a.ks_half;
+                        ai = bi0 = bi1 = seg;
+                        xa = kk * kE;
+                        ya = a.pad_offsets[g] + tl.m_blk * kBM;
+                        xb = kk * kE;
+                        yb0 = g * a.b_rows_per_group + tl.n_blk * BN;
+                        yb1 = yb0 + 128;
+                    } else if constexpr (MODE == MODE_WGRAD) {
+                        xa = a.pad_offsets[g] + ks * kE;
+                        ya = tl.m_blk * kBM;
+                        xb = xa;
+                        yb0 = tl.n_blk * BN;
+                        yb1 = yb0 + 128;
+                    } else {  // FFN2, DGRAD2
+                        xa = ks * kE;
+                        ya = a.pad_offsets[g] + tl.m_blk * kBM;
+                        xb = ks * kE;
+                        yb0 = g * a.b_rows_per_group + tl.n_blk * BN;
+                        yb1 = yb0 + 128;
+                    }
                     if (!wait_bar(&empty[stage], phase ^ 1u, a, abort_flag)) goto producer_done;
                     uint8_t *dA = sA + stage * kAStage;
                     uint8_t *dB = sB + stage * kBStage;
-                    const int ka = (ks % a.a_k_stages) * kElemsPerStage;
-                    const int kb = ks * kElemsPerStage;
                     mbar_arrive_expect_tx(&full[stage], stage_bytes);
-                    tma_load_2d(dA, &am.m[ai], &full[stage], ka, a_row);
-                    tma_load_2d(dB, &tmB0, &full[stage], kb, b_row);
-                    if (BN == 256) {
-                        if (MODE == MODE_FFN1) tma_load_2d(dB + 16384, &tmB1, &full[stage], kb, b_row);
-                        else tma_load_2d(dB + 16384, &tmB0, &full[stage], kb, b_row + 128);
-                    }
-                    if (MX) {
+                    tma_load_2d(dA, &am.m[ai], &full[stage], xa, ya);
+                    tma_load_2d(dB, bi0 ? &tmB1 : &tmB0, &full[stage], xb, yb0);
+                    if (BN == 256) tma_load_2d(dB + 16384, bi1 ? &tmB1 : &tmB0, &full[stage], xb, yb1);
+                    if constexpr (MX) {
                         uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
-                        const uint32_t *sa = a.sfa + (static_cast<int64_t>(ks) * (a.sfa_rows >> 7) + (a_row >> 7)) * 128;
-                        bulk_load(dS, sa, kSfaBytes, &full[stage]);
-                        const uint32_t *sb = a.sfb0 + (static_cast<int64_t>(ks) * (a.sfb_rows >> 7) + (b_row >> 7)) * 128;
-                        if (MODE == MODE_FFN1) {
-                            bulk_load(dS + kSfaBytes, sb, 512, &full[stage]);
-                            const uint32_t *su = a.sfb1 + (static_cast<int64_t>(ks) * (a.sfb_rows >> 7) + (b_row >> 7)) * 128;
-                            bulk_load(dS + kSfaBytes + 512, su, 512, &full[stage]);
-                        } else {
-                            bulk_load(dS + kSfaBytes, sb, (BN / 128) * 512, &full[stage]);
-                        }
+                        bulk_load(dS, a.sfa[ai] + scale_word(xa, ya, a.sfa_rows[ai]), kSfaBytes, &full[stage]);
+                        bulk_load(dS + kSfaBytes, a.sfb[bi0] + scale_word(xb, yb0, a.sfb_rows[bi0]), 512,
+                                  &full[stage]);
+                        if (BN == 256)
+                            bulk_load(dS + kSfaBytes + 512,
+                                      a.sfb[bi1] + scale_word(xb, yb1, a.sfb_rows[bi1]), 512, &full[stage]);
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -283,9 +382,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             const uint32_t idesc = idesc_bf16(kBM, BN);
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
+                const int kst = tile_k_stages<MODE, MX>(a, tl.group);
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a, abort_flag)) break;
                 tc_fence_after();
-                for (int ks = 0; ks < a.k_stages; ++ks) {
+                for (int ks = 0; ks < kst; ++ks) {
                     if (!wait_bar(&full[stage], phase, a, abort_flag)) goto mma_done;
                     tc_fence_after();
                     const uint32_t aaddr = smem_u32(sA + stage * kAStage);
@@ -327,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
             if (!wait_bar(acc_full, acc_phase, a, abort_flag)) break;
             tc_fence_after();
-            if (MODE == MODE_ROUTER) {
+            if constexpr (MODE == MODE_ROUTER) {
                 const int lrow = tl.m_blk * kBM + r;
                 const bool valid = lrow < am.rows[tl.group];
                 const int64_t tok = am.row_start[tl.group] + lrow;
@@ -345,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-            } else if (MODE == MODE_FFN1) {
+            } else if constexpr (MODE == MODE_FFN1) {
                 const int e = tl.group;
                 const int row_in_e = tl.m_blk * kBM + r;
                 const bool valid = row_in_e < a.counts[e];
@@ -378,36 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(uv[i]);
                             store_bf16x32(a.saved_b + off, t);
                         }
+                        if (a.saved_h) store_bf16x32(a.saved_h + off, hv);
                         if (!MX) {
                             store_bf16x32(static_cast<uint16_t *>(a.h) + off, hv);
-                            if (a.saved_h) store_bf16x32(a.saved_h + off, hv);
                         } else {
-                            float amax = 0.0f;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
-                            const int x = mx_scale_exp(amax);
-                            const float inv = mx_inv_scale(x);
-                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.h) + off);
-#pragma unroll
-                            for (int q = 0; q < 2; ++q) {
-                                uint4 w;
-                                const float *s = hv + 16 * q;
-                                w.x = pack_e4m3x2(s[0] * inv, s[1] * inv) | (pack_e4m3x2(s[2] * inv, s[3] * inv) << 16);
-                                w.y = pack_e4m3x2(s[4] * inv, s[5] * inv) | (pack_e4m3x2(s[6] * inv, s[7] * inv) << 16);
-                                w.z = pack_e4m3x2(s[8] * inv, s[9] * inv) | (pack_e4m3x2(s[10] * inv, s[11] * inv) << 16);
-                                w.w = pack_e4m3x2(s[12] * inv, s[13] * inv) | (pack_e4m3x2(s[14] * inv, s[15] * inv) << 16);
-                                o[q] = w;
-                            }
-                            sword |= static_cast<uint32_t>(x + 127) << (8 * (c >> 5));
-                            if (a.saved_h) store_bf16x32(a.saved_h + off, hv);
+                            sword |= quant_mx32(hv, static_cast<uint8_t *>(a.h) + off) << (8 * (c >> 5));
                         }
                     }
                 }
-                if (MX && valid) {
-                    const int64_t g = f0 >> 7;
-                    a.h_scales[(g * (a.h_rows >> 7) + (grow >> 7)) * 128 + (grow & 31) * 4 + ((grow & 127) >> 5)] = sword;
-                }
-            } else {
+                if (MX && valid) a.h_scales[scale_word_row(f0 >> 7, grow, a.h_rows)] = sword;
+            } else if constexpr (MODE == MODE_FFN2) {
                 const int e = tl.group;
                 const int row_in_e = tl.m_blk * kBM + r;
                 const bool valid = row_in_e < a.counts[e];
@@ -428,6 +509,89 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
                         store_bf16x32(dst + c, f);
                     }
+                }
+            } else if constexpr (MODE == MODE_DGRAD2) {
+                // dh -> SwiGLU backward with the saved (BF16) a, b:
+                //   s = sigmoid(a), da = dh b s (1 + a (1 - s)), db = dh a s
+                const int e = tl.group;
+                const int row_in_e = tl.m_blk * kBM + r;
+                const bool valid = row_in_e < a.counts[e];
+                const int64_t grow = a.pad_offsets[e] + row_in_e;
+                const int f0 = tl.n_blk * BN;
+                uint32_t wa = 0, wb = 0;
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32(trow + c, v);
+                    tmem_ld_wait();
+                    if (valid) {
+                        const int64_t off = grow * a.F + f0 + c;
+                        float av[32], bv[32], da[32], db[32];
+                        load_bf16x32(a.in_a + off, av);
+                        load_bf16x32(a.in_b + off, bv);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float dh = __uint_as_float(v[i]);
+                            const float s = 1.0f / (1.0f + __expf(-av[i]));
+                            da[i] = dh * bv[i] * s * (1.0f + av[i] * (1.0f - s));
+                            db[i] = dh * av[i] * s;
+                        }
+                        store_bf16x32(a.out_da + off, da);
+                        store_bf16x32(a.out_db + off, db);
+                        if constexpr (MX) {
+                            // quantise the BF16-rounded values (the stored da, db)
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                da[i] = bf16_bits_to_float(float_to_bf16_bits(da[i]));
+                                db[i] = bf16_bits_to_float(float_to_bf16_bits(db[i]));
+                            }
+                            const int sh = 8 * ((c >> 5) & 3);
+                            wa |= quant_mx32(da, a.q_da + off) << sh;
+                            wb |= quant_mx32(db, a.q_db + off) << sh;
+                            if ((c & 127) == 96) {
+                                const int64_t wi = scale_word_row((f0 + c) >> 7, grow, a.h_rows);
+                                a.s_da[wi] = wa;
+                                a.s_db[wi] = wb;
+                                wa = wb = 0;
+                            }
+                        }
+                    }
+                }
+            } else if constexpr (MODE == MODE_DGRAD1) {
+                const int e = tl.group;
+                const int row_in_e = tl.m_blk * kBM + r;
+                const bool valid = row_in_e < a.counts[e];
+                const int64_t grow = a.pad_offsets[e] + row_in_e;
+                uint16_t *dst = a.out_rows + grow * a.d + tl.n_blk * BN;
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32(trow + c, v);
+                    tmem_ld_wait();
+                    if (valid) {
+                        float f[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+                        store_bf16x32(dst + c, f);
+                    }
+                }
+            } else {  // MODE_WGRAD
+                const int e = tl.group;
+                const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
+                uint16_t *dst = a.out_rows +
+                                (static_cast<int64_t>(e) * a.m_rows + tl.m_blk * kBM + r) * a.out_ld +
+                                tl.n_blk * BN;
+                for (int c = 0; c < BN; c += 32) {
+                    float f[32];
+                    if (!empty_k) {
+                        uint32_t v[32];
+                        tmem_ld_32x32(trow + c, v);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) f[i] = 0.0f;
+                    }
+                    store_bf16x32(dst + c, f);
                 }
             }
             tc_fence_before();
@@ -450,37 +614,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int MODE, bool MX, int NA>
+template <bool MX>
 constexpr size_t smem_bytes()
 {
     return 1024 + kStages * (kAStage + kBStage) + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0) +
            (2 * kStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 1) * 4;
 }
 
-template <int MODE, bool MX, int NA>
-cudaError_t launch_gemm(const AMaps<NA> &am, const CUtensorMap &b0, const CUtensorMap &b1,
-                        const GemmArgs &args, cudaStream_t st)
+template <int MODE, bool MX>
+cudaError_t launch_gemm(const AMaps<MODE == MODE_ROUTER ? 64 : 2> &am, const CUtensorMap &b0,
+                        const CUtensorMap &b1, const GemmArgs &args, cudaStream_t st)
 {
-    constexpr size_t smem = smem_bytes<MODE, MX, NA>();
+    constexpr size_t smem = smem_bytes<MX>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(k_gemm<MODE, MX, NA>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(k_gemm<MODE, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem));
     });
     if (attr_err != cudaSuccess) return attr_err;
-    k_gemm<MODE, MX, NA><<<num_sms(), kThreads, smem, st>>>(am, b0, b1, args);
+    k_gemm<MODE, MX><<<num_sms(), kThreads, smem, st>>>(am, b0, b1, args);
     return cudaGetLastError();
 }
 
+GemmArgs base_args(const Dims &dm, uint32_t *status, uint64_t wait_ns)
+{
+    GemmArgs g = {};
+    g.E = dm.E;
+    g.F = dm.F;
+    g.d = dm.d;
+    g.k_top = dm.k;
+    g.T = dm.T;
+    g.status = status;
+    g.wait_ns = wait_ns;
+    return g;
+}
+
 }  // namespace
+
+static_assert(kMaxRouterSources == 64, "router tensor-map table size");
 
 cudaError_t launch_router_gemm(const Dims &dm, const Sources &src, const uint16_t *w3,
                                const float *bias, float *logits, uint32_t *status,
                                uint64_t wait_ns, cudaStream_t st)
 {
-    static AMaps<kMaxRouterSources> am;  // large: keep off the stack
+    static AMaps<64> am;  // large: keep off the stack
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     if (src.n > kMaxRouterSources) return cudaErrorInvalidValue;
@@ -499,19 +677,16 @@ cudaError_t launch_router_gemm(const Dims &dm, const Sources &src, const uint16_
     CUtensorMap b;
     if (encode_tmap_2d(&b, w3, false, 3 * static_cast<uint64_t>(dm.d), dm.E_pad, 64, 128))
         return cudaErrorInvalidValue;
-    GemmArgs g = {};
-    g.E = 1;
+    GemmArgs g = base_args(dm, status, wait_ns);
+    g.E = src.n;
     g.BN = dm.E_pad >= 256 ? 256 : 128;
     g.n_tiles = dm.E_pad / g.BN;
     g.k_stages = 3 * dm.d / 64;
     g.a_k_stages = dm.d / 64;
-    g.T = dm.T;
     g.logits = logits;
     g.bias = bias;
     g.E_valid = dm.E;
-    g.status = status;
-    g.wait_ns = wait_ns;
-    return launch_gemm<MODE_ROUTER, false, kMaxRouterSources>(am, b, b, g, st);
+    return launch_gemm<MODE_ROUTER, false>(am, b, b, g, st);
 }
 
 cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales,
@@ -525,7 +700,7 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
     const uint32_t box = mx ? 128 : 64;
     const uint64_t EF = static_cast<uint64_t>(dm.E) * dm.F;
     const uint64_t Ed = static_cast<uint64_t>(dm.E) * dm.d;
-    AMaps<1> a1 = {}, a2 = {};
+    AMaps<2> a1 = {}, a2 = {};
     CUtensorMap bg, bu, bd;
     if (encode_tmap_2d(&a1.m[0], xe, mx, dm.d, dm.rows_pad, box, kBM) ||
         encode_tmap_2d(&bg, mx ? static_cast<const void *>(w->q_gate) : w->w_gate, mx, dm.d, EF, box, 128) ||
@@ -535,38 +710,30 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
         return cudaErrorInvalidValue;
     a1.n = a2.n = 1;
 
-    GemmArgs g = {};
-    g.E = dm.E;
+    GemmArgs g = base_args(dm, status, wait_ns);
     g.counts = counts;
     g.offsets = offsets;
     g.pad_offsets = pad_offsets;
-    g.F = dm.F;
-    g.d = dm.d;
-    g.k_top = dm.k;
-    g.T = dm.T;
-    g.status = status;
-    g.wait_ns = wait_ns;
 
     // GEMM1 + SwiGLU: N tile = 128 columns of F, as 128 gate + 128 up rows of B
     GemmArgs g1 = g;
     g1.BN = 256;
     g1.n_tiles = dm.F / 128;
     g1.k_stages = dm.d / static_cast<int>(box);
-    g1.a_k_stages = g1.k_stages;
     g1.b_rows_per_group = dm.F;
-    g1.sfa = xe_scales;
-    g1.sfa_rows = dm.rows_pad;
-    g1.sfb0 = w->s_gate;
-    g1.sfb1 = w->s_up;
-    g1.sfb_rows = static_cast<int64_t>(EF);
+    g1.sfa[0] = xe_scales;
+    g1.sfa_rows[0] = dm.rows_pad;
+    g1.sfb[0] = w->s_gate;
+    g1.sfb[1] = w->s_up;
+    g1.sfb_rows[0] = g1.sfb_rows[1] = static_cast<int64_t>(EF);
     g1.h = h;
     g1.h_scales = h_scales;
     g1.h_rows = dm.rows_pad;
     g1.saved_a = saved_a;
     g1.saved_b = saved_b;
     g1.saved_h = saved_h;
-    cudaError_t err = mx ? launch_gemm<MODE_FFN1, true, 1>(a1, bg, bu, g1, st)
-                         : launch_gemm<MODE_FFN1, false, 1>(a1, bg, bu, g1, st);
+    cudaError_t err = mx ? launch_gemm<MODE_FFN1, true>(a1, bg, bu, g1, st)
+                         : launch_gemm<MODE_FFN1, false>(a1, bg, bu, g1, st);
     if (err != cudaSuccess) return err;
 
     // GEMM2: y = h W_d^T scattered to ystage
@@ -574,18 +741,111 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
     g2.BN = dm.d % 256 == 0 ? 256 : 128;
     g2.n_tiles = dm.d / g2.BN;
     g2.k_stages = dm.F / static_cast<int>(box);
-    g2.a_k_stages = g2.k_stages;
     g2.b_rows_per_group = dm.d;
-    g2.sfa = h_scales;
-    g2.sfa_rows = dm.rows_pad;
-    g2.sfb0 = w->s_down;
-    g2.sfb1 = w->s_down;
-    g2.sfb_rows = static_cast<int64_t>(Ed);
+    g2.sfa[0] = h_scales;
+    g2.sfa_rows[0] = dm.rows_pad;
+    g2.sfb[0] = g2.sfb[1] = w->s_down;
+    g2.sfb_rows[0] = g2.sfb_rows[1] = static_cast<int64_t>(Ed);
     g2.ystage = ystage;
     g2.row_tok = row_tok;
     g2.row_j = row_j;
-    return mx ? launch_gemm<MODE_FFN2, true, 1>(a2, bd, bd, g2, st)
-              : launch_gemm<MODE_FFN2, false, 1>(a2, bd, bd, g2, st);
+    return mx ? launch_gemm<MODE_FFN2, true>(a2, bd, bd, g2, st)
+              : launch_gemm<MODE_FFN2, false>(a2, bd, bd, g2, st);
+}
+
+cudaError_t launch_dgrad(const Dims &dm, const BwdBufs &b, const mok_weights *w,
+                         const int32_t *counts, const int32_t *pad_offsets, uint32_t *status,
+                         uint64_t wait_ns, cudaStream_t st)
+{
+    const bool mx = dm.dtype == MOK_MXFP8;
+    const uint32_t box = mx ? 128 : 64;
+    const uint64_t EF = static_cast<uint64_t>(dm.E) * dm.F;
+    const uint64_t Ed = static_cast<uint64_t>(dm.E) * dm.d;
+    const void *wdT = mx ? static_cast<const void *>(w->qt_down) : w->wt_down;
+    const void *wgT = mx ? static_cast<const void *>(w->qt_gate) : w->wt_gate;
+    const void *wuT = mx ? static_cast<const void *>(w->qt_up) : w->wt_up;
+    AMaps<2> a2 = {}, a1 = {};
+    CUtensorMap bdT, bgT, buT;
+    if (encode_tmap_2d(&a2.m[0], mx ? static_cast<const void *>(b.dy_q) : b.dy, mx, dm.d, dm.rows_pad, box, kBM) ||
+        encode_tmap_2d(&bdT, wdT, mx, dm.d, EF, box, 128) ||
+        encode_tmap_2d(&a1.m[0], mx ? static_cast<const void *>(b.da_q) : b.da, mx, dm.F, dm.rows_pad, box, kBM) ||
+        encode_tmap_2d(&a1.m[1], mx ? static_cast<const void *>(b.db_q) : b.db, mx, dm.F, dm.rows_pad, box, kBM) ||
+        encode_tmap_2d(&bgT, wgT, mx, dm.F, Ed, box, 128) ||
+        encode_tmap_2d(&buT, wuT, mx, dm.F, Ed, box, 128))
+        return cudaErrorInvalidValue;
+    a2.n = 1;
+    a1.n = 2;
+    GemmArgs g = base_args(dm, status, wait_ns);
+    g.counts = counts;
+    g.pad_offsets = pad_offsets;
+
+    // dh = dy W_d (K = d) -> SwiGLU backward -> da, db
+    GemmArgs g2 = g;
+    g2.BN = dm.F % 256 == 0 ? 256 : 128;
+    g2.n_tiles = dm.F / g2.BN;
+    g2.k_stages = dm.d / static_cast<int>(box);
+    g2.b_rows_per_group = dm.F;
+    g2.sfa[0] = b.dy_s;
+    g2.sfa_rows[0] = dm.rows_pad;
+    g2.sfb[0] = g2.sfb[1] = w->st_down;
+    g2.sfb_rows[0] = g2.sfb_rows[1] = static_cast<int64_t>(EF);
+    g2.in_a = b.saved_a;
+    g2.in_b = b.saved_b;
+    g2.out_da = b.da;
+    g2.out_db = b.db;
+    g2.q_da = b.da_q;
+    g2.q_db = b.db_q;
+    g2.s_da = b.da_s;
+    g2.s_db = b.db_s;
+    g2.h_rows = dm.rows_pad;
+    cudaError_t err = mx ? launch_gemm<MODE_DGRAD2, true>(a2, bdT, bdT, g2, st)
+                         : launch_gemm<MODE_DGRAD2, false>(a2, bdT, bdT, g2, st);
+    if (err != cudaSuccess) return err;
+
+    // dx = da W_g + db W_u (K = 2F)
+    GemmArgs g1 = g;
+    g1.BN = dm.d % 256 == 0 ? 256 : 128;
+    g1.n_tiles = dm.d / g1.BN;
+    g1.ks_half = dm.F / static_cast<int>(box);
+    g1.k_stages = 2 * g1.ks_half;
+    g1.b_rows_per_group = dm.d;
+    g1.sfa[0] = b.da_s;
+    g1.sfa[1] = b.db_s;
+    g1.sfa_rows[0] = g1.sfa_rows[1] = dm.rows_pad;
+    g1.sfb[0] = w->st_gate;
+    g1.sfb[1] = w->st_up;
+    g1.sfb_rows[0] = g1.sfb_rows[1] = static_cast<int64_t>(Ed);
+    g1.out_rows = b.dx;
+    return mx ? launch_gemm<MODE_DGRAD1, true>(a1, bgT, buT, g1, st)
+              : launch_gemm<MODE_DGRAD1, false>(a1, bgT, buT, g1, st);
+}
+
+cudaError_t launch_wgrad(const Dims &dm, const void *A_T, const uint32_t *A_s, int64_t a_rows,
+                         const void *B_T, const uint32_t *B_s, int64_t b_rows,
+                         const int32_t *pad_offsets, uint16_t *dW, uint32_t *status,
+                         uint64_t wait_ns, cudaStream_t st)
+{
+    const bool mx = dm.dtype == MOK_MXFP8;
+    const uint32_t box = mx ? 128 : 64;
+    AMaps<2> am = {};
+    CUtensorMap bm;
+    if (encode_tmap_2d(&am.m[0], A_T, mx, dm.rows_pad, a_rows, box, kBM) ||
+        encode_tmap_2d(&bm, B_T, mx, dm.rows_pad, b_rows, box, 128))
+        return cudaErrorInvalidValue;
+    am.n = 1;
+    GemmArgs g = base_args(dm, status, wait_ns);
+    g.pad_offsets = pad_offsets;
+    g.BN = b_rows % 256 == 0 ? 256 : 128;
+    g.n_tiles = static_cast<int>(b_rows / g.BN);
+    g.m_rows = static_cast<int>(a_rows);
+    g.sfa[0] = A_s;
+    g.sfa_rows[0] = a_rows;
+    g.sfb[0] = g.sfb[1] = B_s;
+    g.sfb_rows[0] = g.sfb_rows[1] = b_rows;
+    g.out_rows = dW;
+    g.out_ld = b_rows;
+    return mx ? launch_gemm<MODE_WGRAD, true>(am, bm, bm, g, st)
+              : launch_gemm<MODE_WGRAD, false>(am, bm, bm, g, st);
 }
 
 }  // namespace mok

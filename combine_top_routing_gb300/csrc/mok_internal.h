@@ -47,9 +47,30 @@ struct Dims {
     int nchunks;            // layout chunks of kLayoutChunk slots
 };
 
-constexpr int kLayoutChunk = 1024;
+constexpr int kLayoutChunk = 256;
+
+// Device buffers of the backward (carved from the backward workspace).
+struct BwdBufs {
+    uint16_t *dy;                 // BF16 [rows_pad, d] dy of each slot row
+    uint8_t *dy_q;                // MXFP8 codes of dy along d
+    uint32_t *dy_s;
+    const uint16_t *saved_a, *saved_b, *saved_h;  // BF16 [rows_pad, F] from the forward
+    uint16_t *da, *db;            // BF16 [rows_pad, F]
+    uint8_t *da_q, *db_q;         // MXFP8 along F
+    uint32_t *da_s, *db_s;
+    uint16_t *dx;                 // BF16 [rows_pad, d]
+    void *dyT, *hT, *daT, *dbT, *xT;              // [X, rows_pad] wgrad operands
+    uint32_t *dyT_s, *hT_s, *daT_s, *dbT_s, *xT_s;
+    float *dl_sel;                // [T, k] logit gradients of the chosen experts
+};
+
+struct BwdWs {
+    size_t status, dy, dy_q, dy_s, da, db, da_q, db_q, da_s, db_s, dx, dyT, hT, daT, dbT, xT,
+        dyT_s, hT_s, daT_s, dbT_s, xT_s, dl_sel, total;
+};
 
 int check_config(const mok_config *cfg, Dims *dm);
+void bwd_ws_layout(const Dims &dm, BwdWs *w);
 void fwd_ws_layout(const Dims &dm, FwdWs *w);
 void ctx_layout(const Dims &dm, mok_ctx_layout *c);
 int make_sources(const mok_config *cfg, const Dims &dm, const void *const *x_src, Sources *s);
@@ -82,6 +103,45 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
                        const uint8_t *row_j, void *h, uint32_t *h_scales, uint16_t *ystage,
                        uint16_t *saved_a, uint16_t *saved_b, uint16_t *saved_h,
                        uint32_t *status, uint64_t wait_ns, cudaStream_t st);
+
+#ifdef __CUDACC__
+__device__ __forceinline__ const uint16_t *source_row(const Sources &src, int t, int d)
+{
+    int lo = 0, hi = src.n;  // last s with row_start[s] <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (src.row_start[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    return src.ptr[lo] + static_cast<int64_t>(t - src.row_start[lo]) * d;
+}
+#endif
+
+cudaError_t launch_dgrad(const Dims &dm, const BwdBufs &b, const mok_weights *w,
+                         const int32_t *counts, const int32_t *pad_offsets, uint32_t *status,
+                         uint64_t wait_ns, cudaStream_t st);
+cudaError_t launch_wgrad(const Dims &dm, const void *A_T, const uint32_t *A_s, int64_t a_rows,
+                         const void *B_T, const uint32_t *B_s, int64_t b_rows,
+                         const int32_t *pad_offsets, uint16_t *dW, uint32_t *status,
+                         uint64_t wait_ns, cudaStream_t st);
+cudaError_t launch_rev_combine(const Dims &dm, const uint16_t *dY, const float *gates,
+                               const float *sel_scores, const int32_t *ids,
+                               const int32_t *slot_pos, const int32_t *offsets,
+                               const int32_t *pad_offsets, const uint16_t *ystage,
+                               const BwdBufs &b, float *dgates, float *dlogits, cudaStream_t st);
+cudaError_t launch_transpose_rows(const Dims &dm, const uint16_t *in, const Sources *src, int C,
+                                  const int32_t *counts, const int32_t *offsets,
+                                  const int32_t *pad_offsets, const int32_t *row_tok, void *out,
+                                  uint32_t *out_s, cudaStream_t st);
+cudaError_t launch_rev_dispatch(const Dims &dm, const int32_t *ids, const int32_t *slot_pos,
+                                const int32_t *offsets, const int32_t *pad_offsets,
+                                const uint16_t *dx_rows, const float *dl_sel, const float *W_r,
+                                uint16_t *dX, cudaStream_t st);
+cudaError_t launch_router_wgrad(const Dims &dm, const Sources &src, const int32_t *offsets,
+                                const int32_t *row_tok, const uint8_t *row_j, const float *dl_sel,
+                                float *dW_r, cudaStream_t st);
+cudaError_t launch_transpose_bf16(const uint16_t *src, int64_t batch, int64_t rows, int64_t K,
+                                  uint16_t *dst, cudaStream_t st);
 
 int num_sms();
 // Encodes a 2-D tiled tensor map with 128-byte swizzle; returns 0 on success.

@@ -291,4 +291,51 @@ __device__ __forceinline__ float mx_inv_scale(int x)
     return __uint_as_float(static_cast<uint32_t>(127 - x) << 23);
 }
 
+// ---------------------------------------------------------------- MX rows
+
+// Word index of (k-group g, row r) in the MX scale tile layout of a matrix
+// with `rows` rows (see mok.h).
+__device__ __forceinline__ int64_t mx_word_index(int64_t g, int64_t r, int64_t rows)
+{
+    return (g * (rows >> 7) + (r >> 7)) * 128 + (r & 31) * 4 + ((r & 127) >> 5);
+}
+
+// One warp quantises one 256-element stretch of a row: lane l converts
+// elements [8l, 8l+8), lanes 4b..4b+3 share MX block b, the amax is reduced
+// over those four lanes, and lanes 0 and 16 write the scale words of the two
+// 128-wide k-groups.  A 128-element tail passes nvalid = 16: every lane takes
+// part in the shuffles, lanes 16..31 write nothing.
+__device__ __forceinline__ void mx_quant_stretch(const uint4 raw, int lane, int nvalid,
+                                                 uint8_t *codes_row, int64_t col0,
+                                                 uint32_t *scales, int64_t scale_row,
+                                                 int64_t scale_rows)
+{
+    float f[8];
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+        f[2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const int x = mx_scale_exp(amax);
+    const float inv = mx_inv_scale(x);
+    uint2 out;
+    out.x = pack_e4m3x2(f[0] * inv, f[1] * inv) | (pack_e4m3x2(f[2] * inv, f[3] * inv) << 16);
+    out.y = pack_e4m3x2(f[4] * inv, f[5] * inv) | (pack_e4m3x2(f[6] * inv, f[7] * inv) << 16);
+    if (lane < nvalid) *reinterpret_cast<uint2 *>(codes_row + col0 + 8 * lane) = out;
+    // scale byte of block (lane/4) sits at byte (lane/4) % 4 of its k-group word
+    uint32_t word = static_cast<uint32_t>(x + 127) << (8 * ((lane >> 2) & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 4);
+    word |= __shfl_xor_sync(0xffffffffu, word, 8);
+    if ((lane & 15) == 0 && lane < nvalid) {
+        const int64_t g = (col0 + 8 * lane) >> 7;
+        scales[mx_word_index(g, scale_row, scale_rows)] = word;
+    }
+}
+
 }  // namespace mok

@@ -56,6 +56,39 @@ class MoELayer:
                 q["qt_" + name], q["st_" + name] = codes_t, scales_t
         self.wstruct = mok.weights_struct(q)
 
+    def prepare_backward(self, stream=None):
+        """Transposed weight copies the backward GEMMs read (K-major for dgrad)."""
+        w, E, F, d = self.w, self.w.E, self.w.F, self.w.d
+        q = self.weights
+        if w.dtype == "mxfp8":
+            if "qt_gate" not in q:
+                self.quantize_weights(transposed=True, stream=stream)
+        else:
+            for name, src, rows, K in (("gate", q["w_gate"], F, d), ("up", q["w_up"], F, d),
+                                       ("down", q["w_down"], d, F)):
+                t = torch.empty((E, K, rows), dtype=torch.bfloat16, device=self.device)
+                mok.transpose_bf16(src, E, rows, K, t, stream)
+                q["wt_" + name] = t
+            self.wstruct = mok.weights_struct(q)
+        if not hasattr(self, "bws"):
+            self.bws = torch.empty(mok.workspace_size(self.cfg)[2], dtype=torch.uint8,
+                                   device=self.device)
+            self.grads = {"d_gate": torch.empty((E, F, d), dtype=torch.bfloat16, device=self.device),
+                          "d_up": torch.empty((E, F, d), dtype=torch.bfloat16, device=self.device),
+                          "d_down": torch.empty((E, d, F), dtype=torch.bfloat16, device=self.device)}
+            self.gstruct = mok.weight_grads_struct(self.grads)
+            self.dX = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=self.device)
+            self.dgates = torch.empty((w.T, w.k), dtype=torch.float32, device=self.device)
+            self.dlogits = torch.empty((w.T, w.E), dtype=torch.float32, device=self.device)
+            self.dW_r = torch.empty((w.E, w.d), dtype=torch.float32, device=self.device)
+
+    def backward(self, dY, stream=None, dlogits=True):
+        assert self.ctx is not None, "backward needs a layer built with training=True"
+        mok.moe_backward(self.cfg, self.x_src, self.W_r, self.ctx, dY, self.wstruct, self.dX,
+                         self.gstruct, self.dgates, self.dlogits if dlogits else None, self.dW_r,
+                         self.bws, stream)
+        return self.dX
+
     def forward(self, stream=None):
         mok.moe_forward(self.cfg, self.x_src, self.W_r, self.bias, self.wstruct, self.out,
                         self.ctx, self.ws, stream)

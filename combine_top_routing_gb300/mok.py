@@ -26,7 +26,8 @@ MOK_MAX_SOURCES = 64
 EXPORTS = [
     "mok_max_padded_rows", "mok_workspace_size", "mok_saved_ctx_layout", "mok_route_layout",
     "mok_dispatch", "mok_expert_ffn", "mok_combine", "mok_moe_forward", "mok_moe_backward",
-    "mok_quantize_mx", "mok_reset_device_status", "mok_get_device_status", "mok_status_string",
+    "mok_quantize_mx", "mok_transpose_bf16", "mok_reset_device_status", "mok_get_device_status",
+    "mok_status_string",
 ]
 
 
@@ -44,7 +45,8 @@ class MokConfig(ctypes.Structure):
 class MokWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "w_gate", "w_up", "w_down", "q_gate", "q_up", "q_down", "s_gate", "s_up", "s_down",
-        "qt_gate", "qt_up", "qt_down", "st_gate", "st_up", "st_down")]
+        "qt_gate", "qt_up", "qt_down", "st_gate", "st_up", "st_down", "wt_gate", "wt_up",
+        "wt_down")]
 
 
 class MokWeightGrads(ctypes.Structure):
@@ -84,6 +86,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_moe_backward.argtypes = [cfgp, vp, vp, vp, vp, ctypes.POINTER(MokWeights), vp,
                                        ctypes.POINTER(MokWeightGrads), vp, vp, vp, vp, vp]
         L.mok_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp]
+        L.mok_transpose_bf16.argtypes = [vp, i64, i64, i64, vp, vp]
         L.mok_reset_device_status.argtypes = [vp, vp]
         L.mok_get_device_status.argtypes = [vp, vp]
         L.mok_status_string.argtypes = [ctypes.c_int]
@@ -217,6 +220,18 @@ def moe_backward(cfg, x_src, W_r, saved_ctx, dY, weights: MokWeights, dX, grads:
 def quantize_mx(src, batch, rows, K, transpose, codes, scales, stream=None):
     _check("mok_quantize_mx", lib().mok_quantize_mx(
         _ptr(src), batch, rows, K, int(transpose), _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def transpose_bf16(src, batch, rows, K, dst, stream=None):
+    _check("mok_transpose_bf16", lib().mok_transpose_bf16(_ptr(src), batch, rows, K, _ptr(dst),
+                                                          _stream(stream)))
+
+
+def weight_grads_struct(g: dict) -> MokWeightGrads:
+    s = MokWeightGrads()
+    for name, _ in MokWeightGrads._fields_:
+        setattr(s, name, _ptr(g[name]))
+    return s
 
 
 def reset_device_status(ws, stream=None):

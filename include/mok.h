@@ -100,6 +100,8 @@ typedef struct {
     const uint8_t *qt_gate, *qt_up;            /* device E4M3 [E, d, F] (W_g^T, W_u^T) */
     const uint8_t *qt_down;                    /* device E4M3 [E, F, d] (W_d^T) */
     const uint32_t *st_gate, *st_up, *st_down; /* device scales of the transposes */
+    const void *wt_gate, *wt_up;               /* device BF16 [E, d, F] (BF16 backward) */
+    const void *wt_down;                       /* device BF16 [E, F, d] (BF16 backward) */
 } mok_weights;
 
 typedef struct {
@@ -116,7 +118,7 @@ typedef struct {
 } mok_ctx_layout;
 
 /* Upper bound on padded expert-ordered rows: S + E*(MOK_ROW_ALIGN-1),
- * rounded up to MOK_ROW_ALIGN.  Returns 0 on a bad config. */
+ * rounded up to 256.  Returns 0 on a bad config. */
 int64_t mok_max_padded_rows(const mok_config *cfg);
 
 /* Workspace sizes in bytes: fwd_ws for mok_moe_forward and the step calls,
@@ -204,7 +206,11 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
 /*
  * Backward of mok_moe_forward ([kucoin] §01: backward runs two more rounds
  * of communication in reverse; §02: pull reverse-combine, push
- * reverse-dispatch).  Gradients of L = <dY, out>:
+ * reverse-dispatch).  saved_ctx is the forward's saved context (the forward
+ * must have been called with it); x_src and W_r are the forward's inputs.
+ * MXFP8 layers need w->qt_* / st_* (mok_quantize_mx, transpose = 1); BF16
+ * layers need w->wt_* (mok_transpose_bf16).  ws: bwd_ws bytes.
+ * Gradients of L = <dY, out>:
  *   dy_slot = g dY[t] (BF16), dgates = <dY[t], y_tj>; dh = dy W_d; SwiGLU
  *   backward with the saved a, b; dx_slot = da W_g + db W_u; dW_d = dy^T h,
  *   dW_g = da^T xe, dW_u = db^T xe per expert (BF16); dlogits through the
@@ -229,6 +235,11 @@ int mok_moe_backward(const mok_config *cfg, const void *const *x_src, const floa
  */
 int mok_quantize_mx(const void *src, int64_t batch, int64_t rows, int64_t K,
                     int transpose, uint8_t *codes, uint32_t *scales, void *stream);
+
+/* BF16 transpose of `batch` matrices [rows, K] into [K, rows] each (the
+ * transposed weights of the BF16 backward).  rows, K >= 1. */
+int mok_transpose_bf16(const void *src, int64_t batch, int64_t rows, int64_t K, void *dst,
+                       void *stream);
 
 /* Clears the device status word of a workspace (enqueued on stream). */
 int mok_reset_device_status(void *ws, void *stream);

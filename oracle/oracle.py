@@ -440,13 +440,13 @@ def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode):
     dx_rows = np.zeros((S, d))
     off = lay["offsets"]
     grads = {}
+    F = next(iter(fwd["experts"].values()))["a"].shape[1] if fwd["experts"] else 0
     for e in range(E):
         lo, hi = int(off[e]), int(off[e + 1])
-        Wg, Wu, Wd = get_expert(e)
         if hi == lo:
-            grads[e] = dict(dWd=np.zeros_like(_f64(Wd)), dWg=np.zeros_like(_f64(Wg)),
-                            dWu=np.zeros_like(_f64(Wu)))
+            grads[e] = dict(dWd=np.zeros((d, F)), dWg=np.zeros((F, d)), dWu=np.zeros((F, d)))
             continue
+        Wg, Wu, Wd = get_expert(e)
         f = fwd["experts"][e]
         a_s, b_s = (f["a"], f["b"]) if exact else (bf16_round(f["a"]), bf16_round(f["b"]))
         h_s = f["h"] if exact else bf16_round(f["h"])

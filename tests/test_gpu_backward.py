@@ -1,0 +1,154 @@
+"""GPU parity of the backward layer (B1-B6) against the oracle, and bit
+reproducibility.
+
+Small layers are compared in full: the oracle runs its own forward and
+backward from the BF16 inputs with the GPU's routing injected.  The
+DeepSeek-V3-shaped MXFP8 forward+backward is checked on sampled tokens (dX,
+dgates, dlogits) and on sampled experts for the weight gradients, where the
+oracle's wgrad step is fed the GPU's step-boundary operands (dy rows, saved
+h, da, db and the gathered x rows) and quantises them itself.  Tolerance:
+relative L2 <= 5e-3 and max-abs <= 2e-2 (BF16 / fp32-accumulated)."""
+import numpy as np
+import pytest
+import torch
+
+from combine_top_routing_gb300 import inputs as I
+from oracle import oracle as O
+from mokhelp import bf16_np, check_close, expert_weights_np, f32_np, make_layer, sha
+
+pytestmark = pytest.mark.gpu
+
+SMALL = {
+    "tiny": I.WORKLOADS["tiny"],
+    "bf16_ragged": I.Workload("bf16_ragged", T=300, d=256, E=8, k=2, F=384, dtype="bf16",
+                              router="softmax", seed=41),
+    "mx_ragged": I.Workload("mx_ragged", T=520, d=384, E=16, k=4, F=256, dtype="mxfp8",
+                            router="sigmoid", seed=42, zipf_alpha=0.46),
+    "mx_sources": I.Workload("mx_sources", T=512, d=512, E=32, k=8, F=384, dtype="mxfp8",
+                             router="sigmoid", seed=43, n_sources=4),
+    "bf16_many_empty": I.Workload("bf16_many_empty", T=16, d=256, E=64, k=2, F=256,
+                                  dtype="bf16", router="sigmoid", seed=44),
+}
+
+
+def _kind(w):
+    return O.SOFTMAX if w.router == "softmax" else O.SIGMOID
+
+
+def _run(w):
+    layer, inp = make_layer(w, training=True)
+    layer.prepare_backward()
+    layer.forward()
+    layer.backward(inp["dY"])
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    return layer, inp
+
+
+def _routing(layer, w):
+    ids = layer.ctx_view("ids", torch.int32, (w.T, w.k)).cpu().numpy()
+    gates = f32_np(layer.ctx_view("gates", torch.float32, (w.T, w.k)))
+    return ids, gates
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_backward_small_full_parity(name):
+    w = SMALL[name]
+    layer, inp = _run(w)
+    ids, gates = _routing(layer, w)
+    x = bf16_np(inp["x"])
+    Wr = f32_np(inp["Wr"])
+    bias = None if inp["bias"] is None else f32_np(inp["bias"])
+    ge = lambda e: expert_weights_np(inp, e)
+    f = O.forward(x, Wr, bias, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype, ids=ids, gates=gates)
+    g = O.backward(f, bf16_np(inp["dY"]), x, Wr, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype)
+    check_close(f32_np(layer.dgates), g["dgates"], what="dgates")
+    check_close(f32_np(layer.dlogits), g["dlogits"], what="dlogits")
+    check_close(bf16_np(layer.dX), g["dX"], what="dX")
+    check_close(f32_np(layer.dW_r), g["dWr"], what="dW_r")
+    dWg = np.stack([g["experts"][e]["dWg"] for e in range(w.E)])
+    dWu = np.stack([g["experts"][e]["dWu"] for e in range(w.E)])
+    dWd = np.stack([g["experts"][e]["dWd"] for e in range(w.E)])
+    check_close(bf16_np(layer.grads["d_gate"]), dWg, what="dW_g")
+    check_close(bf16_np(layer.grads["d_up"]), dWu, what="dW_u")
+    check_close(bf16_np(layer.grads["d_down"]), dWd, what="dW_d")
+    counts = np.bincount(ids.reshape(-1), minlength=w.E)
+    for e in np.where(counts == 0)[0]:
+        assert not layer.grads["d_gate"][e].any() and not layer.grads["d_down"][e].any()
+
+
+def test_backward_full_size_sampled():
+    w = I.WORKLOADS["dsv3_fwdbwd"]
+    layer, inp = _run(w)
+    ids, gates = _routing(layer, w)
+    rng = np.random.default_rng(7)
+    tokens = np.sort(rng.choice(w.T, 4, replace=False))
+    x = bf16_np(inp["x"])
+    Wr = f32_np(inp["Wr"])
+    ge = lambda e: expert_weights_np(inp, e)
+    f = O.forward(x, Wr, None, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype, tokens=tokens,
+                  ids=ids[tokens], gates=gates[tokens])
+    dY = bf16_np(inp["dY"][torch.from_numpy(tokens).cuda()])
+    g = O.backward(f, dY, x, Wr, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype)
+    tk = torch.from_numpy(tokens).cuda()
+    check_close(bf16_np(layer.dX[tk]), g["dX"], what="dX")
+    check_close(f32_np(layer.dgates[tk]), g["dgates"], what="dgates")
+    check_close(f32_np(layer.dlogits[tk]), g["dlogits"], what="dlogits")
+
+    # weight gradients of sampled experts from the GPU's step-boundary operands
+    bw = layer.bws
+    R = layer.rows_pad
+    counts = layer.ctx_view("counts", torch.int32, (w.E,)).cpu().numpy()
+    pad = layer.ctx_view("pad_offsets", torch.int32, (w.E + 1,)).cpu().numpy()
+    off = layer.ctx_view("offsets", torch.int32, (w.E + 1,)).cpu().numpy()
+    row_tok = layer.ctx_view("row_tok", torch.int32, (w.S,)).cpu().numpy()
+    h = layer.ctx_view("h", torch.bfloat16, (R, w.F))
+    fields = _bwd_offsets(layer)
+    dy_rows = bw[fields["dy"]:fields["dy"] + R * w.d * 2].view(torch.bfloat16).view(R, w.d)
+    da = bw[fields["da"]:fields["da"] + R * w.F * 2].view(torch.bfloat16).view(R, w.F)
+    db = bw[fields["db"]:fields["db"] + R * w.F * 2].view(torch.bfloat16).view(R, w.F)
+    for e in (int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))):
+        rows = slice(int(pad[e]), int(pad[e]) + int(counts[e]))
+        toks = row_tok[off[e]:off[e] + counts[e]]
+        ref = O.expert_wgrad(bf16_np(dy_rows[rows]), bf16_np(h[rows]), bf16_np(da[rows]),
+                             bf16_np(db[rows]), x[toks], w.dtype)
+        check_close(bf16_np(layer.grads["d_down"][e]), ref["dWd"], what=f"dW_d[{e}]")
+        check_close(bf16_np(layer.grads["d_gate"][e]), ref["dWg"], what=f"dW_g[{e}]")
+        check_close(bf16_np(layer.grads["d_up"][e]), ref["dWu"], what=f"dW_u[{e}]")
+        # router weight gradient of e: only tokens routed to e carry dlogits[:, e]
+        sel = np.where((ids == e).any(1))[0]
+        sc = f32_np(layer.ctx_view("sel_scores", torch.float32, (w.T, w.k)))
+        scores = np.zeros((len(sel), w.E))
+        np.put_along_axis(scores, ids[sel].astype(np.int64), sc[sel], 1)
+        rb = O.router_bwd(x[sel], Wr, scores, ids[sel], gates[sel], f32_np(layer.dgates)[sel], _kind(w))
+        check_close(f32_np(layer.dW_r[e]), rb["dWr"][e], what=f"dW_r[{e}]")
+
+
+def _bwd_offsets(layer):
+    """Byte offsets of the backward workspace fields (mirrors the library's
+    carving order: 256-byte aligned, in declaration order)."""
+    w = layer.w
+    R, d, F = layer.rows_pad, w.d, w.F
+    mx = w.dtype == "mxfp8"
+    sizes = [("status", 256), ("dy", R * d * 2), ("dy_q", R * d if mx else 0),
+             ("dy_s", R * d // 32 if mx else 0), ("da", R * F * 2), ("db", R * F * 2)]
+    out, cur = {}, 0
+    for name, n in sizes:
+        cur = (cur + 255) // 256 * 256
+        out[name] = cur
+        cur += n
+    return out
+
+
+def test_backward_bit_reproducible():
+    w = SMALL["mx_sources"]
+    layer, inp = make_layer(w, training=True)
+    layer.prepare_backward()
+    hashes = set()
+    for _ in range(3):
+        layer.forward()
+        layer.backward(inp["dY"])
+        hashes.add((sha(layer.dX), sha(layer.grads["d_gate"]), sha(layer.grads["d_down"]),
+                    sha(layer.dW_r), sha(layer.dgates)))
+    torch.cuda.synchronize()
+    assert len(hashes) == 1
