@@ -14,7 +14,7 @@ from combine_top_routing_gb300.layer import MoELayer
 from oracle import oracle as O
 
 # Tolerances for BF16 / fp32-accumulated outputs and gradients (GPU vs oracle):
-# relative L2 error, and max-abs error after dividing by max(1, RMS(ref)).
+# relative L2 error, and max-abs error |got - ref| / max(1, |ref|) elementwise.
 REL_L2 = 5e-3
 MAX_ABS = 2e-2
 
@@ -44,10 +44,9 @@ def check_close(got: np.ndarray, ref: np.ndarray, rel=REL_L2, mabs=MAX_ABS, what
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     err = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-    # max-abs in units of the tensor's own scale: unchanged for O(1) tensors,
-    # scale-aware for large ones (gate gradients are sums of d products)
-    scale = max(1.0, float(np.sqrt(np.mean(ref * ref)))) if ref.size else 1.0
-    mx = np.abs(got - ref).max() / scale if got.size else 0.0
+    # max-abs bound elementwise: absolute for |ref| <= 1, relative above (one
+    # BF16 ulp at |v| in [4, 8) is already 0.031 > 2e-2)
+    mx = (np.abs(got - ref) / np.maximum(1.0, np.abs(ref))).max() if got.size else 0.0
     assert err <= rel and mx <= mabs, f"{what}: rel_l2={err:.3e} max_abs={mx:.3e}"
     return err, mx
 
