@@ -63,6 +63,19 @@ def test_backward_small_full_parity(name):
     f = O.forward(x, Wr, bias, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype, ids=ids, gates=gates)
     g = O.backward(f, bf16_np(inp["dY"]), x, Wr, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype)
     check_close(f32_np(layer.dgates), g["dgates"], what="dgates")
+    # B1 at its step boundary: the GPU's own ystage and gates into the
+    # oracle's reverse-combine -- dy rows bit-exact, dgates to fp32 accuracy
+    ystage = bf16_np(layer.ctx_view("ystage", torch.bfloat16, (w.T, w.k, w.d)))
+    dy_ref, dg_ref = O.rev_combine(bf16_np(inp["dY"]), gates, ystage)
+    slot_pos = layer.ctx_view("slot_pos", torch.int32, (w.T, w.k)).cpu().numpy()
+    off = layer.ctx_view("offsets", torch.int32, (w.E + 1,)).cpu().numpy()
+    pad = layer.ctx_view("pad_offsets", torch.int32, (w.E + 1,)).cpu().numpy()
+    q = pad[ids] + slot_pos - off[ids]
+    R = layer.rows_pad
+    dy_rows = bf16_np(layer.bws[256:256 + R * w.d * 2].view(torch.bfloat16).view(R, w.d))
+    assert np.array_equal(dy_rows[q.reshape(-1)], dy_ref.reshape(-1, w.d))
+    dg = f32_np(layer.dgates)
+    assert np.all(np.abs(dg - dg_ref) <= 1e-5 * (1 + np.abs(dg_ref)) + 1e-6 * w.d)
     check_close(f32_np(layer.dlogits), g["dlogits"], what="dlogits")
     check_close(bf16_np(layer.dX), g["dX"], what="dX")
     check_close(f32_np(layer.dW_r), g["dWr"], what="dW_r")
