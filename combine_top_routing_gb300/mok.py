@@ -27,7 +27,7 @@ EXPORTS = [
     "mok_max_padded_rows", "mok_workspace_size", "mok_saved_ctx_layout", "mok_route_layout",
     "mok_dispatch", "mok_expert_ffn", "mok_combine", "mok_moe_forward", "mok_moe_backward",
     "mok_quantize_mx", "mok_transpose_bf16", "mok_reset_device_status", "mok_get_device_status",
-    "mok_status_string",
+    "mok_status_string", "mok_layout_static",
 ]
 
 
@@ -87,6 +87,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
                                        ctypes.POINTER(MokWeightGrads), vp, vp, vp, vp, vp]
         L.mok_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp]
         L.mok_transpose_bf16.argtypes = [vp, i64, i64, i64, vp, vp]
+        L.mok_layout_static.argtypes = [cfgp] + [vp] * 8
         L.mok_reset_device_status.argtypes = [vp, vp]
         L.mok_get_device_status.argtypes = [vp, vp]
         L.mok_status_string.argtypes = [ctypes.c_int]
@@ -232,6 +233,14 @@ def weight_grads_struct(g: dict) -> MokWeightGrads:
     for name, _ in MokWeightGrads._fields_:
         setattr(s, name, _ptr(g[name]))
     return s
+
+
+def layout_static(cfg, ids, counts, offsets, pad_offsets, slot_pos, row_tok, row_j,
+                  stream=None):
+    """The layout step with the library's own fixed scratch: no workspace."""
+    _check("mok_layout_static", lib().mok_layout_static(
+        cfg.ref, _ptr(ids), _ptr(counts), _ptr(offsets), _ptr(pad_offsets), _ptr(slot_pos),
+        _ptr(row_tok), _ptr(row_j), _stream(stream)))
 
 
 def reset_device_status(ws, stream=None):

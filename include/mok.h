@@ -241,6 +241,38 @@ int mok_quantize_mx(const void *src, int64_t batch, int64_t rows, int64_t K,
 int mok_transpose_bf16(const void *src, int64_t batch, int64_t rows, int64_t K, void *dst,
                        void *stream);
 
+/*
+ * Layout step without any caller-provided scratch.  No passage of the pages
+ * corresponds to this call: it is a convenience of this library.
+ *
+ * Who it is for: callers that cannot allocate device memory when they need
+ * the layout -- a host callback or a runtime that forbids CUDA API calls that
+ * synchronise the device (cudaMalloc and cudaFree may), an embedding that
+ * hands the library a fixed set of buffers with a hard memory budget, or a
+ * hot path that must not grow its allocator.  mok_route_layout needs a
+ * workspace for two per-chunk tables; this call keeps them in one 1 MiB array
+ * owned by the library instead, so it needs no workspace at all.
+ *
+ * Computes exactly what the layout part of mok_route_layout computes, from
+ * the routing ids [T, k] (device int32): counts, offsets, pad_offsets,
+ * slot_pos, row_tok, row_j, with the same layouts and the same bits.
+ *
+ * Limit: 2 * ceil(T*k / 256) * E <= 262144 (for example T*k = 131072 slots
+ * with E = 256 experts); larger layers return MOK_ERR_UNSUPPORTED and enqueue
+ * nothing.  It allocates nothing and calls no allocating routine.
+ * The first call on a device looks up the array's device address with that
+ * device current (once per device); make that first call before any stream
+ * capture.  Every GPU that loads the library holds the 1 MiB until the
+ * process exits.  All calls on a device share the one array, and each call
+ * overwrites what the previous one left there (nothing in it needs to start
+ * at zero), so two calls that can run at the same time on the GPU -- on
+ * different streams without ordering between them -- race and give wrong
+ * results; order them on one stream.
+ */
+int mok_layout_static(const mok_config *cfg, const int32_t *ids, int32_t *counts,
+                      int32_t *offsets, int32_t *pad_offsets, int32_t *slot_pos,
+                      int32_t *row_tok, uint8_t *row_j, void *stream);
+
 /* Clears the device status word of a workspace (enqueued on stream). */
 int mok_reset_device_status(void *ws, void *stream);
 
