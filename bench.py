@@ -37,6 +37,7 @@ def _args():
     p.add_argument("--impl", choices=["mok", "reference"], default="mok")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-backward", action="store_true")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
     p.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                    help="override a workload field (e.g. T=2048, E=32) for profiling runs")
@@ -72,7 +73,7 @@ def _peaks():
 class ClockSampler:
     """nvidia-smi clock / throttle sampling while the timed region runs."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -80,6 +81,10 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.file = None
+        self.window = None  # (t0, t1) host wall-clock of the timed region
+
+    def mark(self, t0: float, t1: float):
+        self.window = (t0, t1)
 
     def __enter__(self):
         try:
@@ -107,19 +112,30 @@ class ClockSampler:
         with open(self.file.name) as f:
             rows = [r.strip().split(",") for r in f if r.strip()]
         os.unlink(self.file.name)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        import datetime
+        parsed = []
         for r in rows:
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                parsed.append((ts, float(r[2]), float(r[3]), r[6:10]))
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
+        inside = parsed
+        if self.window and parsed:
+            t0, t1 = self.window
+            inside = [p for p in parsed if t0 - 0.05 <= p[0] <= t1 + 0.05]
+            if not inside:  # timed region shorter than the sampling period
+                inside = [min(parsed, key=lambda p: abs(p[0] - 0.5 * (t0 + t1)))]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for p in inside:
+            for n, v in zip(names, p[3]):
                 if v.strip().lower() == "active":
                     reasons.add(n)
+        sm = [p[1] for p in inside]
+        smax = [p[2] for p in inside]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else sm_max_default,
                 "reasons": sorted(reasons), "samples": len(sm)}
@@ -250,19 +266,21 @@ def main():
             dist.barrier()
 
     # ---------------- device-resident timed region
-    for _ in range(max(3, args.warmup)):
-        layer.forward()
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     peaks, peak_src = _peaks()
     with ClockSampler(local) as clk:
+        for _ in range(max(3, args.warmup)):
+            layer.forward()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.time()
         ev0.record(stream)
         for _ in range(args.steps):
             layer.forward()
         ev1.record(stream)
         torch.cuda.synchronize()
+        clk.mark(wall0, time.time())
     barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
     status = layer.status()
@@ -273,6 +291,34 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = world * w.T / (ms / 1e3)
+
+    # ---------------- forward + backward (training layer: saved context)
+    fb_ms = None
+    if not args.no_backward:
+        tl = MoELayer(w, inp, training=True)
+        tl.prepare_backward()
+        for _ in range(max(3, args.warmup)):
+            tl.forward()
+            tl.backward(inp["dY"])
+        torch.cuda.synchronize()
+        barrier()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        fb_steps = max(3, min(args.steps, 20))
+        f0.record(stream)
+        for _ in range(fb_steps):
+            tl.forward()
+            tl.backward(inp["dY"])
+        f1.record(stream)
+        torch.cuda.synchronize()
+        if tl.status() != 0:
+            raise RuntimeError("device status after backward: " + mok.status_string(tl.status()))
+        fb_ms = f0.elapsed_time(f1) / fb_steps
+        if world > 1:
+            t = torch.tensor([fb_ms], device="cuda")
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            fb_ms = float(t.item())
+        del tl
+        torch.cuda.empty_cache()
 
     # ---------------- the expert FFN (dominant kernels) timed alone, same stream
     R = _route_for_ffn(layer)
@@ -342,6 +388,9 @@ def main():
             "layer_roofline": {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
                                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /
                                            peaks.get("hbm_gbs", 6800.0)},
+            "fwd_bwd": None if fb_ms is None else {
+                "value": world * w.T / (fb_ms / 1e3), "unit": "tokens/s", "ms_per_step": fb_ms,
+                "tensor_frac": 3 * flops / (fb_ms / 1e3) / 1e12 / peak_tc},
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2},
             "gpu_launches": launches_per_step * args.steps,

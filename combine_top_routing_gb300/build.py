@@ -46,15 +46,20 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose: bool = False, out: str | None = None,
+          defines: tuple[str, ...] = ()) -> str:
+    """Compile and link; `out` / `defines` build a variant library elsewhere."""
+    lib_path = out or LIB
+    if not force and out is None and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD if out is None else out + ".objs"
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     jobs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-I", INCLUDE, "-c", src, "-o", obj]
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-I", INCLUDE, "-c", src,
+               "-o", obj]
         jobs.append((src, obj, cmd))
 
     def run(job):
@@ -70,13 +75,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
             if verbose and (r.stdout or r.stderr):
                 print(r.stdout, r.stderr)
     objs = [j[1] for j in jobs]
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":

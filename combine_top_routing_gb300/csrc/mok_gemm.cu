@@ -54,6 +54,10 @@ constexpr int kSfaBytes = 512;            // 128 rows x 4 scale bytes
 constexpr int kSfbBytes = 1024;           // 256 rows x 4 scale bytes
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 256;          // scale columns: 16 per stage after the accumulator
+#ifndef MOK_GEMM_CLUSTER
+#define MOK_GEMM_CLUSTER 1
+#endif
+constexpr int kCluster = MOK_GEMM_CLUSTER;  // CTAs per cluster of the GEMM launch
 
 enum { MODE_ROUTER = 0, MODE_FFN1, MODE_FFN2, MODE_DGRAD2, MODE_DGRAD1, MODE_WGRAD };
 
@@ -628,12 +632,52 @@ cudaError_t launch_gemm(const AMaps<MODE == MODE_ROUTER ? 64 : 2> &am, const CUt
     constexpr size_t smem = smem_bytes<MX>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
+    static int grid = 0;
     std::call_once(once, [] {
         attr_err = cudaFuncSetAttribute(k_gemm<MODE, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem));
+        grid = num_sms();
+        if (attr_err == cudaSuccess && kCluster > 1) {
+            // CTAs of a cluster share a GPC (so one die and its L2 partition):
+            // consecutive tiles -- the row tiles of one weight tile -- run side
+            // by side there.  The grid is the number of clusters that fit at once.
+            attr_err = cudaFuncSetAttribute(k_gemm<MODE, MX>,
+                                            cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = kCluster;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(grid / kCluster * kCluster));
+            cfg.blockDim = dim3(kThreads);
+            cfg.dynamicSmemBytes = smem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int clusters = 0;
+            if (attr_err == cudaSuccess)
+                attr_err = cudaOccupancyMaxActiveClusters(&clusters, k_gemm<MODE, MX>, &cfg);
+            if (attr_err == cudaSuccess) grid = clusters > 0 ? clusters * kCluster : 0;
+            if (grid == 0) attr_err = cudaErrorInvalidConfiguration;
+        }
     });
     if (attr_err != cudaSuccess) return attr_err;
-    k_gemm<MODE, MX><<<num_sms(), kThreads, smem, st>>>(am, b0, b1, args);
+    if (kCluster > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = kCluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, k_gemm<MODE, MX>, am, b0, b1, args);
+    }
+    k_gemm<MODE, MX><<<grid, kThreads, smem, st>>>(am, b0, b1, args);
     return cudaGetLastError();
 }
 
