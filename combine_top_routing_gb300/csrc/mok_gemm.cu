@@ -217,6 +217,38 @@ __device__ __forceinline__ int64_t scale_word_row(int64_t g, int64_t r, int64_t 
     return (g * (rows >> 7) + (r >> 7)) * 128 + (r & 31) * 4 + ((r & 127) >> 5);
 }
 
+// Reads BN (<= 256) fp32 accumulator columns of this thread's TMEM lane into
+// packed BF16 pairs (zeros when `zero`), 64 columns per TMEM wait.
+__device__ __forceinline__ void drain_row_bf16(uint32_t trow, int BN, bool zero, uint32_t (&pk)[128])
+{
+#pragma unroll
+    for (int c = 0; c < 256; c += 64) {
+        if (c < BN) {
+            uint32_t v0[32], v1[32];
+            if (!zero) {
+                tmem_ld_32x32(trow + c, v0);
+                tmem_ld_32x32(trow + c + 32, v1);
+                tmem_ld_wait();
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                pk[c / 2 + i] = zero ? 0u : pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+                pk[c / 2 + 16 + i] =
+                    zero ? 0u : pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            }
+        }
+    }
+}
+
+// Stores BN packed BF16 values (16-byte stores).
+__device__ __forceinline__ void store_row_bf16(uint16_t *dst, int BN, const uint32_t (&pk)[128])
+{
+    uint4 *o = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int c = 0; c < 256; c += 8)
+        if (c < BN) o[c / 8] = make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
+}
+
 template <int MODE>
 __device__ __forceinline__ int group_row_tiles(const AMaps<MODE == MODE_ROUTER ? 64 : 2> &am,
                                                const GemmArgs &a, int g)
@@ -432,6 +464,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
             if (!wait_bar(acc_full, acc_phase, a, abort_flag)) break;
             tc_fence_after();
+            // Hands the accumulator back to the MMA warp; epilogues that first
+            // drain their row into registers call it before their global stores,
+            // so the stores overlap the next tile's main loop.
+            bool released = false;
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                released = true;
+            };
             if constexpr (MODE == MODE_ROUTER) {
                 const int lrow = tl.m_blk * kBM + r;
                 const bool valid = lrow < am.rows[tl.group];
@@ -457,6 +499,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t grow = a.pad_offsets[e] + row_in_e;
                 const int f0 = tl.n_blk * 128;
                 uint32_t sword = 0;
+                if (!a.saved_a && !a.saved_b && !a.saved_h) {
+                    // inference: h for the row's 128 columns into registers, release, store
+                    uint32_t hq[64];  // BF16 pairs (64) or E4M3 quads (32)
+#pragma unroll
+                    for (int c = 0; c < 128; c += 32) {
+                        uint32_t gv[32], uv[32];
+                        tmem_ld_32x32(trow + c, gv);
+                        tmem_ld_32x32(trow + 128 + c, uv);
+                        tmem_ld_wait();
+                        float hv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float av = __uint_as_float(gv[i]);
+                            hv[i] = av / (1.0f + __expf(-av)) * __uint_as_float(uv[i]);
+                        }
+                        if (!MX) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) hq[c / 2 + i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
+                        } else {
+                            float amax = 0.0f;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
+                            const int x = mx_scale_exp(amax);
+                            const float inv = mx_inv_scale(x);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                hq[c / 4 + i] = pack_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
+                                                (pack_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
+                            sword |= static_cast<uint32_t>(x + 127) << (8 * (c >> 5));
+                        }
+                    }
+                    release();
+                    if (valid) {
+                        const int64_t off = grow * a.F + f0;
+                        if (!MX) {
+                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.h) + off);
+#pragma unroll
+                            for (int q = 0; q < 16; ++q)
+                                o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
+                        } else {
+                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.h) + off);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q)
+                                o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
+                            a.h_scales[scale_word_row(f0 >> 7, grow, a.h_rows)] = sword;
+                        }
+                    }
+                } else
                 for (int c = 0; c < 128; c += 32) {
                     uint32_t gv[32], uv[32];
                     tmem_ld_32x32(trow + c, gv);
@@ -491,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (MX && valid) a.h_scales[scale_word_row(f0 >> 7, grow, a.h_rows)] = sword;
+                if (MX && valid && !released) a.h_scales[scale_word_row(f0 >> 7, grow, a.h_rows)] = sword;
             } else if constexpr (MODE == MODE_FFN2) {
                 const int e = tl.group;
                 const int row_in_e = tl.m_blk * kBM + r;
@@ -503,17 +593,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t j = a.row_j[p];
                     dst = a.ystage + (t * a.k_top + j) * a.d + tl.n_blk * BN;
                 }
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32(trow + c, v);
-                    tmem_ld_wait();
-                    if (valid) {
-                        float f[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-                        store_bf16x32(dst + c, f);
-                    }
-                }
+                uint32_t pk[128];
+                drain_row_bf16(trow, BN, false, pk);
+                release();
+                if (valid) store_row_bf16(dst, BN, pk);
             } else if constexpr (MODE == MODE_DGRAD2) {
                 // dh -> SwiGLU backward with the saved (BF16) a, b:
                 //   s = sigmoid(a), da = dh b s (1 + a (1 - s)), db = dh a s
@@ -566,41 +649,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = row_in_e < a.counts[e];
                 const int64_t grow = a.pad_offsets[e] + row_in_e;
                 uint16_t *dst = a.out_rows + grow * a.d + tl.n_blk * BN;
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t v[32];
-                    tmem_ld_32x32(trow + c, v);
-                    tmem_ld_wait();
-                    if (valid) {
-                        float f[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-                        store_bf16x32(dst + c, f);
-                    }
-                }
+                uint32_t pk[128];
+                drain_row_bf16(trow, BN, false, pk);
+                release();
+                if (valid) store_row_bf16(dst, BN, pk);
             } else {  // MODE_WGRAD
                 const int e = tl.group;
                 const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
                 uint16_t *dst = a.out_rows +
                                 (static_cast<int64_t>(e) * a.m_rows + tl.m_blk * kBM + r) * a.out_ld +
                                 tl.n_blk * BN;
-                for (int c = 0; c < BN; c += 32) {
-                    float f[32];
-                    if (!empty_k) {
-                        uint32_t v[32];
-                        tmem_ld_32x32(trow + c, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) f[i] = 0.0f;
-                    }
-                    store_bf16x32(dst + c, f);
-                }
+                uint32_t pk[128];
+                drain_row_bf16(trow, BN, empty_k, pk);
+                release();
+                store_row_bf16(dst, BN, pk);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (!released) release();
             acc_phase ^= 1u;
         }
     }
