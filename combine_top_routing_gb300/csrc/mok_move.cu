@@ -45,10 +45,22 @@ __global__ void __launch_bounds__(256) k_dispatch(const Sources src, int64_t S, 
             for (int c = lane; c < d / 8; c += 32) out[c] = __ldg(in + c);
         } else {
             uint8_t *codes_row = static_cast<uint8_t *>(xe) + q * d;
-            for (int c0 = 0; c0 < d; c0 += 256) {
-                const int nvalid = d - c0 >= 256 ? 32 : 16;
-                const uint4 raw = lane < nvalid ? __ldg(in + (c0 >> 3) + lane) : make_uint4(0, 0, 0, 0);
-                mx_quant_stretch(raw, lane, nvalid, codes_row, c0, xe_scales, q, rows_pad);
+            // four 256-element stretches per step: their loads are in flight together
+            for (int c0 = 0; c0 < d; c0 += 1024) {
+                uint4 raw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int cu = c0 + 256 * u;
+                    const int nvalid = cu >= d ? 0 : (d - cu >= 256 ? 32 : 16);
+                    raw[u] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int cu = c0 + 256 * u;
+                    if (cu < d)
+                        mx_quant_stretch(raw[u], lane, d - cu >= 256 ? 32 : 16, codes_row, cu,
+                                         xe_scales, q, rows_pad);
+                }
             }
         }
     }

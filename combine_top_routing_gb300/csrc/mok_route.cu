@@ -155,18 +155,23 @@ cudaError_t launch_topk(const Dims &dm, const float *logits, int32_t *ids, float
 }
 
 // ---------------------------------------------------------------------------
-// Layout: a stable counting sort of the S = T*k slots by expert, in three
-// integer passes over chunks of kLayoutChunk consecutive slots.
-//   count: per-chunk histogram (shared-memory integer atomics);
-//   scan : per expert, exclusive prefix over chunks; counts, dense offsets,
-//          padded offsets (segments rounded up to MOK_ROW_ALIGN rows);
-//   place: one warp walks its chunk 32 slots at a time in slot order; lanes
-//          with equal expert get consecutive ranks (match + popc), so a slot's
-//          row is offsets[e] + (slots of e before it) -- stable by t*k+j.
+// Layout: a stable counting sort of the S = T*k slots by expert, in integer
+// passes over chunks of kLayoutChunk consecutive slots.  The per-chunk tables
+// are expert-major ([E][nchunks]) so that one expert's chunks are contiguous.
+//   count        : per-chunk histogram (shared-memory integer atomics);
+//   scan_chunks  : one block per expert, exclusive prefix over its chunks
+//                  (relative to the expert's first row) and its total count;
+//   scan_experts : dense offsets and padded offsets (segments rounded up to
+//                  MOK_ROW_ALIGN rows) from the counts;
+//   place        : one warp walks its chunk 32 slots at a time in slot order;
+//                  lanes with equal expert get consecutive ranks (match +
+//                  popc), so a slot's row is offsets[e] + (slots of e before
+//                  it) -- stable by t*k+j.
 // Everything is integer, so the result is the same on every run.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_layout_count(const int32_t *__restrict__ ids, int64_t S,
-                                                      int E, int32_t *__restrict__ chunk_counts)
+                                                      int E, int nchunks,
+                                                      int32_t *__restrict__ chunk_counts)
 {
     extern __shared__ int32_t hist[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
@@ -176,30 +181,60 @@ __global__ void __launch_bounds__(256) k_layout_count(const int32_t *__restrict_
     for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) atomicAdd(&hist[ids[i]], 1);
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
-        chunk_counts[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+        chunk_counts[static_cast<int64_t>(e) * nchunks + blockIdx.x] = hist[e];
 }
 
-__global__ void __launch_bounds__(1024) k_layout_scan(const int32_t *__restrict__ chunk_counts,
-                                                      int nchunks, int E,
-                                                      int32_t *__restrict__ chunk_base,
-                                                      int32_t *__restrict__ counts,
-                                                      int32_t *__restrict__ offsets,
-                                                      int32_t *__restrict__ pad_offsets)
+// Block-wide exclusive scan of `v` (256 threads); returns the block total.
+__device__ __forceinline__ int32_t block_excl_scan256(int32_t v, int32_t *excl, int32_t *s_warp)
 {
-    __shared__ int32_t s_cnt[MOK_MAX_EXPERTS];
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[wid] = incl;
+    __syncthreads();
+    int32_t base = 0, total = 0;
+    for (int w = 0; w < 8; ++w) {
+        if (w < wid) base += s_warp[w];
+        total += s_warp[w];
+    }
+    __syncthreads();
+    *excl = base + incl - v;
+    return total;
+}
+
+__global__ void __launch_bounds__(256) k_layout_scan_chunks(const int32_t *__restrict__ chunk_counts,
+                                                            int nchunks,
+                                                            int32_t *__restrict__ chunk_base,
+                                                            int32_t *__restrict__ counts)
+{
+    __shared__ int32_t s_warp[8];
+    const int e = blockIdx.x;
+    const int32_t *cc = chunk_counts + static_cast<int64_t>(e) * nchunks;
+    int32_t *cb = chunk_base + static_cast<int64_t>(e) * nchunks;
+    int32_t carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 256) {
+        const int c = c0 + threadIdx.x;
+        const int32_t v = c < nchunks ? cc[c] : 0;
+        int32_t excl;
+        const int32_t total = block_excl_scan256(v, &excl, s_warp);
+        if (c < nchunks) cb[c] = carry + excl;
+        carry += total;
+    }
+    if (threadIdx.x == 0) counts[e] = carry;
+}
+
+__global__ void __launch_bounds__(1024) k_layout_scan_experts(const int32_t *__restrict__ counts,
+                                                              int E, int32_t *__restrict__ offsets,
+                                                              int32_t *__restrict__ pad_offsets)
+{
     __shared__ int32_t s_warp[2][32];
     const int e = threadIdx.x;
-    int32_t run = 0;
-    if (e < E) {
-        for (int c = 0; c < nchunks; ++c) {
-            chunk_base[static_cast<int64_t>(c) * E + e] = run;
-            run += chunk_counts[static_cast<int64_t>(c) * E + e];
-        }
-        counts[e] = run;
-    }
-    // block-wide exclusive scans of counts and padded counts over e
-    const int32_t cnt = e < E ? run : 0;
-    const int32_t pad = e < E ? static_cast<int32_t>(round_up(run, MOK_ROW_ALIGN)) : 0;
+    const int32_t cnt = e < E ? counts[e] : 0;
+    const int32_t pad = static_cast<int32_t>(round_up(cnt, MOK_ROW_ALIGN));
     const int lane = e & 31, wid = e >> 5;
     int32_t ic = cnt, ip = pad;
 #pragma unroll
@@ -217,8 +252,8 @@ __global__ void __launch_bounds__(1024) k_layout_scan(const int32_t *__restrict_
     }
     __syncthreads();
     if (wid == 0) {
-        int32_t a = lane < (blockDim.x >> 5) ? s_warp[0][lane] : 0;
-        int32_t b = lane < (blockDim.x >> 5) ? s_warp[1][lane] : 0;
+        int32_t a = s_warp[0][lane];
+        int32_t b = s_warp[1][lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int32_t x = __shfl_up_sync(0xffffffffu, a, o);
@@ -232,12 +267,9 @@ __global__ void __launch_bounds__(1024) k_layout_scan(const int32_t *__restrict_
         s_warp[1][lane] = b;
     }
     __syncthreads();
-    const int32_t base_c = wid ? s_warp[0][wid - 1] : 0;
-    const int32_t base_p = wid ? s_warp[1][wid - 1] : 0;
-    const int32_t excl_c = base_c + ic - cnt;
-    const int32_t excl_p = base_p + ip - pad;
+    const int32_t excl_c = (wid ? s_warp[0][wid - 1] : 0) + ic - cnt;
+    const int32_t excl_p = (wid ? s_warp[1][wid - 1] : 0) + ip - pad;
     if (e < E) {
-        s_cnt[e] = excl_c;
         offsets[e] = excl_c;
         pad_offsets[e] = excl_p;
         if (e == E - 1) {
@@ -245,21 +277,20 @@ __global__ void __launch_bounds__(1024) k_layout_scan(const int32_t *__restrict_
             pad_offsets[E] = excl_p + pad;
         }
     }
-    __syncthreads();
-    if (e < E)
-        for (int c = 0; c < nchunks; ++c) chunk_base[static_cast<int64_t>(c) * E + e] += s_cnt[e];
 }
 
 __global__ void __launch_bounds__(32) k_layout_place(const int32_t *__restrict__ ids, int64_t S,
-                                                     int k, int E,
+                                                     int k, int E, int nchunks,
                                                      const int32_t *__restrict__ chunk_base,
+                                                     const int32_t *__restrict__ offsets,
                                                      int32_t *__restrict__ slot_pos,
                                                      int32_t *__restrict__ row_tok,
                                                      uint8_t *__restrict__ row_j)
 {
     extern __shared__ int32_t run[];
     const int lane = threadIdx.x;
-    for (int e = lane; e < E; e += 32) run[e] = chunk_base[static_cast<int64_t>(blockIdx.x) * E + e];
+    for (int e = lane; e < E; e += 32)
+        run[e] = offsets[e] + chunk_base[static_cast<int64_t>(e) * nchunks + blockIdx.x];
     __syncwarp();
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * kLayoutChunk;
     const int64_t hi = lo + kLayoutChunk < S ? lo + kLayoutChunk : S;
@@ -288,15 +319,17 @@ cudaError_t launch_layout(const Dims &dm, const int32_t *ids, int32_t *counts, i
                           cudaStream_t st)
 {
     const size_t hist_bytes = static_cast<size_t>(dm.E) * sizeof(int32_t);
-    k_layout_count<<<dm.nchunks, 256, hist_bytes, st>>>(ids, dm.S, dm.E, chunk_counts);
+    k_layout_count<<<dm.nchunks, 256, hist_bytes, st>>>(ids, dm.S, dm.E, dm.nchunks, chunk_counts);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    k_layout_scan<<<1, 1024, 0, st>>>(chunk_counts, dm.nchunks, dm.E, chunk_base, counts, offsets,
-                                      pad_offsets);
+    k_layout_scan_chunks<<<dm.E, 256, 0, st>>>(chunk_counts, dm.nchunks, chunk_base, counts);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    k_layout_place<<<dm.nchunks, 32, hist_bytes, st>>>(ids, dm.S, dm.k, dm.E, chunk_base,
-                                                        slot_pos, row_tok, row_j);
+    k_layout_scan_experts<<<1, 1024, 0, st>>>(counts, dm.E, offsets, pad_offsets);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    k_layout_place<<<dm.nchunks, 32, hist_bytes, st>>>(ids, dm.S, dm.k, dm.E, dm.nchunks, chunk_base,
+                                                        offsets, slot_pos, row_tok, row_j);
     return cudaGetLastError();
 }
 

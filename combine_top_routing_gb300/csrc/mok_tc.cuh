@@ -1,0 +1,141 @@
+// mok_tc.cuh -- building blocks shared by the tcgen05 GEMM kernels: tile and
+// pipeline constants, bounded waits, and the register-level epilogue helpers
+// (BF16 packing, MXFP8 block quantisation, MX scale tile addressing).
+#pragma once
+
+#include "mok.h"
+#include "mok_ptx.cuh"
+
+namespace mok {
+
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;
+constexpr int kAStage = kBM * kBKBytes;   // 16 KB
+constexpr int kBStage = 256 * kBKBytes;   // 32 KB
+constexpr int kSfaBytes = 512;            // 128 rows x 4 scale bytes
+constexpr int kSfbBytes = 1024;           // 256 rows x 4 scale bytes
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSfCol = 256;          // scale columns: 16 per stage after the accumulator
+
+
+__device__ __noinline__ void report_timeout(uint32_t *status, volatile int *abort_flag)
+{
+    *abort_flag = 1;
+    if (status) atomicMax(status, static_cast<uint32_t>(MOK_ERR_TIMEOUT));
+}
+
+// Bounded mbarrier wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                         uint64_t wait_ns, volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > wait_ns) {
+                report_timeout(status, abort_flag);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void store_bf16x32(uint16_t *dst, const float *v)
+{
+    uint4 *o = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+        w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+        w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+        w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+        o[q] = w;
+    }
+}
+
+__device__ __forceinline__ void load_bf16x32(const uint16_t *src, float *v)
+{
+    const uint4 *p = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint4 w = p[q];
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[8 * q + 2 * i] = bf16_bits_to_float(u[i] & 0xFFFFu);
+            v[8 * q + 2 * i + 1] = bf16_bits_to_float(u[i] >> 16);
+        }
+    }
+}
+
+// 32 fp32 values -> one MX block: 32 E4M3 codes at dst (16-byte aligned);
+// returns the E8M0 scale byte.
+__device__ __forceinline__ uint32_t quant_mx32(const float *v, uint8_t *dst)
+{
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int x = mx_scale_exp(amax);
+    const float inv = mx_inv_scale(x);
+    uint4 *o = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        const float *s = v + 16 * q;
+        uint4 w;
+        w.x = pack_e4m3x2(s[0] * inv, s[1] * inv) | (pack_e4m3x2(s[2] * inv, s[3] * inv) << 16);
+        w.y = pack_e4m3x2(s[4] * inv, s[5] * inv) | (pack_e4m3x2(s[6] * inv, s[7] * inv) << 16);
+        w.z = pack_e4m3x2(s[8] * inv, s[9] * inv) | (pack_e4m3x2(s[10] * inv, s[11] * inv) << 16);
+        w.w = pack_e4m3x2(s[12] * inv, s[13] * inv) | (pack_e4m3x2(s[14] * inv, s[15] * inv) << 16);
+        o[q] = w;
+    }
+    return static_cast<uint32_t>(x + 127);
+}
+
+__device__ __forceinline__ int64_t scale_word(int64_t x_elem, int64_t row, int64_t rows)
+{
+    return ((x_elem >> 7) * (rows >> 7) + (row >> 7)) * 128;
+}
+
+__device__ __forceinline__ int64_t scale_word_row(int64_t g, int64_t r, int64_t rows)
+{
+    return (g * (rows >> 7) + (r >> 7)) * 128 + (r & 31) * 4 + ((r & 127) >> 5);
+}
+
+// Reads BN (<= 256) fp32 accumulator columns of this thread's TMEM lane into
+// packed BF16 pairs (zeros when `zero`), 64 columns per TMEM wait.
+__device__ __forceinline__ void drain_row_bf16(uint32_t trow, int BN, bool zero, uint32_t (&pk)[128])
+{
+#pragma unroll
+    for (int c = 0; c < 256; c += 64) {
+        if (c < BN) {
+            uint32_t v0[32], v1[32];
+            if (!zero) {
+                tmem_ld_32x32(trow + c, v0);
+                tmem_ld_32x32(trow + c + 32, v1);
+                tmem_ld_wait();
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                pk[c / 2 + i] = zero ? 0u : pack_bf16x2(__uint_as_float(v0[2 * i]), __uint_as_float(v0[2 * i + 1]));
+                pk[c / 2 + 16 + i] =
+                    zero ? 0u : pack_bf16x2(__uint_as_float(v1[2 * i]), __uint_as_float(v1[2 * i + 1]));
+            }
+        }
+    }
+}
+
+// Stores BN packed BF16 values (16-byte stores).
+__device__ __forceinline__ void store_row_bf16(uint16_t *dst, int BN, const uint32_t (&pk)[128])
+{
+    uint4 *o = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int c = 0; c < 256; c += 8)
+        if (c < BN) o[c / 8] = make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
+}
+
+}  // namespace mok
