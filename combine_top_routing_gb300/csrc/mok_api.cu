@@ -101,6 +101,7 @@ void fwd_ws_layout(const Dims &dm, FwdWs *w)
     w->h = take(&cur, static_cast<size_t>(dm.rows_pad) * dm.F * esize);
     w->h_scales = take(&cur, dm.dtype == MOK_MXFP8 ? static_cast<size_t>(dm.rows_pad) * dm.F / 32 : 0);
     w->ystage = take(&cur, static_cast<size_t>(dm.S) * dm.d * 2);
+    w->counters = take(&cur, static_cast<size_t>(fused_counter_ints(dm)) * 4);
     w->total = (cur + kAlign - 1) / kAlign * kAlign;
 }
 
@@ -396,6 +397,11 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     if (!mx && (!w->w_gate || !w->w_up || !w->w_down)) return MOK_ERR_INVALID_ARG;
     Sources src;
     if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    {
+        // the token ring must hold at least one minibatch of every size (256 rows)
+        const int64_t ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
+        if (ring_rows < 256) return MOK_ERR_INVALID_ARG;
+    }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     FwdWs fw;
     fwd_ws_layout(dm, &fw);
@@ -409,17 +415,27 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     if (e != cudaSuccess) return MOK_ERR_CUDA;
     rc = route_layout_impl(cfg, dm, src, W_r, bias, o, ws, st);
     if (rc != MOK_OK) return rc;
-    e = launch_dispatch(dm, src, o.ids, o.offsets, o.pad_offsets, o.row_tok, o.row_j,
-                        at<void>(ws, fw.xe), mx ? at<uint32_t>(ws, fw.xe_scales) : nullptr, st);
-    if (e == cudaSuccess)
-        e = launch_ffn(dm, at<void>(ws, fw.xe), mx ? at<uint32_t>(ws, fw.xe_scales) : nullptr, w,
-                       o.counts, o.offsets, o.pad_offsets, o.row_tok, o.row_j, at<void>(ws, fw.h),
-                       mx ? at<uint32_t>(ws, fw.h_scales) : nullptr, ystage,
-                       saved_ctx ? at<uint16_t>(saved_ctx, c.a) : nullptr,
-                       saved_ctx ? at<uint16_t>(saved_ctx, c.b) : nullptr,
-                       saved_ctx ? at<uint16_t>(saved_ctx, c.h) : nullptr, status,
-                       wait_ns(cfg), st);
-    if (e == cudaSuccess) e = launch_combine(dm, ystage, o.gates, static_cast<uint16_t *>(out), st);
+    // dispatch, expert FFN and combine: one persistent kernel (role split,
+    // token ring, on-GPU hand-off counters)
+    FusedIo io;
+    io.ids = o.ids;
+    io.counts = o.counts;
+    io.offsets = o.offsets;
+    io.pad_offsets = o.pad_offsets;
+    io.row_tok = o.row_tok;
+    io.row_j = o.row_j;
+    io.gates = o.gates;
+    io.ring = at<void>(ws, fw.xe);
+    io.ring_scales = mx ? at<uint32_t>(ws, fw.xe_scales) : nullptr;
+    io.h = at<void>(ws, fw.h);
+    io.h_scales = mx ? at<uint32_t>(ws, fw.h_scales) : nullptr;
+    io.ystage = ystage;
+    io.out = static_cast<uint16_t *>(out);
+    io.saved_a = saved_ctx ? at<uint16_t>(saved_ctx, c.a) : nullptr;
+    io.saved_b = saved_ctx ? at<uint16_t>(saved_ctx, c.b) : nullptr;
+    io.saved_h = saved_ctx ? at<uint16_t>(saved_ctx, c.h) : nullptr;
+    io.counters = at<int>(ws, fw.counters);
+    e = launch_fused(dm, cfg, src, io, w, status, wait_ns(cfg), st);
     return cuda_status(e);
 }
 

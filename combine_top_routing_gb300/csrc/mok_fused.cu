@@ -1,0 +1,616 @@
+// mok_fused.cu -- A7: dispatch, the grouped SwiGLU FFN and the weighted
+// combine of the forward layer as ONE persistent cooperative kernel.
+//
+// [kucoin] = "Cursor's MoK achieves 2.37x performance boost on NVIDIA GB300
+// NVL72" (kucoin.com flash, Arabic), §02: the megakernel splits the SMs into
+// a part that runs dispatch, combine and state management and a part that
+// runs the expert FFN; the communication side tells the compute side through
+// a local on-GPU counter when a full set of tokens has arrived, and the
+// compute side tells it back when results can go out; the minibatch (tokens
+// handed over per step) trades early start against GEMM efficiency; a
+// fixed-size token ring buffer is filled by dispatch and reused as soon as
+// the experts are done with it, with no CPU in the loop.  [miku]: results are
+// bit-identical whatever the schedule.
+//
+// On one GPU this becomes:
+//   * gather role (the first n_gather CTAs): pull each expert-ordered row from
+//     its (source, row), quantise it (MXFP8) and write it into the token ring
+//     (ring row = padded row mod ring_rows); after each minibatch of mb rows,
+//     bump ready[row tile] (release).  Before reusing ring rows it waits until
+//     every FFN1 tile that read their previous occupant has loaded them
+//     (consumed[row tile] == FFN1 N tiles).  When the gather is done these
+//     CTAs join the GEMM role.
+//   * GEMM role: a dynamic scheduler (one global atomic) hands out all FFN1
+//     tiles, then all FFN2 tiles, expert by expert in bands of row tiles
+//     (N tile by N tile, the band's row tiles innermost; one band per expert
+//     unless the ring is capped, then half the ring per band).  An FFN1 tile
+//     waits for ready[m], loads A from the ring, and signals consumed[m] once
+//     its loads have landed; its epilogue writes h and bumps h_done[m] (once
+//     per epilogue warp).  An FFN2 tile waits until all FFN1 N tiles of m are
+//     in h and pushes y rows to their token slots (ystage), then bumps
+//     ffn2_done.
+//   * combine: every CTA waits for ffn2_done == all FFN2 tiles, then combines
+//     a share of the tokens in the fixed j order.
+// Each tile is computed by exactly one CTA with the same instruction sequence
+// as the separate-kernel path, so the output is bit-identical to it for every
+// SM split, minibatch and ring size.  Every wait is bounded (wait_ns): on
+// expiry the status word gets MOK_ERR_TIMEOUT and the kernel winds down.
+// Deadlock-free: the ring fills strictly in row-tile order and holds two
+// bands, the rows a gather waits for belong to a band whose tiles all precede
+// the tiles that wait for that gather, and every CTA processes its tiles in
+// schedule order (cooperative launch: all CTAs are resident).
+#include <cuda_bf16.h>
+
+#include <mutex>
+
+#include "mok_internal.h"
+#include "mok_ptx.cuh"
+#include "mok_tc.cuh"
+
+namespace mok {
+
+namespace {
+
+constexpr int kTQ = 2;  // depth of the tile-id queue from the scheduler thread to MMA / epilogue
+
+struct FusedArgs {
+    int E, T, k, d, F;
+    const int32_t *ids, *counts, *offsets, *pad_offsets, *row_tok;
+    const uint8_t *row_j;
+    const float *gates;
+    Sources src;
+    uint8_t *ring;            // [ring_rows, d] BF16 or E4M3
+    uint32_t *ring_scales;    // MX scale tile layout, rows = ring_rows, K = d
+    int64_t ring_rows;        // multiple of 256 (holds any minibatch)
+    void *h;                  // [h_rows, F]
+    uint32_t *h_scales;
+    int64_t h_rows;
+    const uint32_t *s_gate, *s_up, *s_down;
+    int64_t EF, Ed;
+    uint16_t *ystage, *out;
+    uint16_t *saved_a, *saved_b, *saved_h;
+    int mb;                   // minibatch rows per hand-off (64, 128, 256)
+    int n_gather;             // CTAs that start in the gather role
+    int NT1, NT2, BN2, k1, k2;
+    int band1;                // row tiles per band of the FFN1 order (ring-bounded)
+    int *counters;            // zeroed: [0] next tile, [1] next minibatch, [2] FFN2 tiles done,
+                              // then ready[mt], consumed[mt], h_done[mt]
+    int max_mt;
+    uint32_t *status;
+    uint64_t wait_ns;
+};
+
+// Bounded spin until *p >= target (acquire).
+__device__ __forceinline__ bool spin_ge(const int *p, int target, const FusedArgs &a,
+                                        volatile int *abort_flag)
+{
+    if (ld_acquire_gpu(p) >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire_gpu(p) >= target) return true;
+        if ((it & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > a.wait_ns) {
+                report_timeout(a.status, abort_flag);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
+// Tile order of one phase (FFN1 or FFN2, NT N tiles per row tile): expert by
+// expert; inside an expert, bands of up to `band` row tiles; inside a band,
+// N tile by N tile with the band's row tiles innermost, so the CTAs running
+// side by side share a weight tile through L2 and a band's ring rows are
+// released by tiles that all come before the next band's.
+struct PTile {
+    int m, n;
+};
+__device__ __forceinline__ PTile decode_phase_tile(int t, const int *s_pad, int E, int NT, int band)
+{
+    int lo = 0, hi = E;  // last expert whose first tile index <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((s_pad[mid] / 128) * NT <= t) lo = mid;
+        else hi = mid;
+    }
+    const int m0 = s_pad[lo] / 128;
+    const int mt = s_pad[lo + 1] / 128 - m0;
+    const int b = band < mt ? band : mt;  // b * NT <= the expert's tile count
+    const int local = t - m0 * NT;
+    const int j = local / (b * NT);
+    const int bm = mt - j * b < b ? mt - j * b : b;
+    const int ll = local - j * b * NT;
+    PTile r;
+    r.n = ll / bm;
+    r.m = m0 + j * b + ll % bm;
+    return r;
+}
+
+// expert whose padded segment holds row q (last e with pad[e] <= q)
+__device__ __forceinline__ int expert_of_row(const int *s_pad, int E, int64_t q)
+{
+    int lo = 0, hi = E;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pad[mid] <= q) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+template <bool MX>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_moe_fused(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ CUtensorMap tmG,
+                const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
+                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ FusedArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = sA + kStages * kAStage;
+    uint8_t *sSF = sB + kStages * kBStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0));
+    uint64_t *full = bars;
+    uint64_t *empty = bars + kStages;
+    uint64_t *acc_full = bars + 2 * kStages;
+    uint64_t *acc_empty = acc_full + 1;
+    uint64_t *tq_full = acc_empty + 1;
+    uint64_t *tq_empty = tq_full + kTQ;
+    int *tq = reinterpret_cast<int *>(tq_empty + kTQ);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(tq + kTQ);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    int *s_unit = reinterpret_cast<int *>(tmem_holder + 2);
+    int *s_pad = reinterpret_cast<int *>(tmem_holder + 4);  // [E + 1]
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    int *next_tile = a.counters;
+    int *next_unit = a.counters + 1;
+    int *ffn2_done = a.counters + 2;
+    int *ready = a.counters + 3;
+    int *consumed = ready + a.max_mt;
+    int *h_done = consumed + a.max_mt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        for (int i = 0; i < kTQ; ++i) {
+            mbar_init(&tq_full[i], 1);
+            mbar_init(&tq_empty[i], 5);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmRing);
+        prefetch_tmap(&tmG);
+        prefetch_tmap(&tmU);
+        prefetch_tmap(&tmH);
+        prefetch_tmap(&tmD);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x) s_pad[e] = a.pad_offsets[e];
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int64_t pad_end = s_pad[a.E];
+    const int total_mt = static_cast<int>(pad_end / kBM);
+    const int T1 = total_mt * a.NT1;
+    const int total_tiles = T1 + total_mt * a.NT2;
+    constexpr int kE = MX ? 128 : 64;
+
+    // ---------------------------------------------------------- gather role
+    if (static_cast<int>(blockIdx.x) < a.n_gather) {
+        const int units = static_cast<int>((pad_end + a.mb - 1) / a.mb);
+        const int ring_tiles = static_cast<int>(a.ring_rows / kBM);
+        for (;;) {
+            if (threadIdx.x == 0) *s_unit = atomicAdd(next_unit, 1);
+            __syncthreads();
+            const int u = *s_unit;
+            if (u >= units || *abort_flag) break;
+            const int64_t r0 = static_cast<int64_t>(u) * a.mb;
+            const int64_t r1 = r0 + a.mb < pad_end ? r0 + a.mb : pad_end;
+            if (threadIdx.x == 0) {
+                // the ring rows' previous occupants must have been loaded by every FFN1 tile
+                for (int64_t q = r0; q < r1; q += kBM) {
+                    const int m_prev = static_cast<int>(q / kBM) - ring_tiles;
+                    if (m_prev >= 0 && !spin_ge(&consumed[m_prev], a.NT1, a, abort_flag)) break;
+                }
+            }
+            __syncthreads();
+            if (*abort_flag) break;
+            for (int64_t q = r0 + warp; q < r1; q += kThreads / 32) {
+                const int e = expert_of_row(s_pad, a.E, q);
+                const int64_t local = q - s_pad[e];
+                if (local >= a.counts[e]) continue;  // padding row: nothing to pull
+                const int t = a.row_tok[a.offsets[e] + local];
+                const uint4 *in = reinterpret_cast<const uint4 *>(source_row(a.src, t, a.d));
+                const int64_t rr = q % a.ring_rows;
+                if (!MX) {
+                    uint4 *o = reinterpret_cast<uint4 *>(a.ring + rr * a.d * 2);
+#pragma unroll 8
+                    for (int c = lane; c < a.d / 8; c += 32) o[c] = __ldg(in + c);
+                } else {
+                    uint8_t *codes_row = a.ring + rr * a.d;
+                    for (int c0 = 0; c0 < a.d; c0 += 2048) {
+                        uint4 raw[8];
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const int cu = c0 + 256 * w;
+                            const int nvalid = cu >= a.d ? 0 : (a.d - cu >= 256 ? 32 : 16);
+                            raw[w] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int w = 0; w < 8; ++w) {
+                            const int cu = c0 + 256 * w;
+                            if (cu < a.d)
+                                mx_quant_stretch(raw[w], lane, a.d - cu >= 256 ? 32 : 16, codes_row, cu,
+                                                 a.ring_scales, rr, a.ring_rows);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_global();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                __threadfence();
+                for (int64_t q = r0; q < r1; q += 64)  // hand over in 64-row halves of row tiles
+                    red_release_gpu_add(&ready[q / kBM], 1);
+            }
+        }
+        __syncthreads();
+    }
+
+    // ------------------------------------------------------------ GEMM role
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
+            for (;;) {
+                int tile = *abort_flag ? -1 : atomicAdd(next_tile, 1);
+                if (tile >= total_tiles) tile = -1;
+                if (!wait_bar(&tq_empty[qs], qphase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
+                tq[qs] = tile;
+                mbar_arrive(&tq_full[qs]);
+                if (++qs == kTQ) {
+                    qs = 0;
+                    qphase ^= 1u;
+                }
+                if (tile < 0) break;
+                const bool f1 = tile < T1;
+                const PTile pt = f1 ? decode_phase_tile(tile, s_pad, a.E, a.NT1, a.band1)
+                                    : decode_phase_tile(tile - T1, s_pad, a.E, a.NT2, 1 << 30);
+                const int m = pt.m, n = pt.n;
+                if (m < 0 || m >= total_mt || n < 0 || n >= (f1 ? a.NT1 : a.NT2)) {
+                    report_timeout(a.status, abort_flag);  // a schedule bug: stop, touch nothing
+                    break;
+                }
+                const int e = expert_of_row(s_pad, a.E, static_cast<int64_t>(m) * kBM);
+                if (f1 ? !spin_ge(&ready[m], 2, a, abort_flag) : !spin_ge(&h_done[m], 4 * a.NT1, a, abort_flag))
+                    break;
+                fence_proxy_async_global();
+                const int BN = f1 ? 256 : a.BN2;
+                const uint32_t stage_bytes = kAStage + (BN / 128) * 16384 + (MX ? kSfaBytes + (BN / 128) * 512 : 0);
+                const int kst = f1 ? a.k1 : a.k2;
+                const int ya = f1 ? static_cast<int>((static_cast<int64_t>(m) * kBM) % a.ring_rows) : m * kBM;
+                const int yb = f1 ? e * a.F + n * 128 : e * a.d + n * BN;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!wait_bar(&empty[stage], phase ^ 1u, a.status, a.wait_ns, abort_flag)) goto producer_done;
+                    uint8_t *dA = sA + stage * kAStage;
+                    uint8_t *dB = sB + stage * kBStage;
+                    const int x = ks * kE;
+                    mbar_arrive_expect_tx(&full[stage], stage_bytes);
+                    if (f1) {
+                        tma_load_2d(dA, &tmRing, &full[stage], x, ya);
+                        tma_load_2d(dB, &tmG, &full[stage], x, yb);
+                        tma_load_2d(dB + 16384, &tmU, &full[stage], x, yb);
+                    } else {
+                        tma_load_2d(dA, &tmH, &full[stage], x, ya);
+                        tma_load_2d(dB, &tmD, &full[stage], x, yb);
+                        if (BN == 256) tma_load_2d(dB + 16384, &tmD, &full[stage], x, yb + 128);
+                    }
+                    if constexpr (MX) {
+                        uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
+                        if (f1) {
+                            bulk_load(dS, a.ring_scales + scale_word(x, ya, a.ring_rows), kSfaBytes, &full[stage]);
+                            bulk_load(dS + kSfaBytes, a.s_gate + scale_word(x, yb, a.EF), 512, &full[stage]);
+                            bulk_load(dS + kSfaBytes + 512, a.s_up + scale_word(x, yb, a.EF), 512, &full[stage]);
+                        } else {
+                            bulk_load(dS, a.h_scales + scale_word(x, ya, a.h_rows), kSfaBytes, &full[stage]);
+                            bulk_load(dS + kSfaBytes, a.s_down + scale_word(x, yb, a.Ed), (BN / 128) * 512,
+                                      &full[stage]);
+                        }
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc_phase = 0, qs = 0, qphase = 0;
+            for (;;) {
+                if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
+                const int tile = tq[qs];
+                mbar_arrive(&tq_empty[qs]);
+                if (++qs == kTQ) {
+                    qs = 0;
+                    qphase ^= 1u;
+                }
+                if (tile < 0) break;
+                const bool f1 = tile < T1;
+                const int m = f1 ? decode_phase_tile(tile, s_pad, a.E, a.NT1, a.band1).m : 0;
+                const int BN = f1 ? 256 : a.BN2;
+                const int kst = f1 ? a.k1 : a.k2;
+                const uint32_t idesc = idesc_bf16(kBM, BN);
+                if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
+                tc_fence_after();
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    tc_fence_after();
+                    if (f1 && ks == kst - 1) {
+                        // every ring row of row tile m this tile needs is now in shared memory
+                        __threadfence();
+                        red_release_gpu_add(&consumed[m], 1);
+                    }
+                    const uint32_t aaddr = smem_u32(sA + stage * kAStage);
+                    const uint32_t baddr = smem_u32(sB + stage * kBStage);
+                    const uint32_t sfa_col = tmem + kSfCol + stage * 16;
+                    const uint32_t sfb_col = sfa_col + 4;
+                    if (MX) {
+                        const uint32_t sbase = smem_u32(sSF + stage * (kSfaBytes + kSfbBytes));
+                        tmem_cp_32x128b_warpx4(sfa_col, sdesc_sf(sbase));
+                        tmem_cp_32x128b_warpx4(sfb_col, sdesc_sf(sbase + kSfaBytes));
+                        if (BN == 256) tmem_cp_32x128b_warpx4(sfb_col + 4, sdesc_sf(sbase + kSfaBytes + 512));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_k_sw128(aaddr + kk * 32);
+                        const uint64_t bd = sdesc_k_sw128(baddr + kk * 32);
+                        const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
+                        if (MX) mma_mxf8(tmem, ad, bd, idesc_mxf8(kBM, BN, kk, kk), sfa_col, sfb_col, accum);
+                        else mma_bf16(tmem, ad, bd, idesc, accum);
+                    }
+                    tc_commit(&empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit(acc_full);
+                acc_phase ^= 1u;
+            }
+        mma_done:;
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        uint32_t acc_phase = 0, qs = 0, qphase = 0;
+        for (;;) {
+            if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
+            const int tile = tq[qs];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tq_empty[qs]);
+            if (++qs == kTQ) {
+                qs = 0;
+                qphase ^= 1u;
+            }
+            if (tile < 0) break;
+            const bool f1 = tile < T1;
+            const PTile pt = f1 ? decode_phase_tile(tile, s_pad, a.E, a.NT1, a.band1)
+                                : decode_phase_tile(tile - T1, s_pad, a.E, a.NT2, 1 << 30);
+            const int m = pt.m, n = pt.n;
+            if (m < 0 || m >= total_mt || n < 0 || n >= (f1 ? a.NT1 : a.NT2)) {
+                report_timeout(a.status, abort_flag);
+                break;
+            }
+            const int64_t q = static_cast<int64_t>(m) * kBM + r;   // padded row of this thread
+            const int e = expert_of_row(s_pad, a.E, static_cast<int64_t>(m) * kBM);
+            const int64_t row_in_e = q - s_pad[e];
+            const bool valid = row_in_e < a.counts[e];
+            if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
+            tc_fence_after();
+            bool released = false;
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                released = true;
+            };
+            if (f1) {
+                epi_ffn1<MX>(trow, valid, q, n * 128, a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b,
+                             a.saved_h, release);
+            } else {
+                uint16_t *dst = nullptr;
+                if (valid) {
+                    const int64_t p = a.offsets[e] + row_in_e;
+                    dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k + a.row_j[p]) * a.d +
+                          n * a.BN2;
+                }
+                epi_rows_bf16(trow, a.BN2, false, valid, dst, release);
+            }
+            if (!released) release();
+            acc_phase ^= 1u;
+            // publish this warp's quarter of the tile (h rows for FFN2 tiles, ystage
+            // rows for the combine); each epilogue warp counts for itself, so no
+            // barrier ties the four warps together
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                red_release_gpu_add(f1 ? &h_done[m] : ffn2_done, 1);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+
+    // ----------------------------------------------------- weighted combine
+    if (threadIdx.x == 0 && !*abort_flag) spin_ge(ffn2_done, 4 * total_mt * a.NT2, a, abort_flag);
+    __syncthreads();
+    if (*abort_flag) return;
+    const int vec = a.d / 8;
+    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+        for (int c = threadIdx.x; c < vec; c += blockDim.x) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (int j = 0; j < a.k; ++j) {
+                const float g = a.gates[t * a.k + j];
+                const uint4 y = *(reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c);
+                const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(g, bf16_bits_to_float(w[i] & 0xFFFFu), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(g, bf16_bits_to_float(w[i] >> 16), acc[2 * i + 1]);
+                }
+            }
+            reinterpret_cast<uint4 *>(a.out + t * a.d)[c] =
+                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        }
+    }
+}
+
+template <bool MX>
+constexpr size_t fused_smem_bytes()
+{
+    return 1024 + kStages * (kAStage + kBStage) + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0) +
+           (2 * kStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + (MOK_MAX_EXPERTS + 1) * 4;
+}
+
+template <bool MX>
+cudaError_t launch_fused_t(const CUtensorMap &ring, const CUtensorMap &g, const CUtensorMap &u,
+                           const CUtensorMap &h, const CUtensorMap &dn, const FusedArgs &args,
+                           cudaStream_t st)
+{
+    constexpr size_t smem = fused_smem_bytes<MX>();
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(k_moe_fused<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+        int per_sm = 0;
+        if (attr_err == cudaSuccess)
+            attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe_fused<MX>, kThreads, smem);
+        if (attr_err == cudaSuccess && per_sm < 1) attr_err = cudaErrorInvalidConfiguration;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms()));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_moe_fused<MX>, ring, g, u, h, dn, args);
+}
+
+}  // namespace
+
+int64_t fused_ring_rows(const Dims &dm, size_t ring_bytes)
+{
+    if (ring_bytes == 0) return dm.rows_pad;
+    const int64_t row_bytes = dm.dtype == MOK_MXFP8 ? dm.d + dm.d / 32 : 2 * static_cast<int64_t>(dm.d);
+    int64_t rows = static_cast<int64_t>(ring_bytes) / row_bytes / 256 * 256;
+    return rows < dm.rows_pad ? rows : dm.rows_pad;
+}
+
+int fused_counter_ints(const Dims &dm) { return 3 + 3 * static_cast<int>(dm.rows_pad / 128); }
+
+cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &src, const FusedIo &io,
+                         const mok_weights *w, uint32_t *status, uint64_t wait_ns, cudaStream_t st)
+{
+    const bool mx = dm.dtype == MOK_MXFP8;
+    const uint32_t box = mx ? 128 : 64;
+    const int64_t ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
+    if (ring_rows < 256) return cudaErrorInvalidValue;
+    const uint64_t EF = static_cast<uint64_t>(dm.E) * dm.F;
+    const uint64_t Ed = static_cast<uint64_t>(dm.E) * dm.d;
+    CUtensorMap tr, tg, tu, th, td;
+    if (encode_tmap_2d(&tr, io.ring, mx, dm.d, ring_rows, box, kBM) ||
+        encode_tmap_2d(&tg, mx ? static_cast<const void *>(w->q_gate) : w->w_gate, mx, dm.d, EF, box, 128) ||
+        encode_tmap_2d(&tu, mx ? static_cast<const void *>(w->q_up) : w->w_up, mx, dm.d, EF, box, 128) ||
+        encode_tmap_2d(&th, io.h, mx, dm.F, dm.rows_pad, box, kBM) ||
+        encode_tmap_2d(&td, mx ? static_cast<const void *>(w->q_down) : w->w_down, mx, dm.F, Ed, box, 128))
+        return cudaErrorInvalidValue;
+    FusedArgs a = {};
+    a.E = dm.E;
+    a.T = dm.T;
+    a.k = dm.k;
+    a.d = dm.d;
+    a.F = dm.F;
+    a.ids = io.ids;
+    a.counts = io.counts;
+    a.offsets = io.offsets;
+    a.pad_offsets = io.pad_offsets;
+    a.row_tok = io.row_tok;
+    a.row_j = io.row_j;
+    a.gates = io.gates;
+    a.src = src;
+    a.ring = static_cast<uint8_t *>(io.ring);
+    a.ring_scales = io.ring_scales;
+    a.ring_rows = ring_rows;
+    a.h = io.h;
+    a.h_scales = io.h_scales;
+    a.h_rows = dm.rows_pad;
+    a.s_gate = w->s_gate;
+    a.s_up = w->s_up;
+    a.s_down = w->s_down;
+    a.EF = static_cast<int64_t>(EF);
+    a.Ed = static_cast<int64_t>(Ed);
+    a.ystage = io.ystage;
+    a.out = io.out;
+    a.saved_a = io.saved_a;
+    a.saved_b = io.saved_b;
+    a.saved_h = io.saved_h;
+    a.mb = cfg->minibatch_rows ? cfg->minibatch_rows : 128;
+    const int sms = num_sms();
+    const float frac = cfg->gather_sm_fraction > 0.0f ? cfg->gather_sm_fraction : 0.25f;
+    int ng = static_cast<int>(frac * static_cast<float>(sms) + 0.5f);
+    a.n_gather = ng < 1 ? 1 : (ng > sms - 1 ? sms - 1 : ng);
+    a.NT1 = dm.F / 128;
+    a.BN2 = dm.d % 256 == 0 ? 256 : 128;
+    a.NT2 = dm.d / a.BN2;
+    a.k1 = dm.d / static_cast<int>(box);
+    a.k2 = dm.F / static_cast<int>(box);
+    // an uncapped ring never wraps: one band per expert (the separate-kernel
+    // order); a capped ring holds two bands, so a band is always free to fill
+    a.band1 = ring_rows >= dm.rows_pad ? (1 << 30) : static_cast<int>(ring_rows / 128 / 2);
+    a.counters = io.counters;
+    a.max_mt = static_cast<int>(dm.rows_pad / 128);
+    a.status = status;
+    a.wait_ns = wait_ns;
+    cudaError_t e = cudaMemsetAsync(io.counters, 0, sizeof(int) * fused_counter_ints(dm), st);
+    if (e != cudaSuccess) return e;
+    return mx ? launch_fused_t<true>(tr, tg, tu, th, td, a, st)
+              : launch_fused_t<false>(tr, tg, tu, th, td, a, st);
+}
+
+}  // namespace mok

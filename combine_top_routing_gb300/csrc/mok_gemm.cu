@@ -368,93 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else if constexpr (MODE == MODE_FFN1) {
                 const int e = tl.group;
                 const int row_in_e = tl.m_blk * kBM + r;
-                const bool valid = row_in_e < a.counts[e];
-                const int64_t grow = a.pad_offsets[e] + row_in_e;
-                const int f0 = tl.n_blk * 128;
-                uint32_t sword = 0;
-                if (!a.saved_a && !a.saved_b && !a.saved_h) {
-                    // inference: h for the row's 128 columns into registers, release, store
-                    uint32_t hq[64];  // BF16 pairs (64) or E4M3 quads (32)
-#pragma unroll
-                    for (int c = 0; c < 128; c += 32) {
-                        uint32_t gv[32], uv[32];
-                        tmem_ld_32x32(trow + c, gv);
-                        tmem_ld_32x32(trow + 128 + c, uv);
-                        tmem_ld_wait();
-                        float hv[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float av = __uint_as_float(gv[i]);
-                            hv[i] = av / (1.0f + __expf(-av)) * __uint_as_float(uv[i]);
-                        }
-                        if (!MX) {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) hq[c / 2 + i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
-                        } else {
-                            float amax = 0.0f;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
-                            const int x = mx_scale_exp(amax);
-                            const float inv = mx_inv_scale(x);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                hq[c / 4 + i] = pack_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
-                                                (pack_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
-                            sword |= static_cast<uint32_t>(x + 127) << (8 * (c >> 5));
-                        }
-                    }
-                    release();
-                    if (valid) {
-                        const int64_t off = grow * a.F + f0;
-                        if (!MX) {
-                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.h) + off);
-#pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
-                        } else {
-                            uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.h) + off);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q)
-                                o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
-                            a.h_scales[scale_word_row(f0 >> 7, grow, a.h_rows)] = sword;
-                        }
-                    }
-                } else
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t gv[32], uv[32];
-                    tmem_ld_32x32(trow + c, gv);
-                    tmem_ld_32x32(trow + 128 + c, uv);
-                    tmem_ld_wait();
-                    float hv[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float av = __uint_as_float(gv[i]);
-                        const float bv = __uint_as_float(uv[i]);
-                        hv[i] = av / (1.0f + __expf(-av)) * bv;
-                    }
-                    if (valid) {
-                        const int64_t off = grow * a.F + f0 + c;
-                        if (a.saved_a) {
-                            float t[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(gv[i]);
-                            store_bf16x32(a.saved_a + off, t);
-                        }
-                        if (a.saved_b) {
-                            float t[32];
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(uv[i]);
-                            store_bf16x32(a.saved_b + off, t);
-                        }
-                        if (a.saved_h) store_bf16x32(a.saved_h + off, hv);
-                        if (!MX) {
-                            store_bf16x32(static_cast<uint16_t *>(a.h) + off, hv);
-                        } else {
-                            sword |= quant_mx32(hv, static_cast<uint8_t *>(a.h) + off) << (8 * (c >> 5));
-                        }
-                    }
-                }
-                if (MX && valid && !released) a.h_scales[scale_word_row(f0 >> 7, grow, a.h_rows)] = sword;
+                epi_ffn1<MX>(trow, row_in_e < a.counts[e], a.pad_offsets[e] + row_in_e, tl.n_blk * 128,
+                             a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b, a.saved_h, release);
             } else if constexpr (MODE == MODE_FFN2) {
                 const int e = tl.group;
                 const int row_in_e = tl.m_blk * kBM + r;
@@ -466,10 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t j = a.row_j[p];
                     dst = a.ystage + (t * a.k_top + j) * a.d + tl.n_blk * BN;
                 }
-                uint32_t pk[128];
-                drain_row_bf16(trow, BN, false, pk);
-                release();
-                if (valid) store_row_bf16(dst, BN, pk);
+                epi_rows_bf16(trow, BN, false, valid, dst, release);
             } else if constexpr (MODE == MODE_DGRAD2) {
                 // dh -> SwiGLU backward with the saved (BF16) a, b:
                 //   s = sigmoid(a), da = dh b s (1 + a (1 - s)), db = dh a s

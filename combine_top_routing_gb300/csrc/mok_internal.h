@@ -35,6 +35,7 @@ struct FwdWs {
     size_t xe, xe_scales;   // expert-ordered activations (padded rows)
     size_t h, h_scales;     // SwiGLU output (padded rows)
     size_t ystage;          // BF16 [T, k, d] (when no saved ctx)
+    size_t counters;        // int32 hand-off counters of the fused forward
     size_t total;
 };
 
@@ -142,6 +143,23 @@ cudaError_t launch_router_wgrad(const Dims &dm, const Sources &src, const int32_
                                 float *dW_r, cudaStream_t st);
 cudaError_t launch_transpose_bf16(const uint16_t *src, int64_t batch, int64_t rows, int64_t K,
                                   uint16_t *dst, cudaStream_t st);
+
+// Buffers of the fused persistent forward.
+struct FusedIo {
+    const int32_t *ids, *counts, *offsets, *pad_offsets, *row_tok;
+    const uint8_t *row_j;
+    const float *gates;
+    void *ring;               // token ring (a prefix of the xe buffer)
+    uint32_t *ring_scales;
+    void *h;
+    uint32_t *h_scales;
+    uint16_t *ystage, *out, *saved_a, *saved_b, *saved_h;
+    int *counters;            // fused_counter_ints(dm) ints
+};
+int64_t fused_ring_rows(const Dims &dm, size_t ring_bytes);
+int fused_counter_ints(const Dims &dm);
+cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &src, const FusedIo &io,
+                         const mok_weights *w, uint32_t *status, uint64_t wait_ns, cudaStream_t st);
 
 int num_sms();
 // Encodes a 2-D tiled tensor map with 128-byte swizzle; returns 0 on success.

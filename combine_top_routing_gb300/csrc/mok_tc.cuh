@@ -20,7 +20,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol = 256;          // scale columns: 16 per stage after the accumulator
 
 
-__device__ __noinline__ void report_timeout(uint32_t *status, volatile int *abort_flag)
+static __device__ __noinline__ void report_timeout(uint32_t *status, volatile int *abort_flag)
 {
     *abort_flag = 1;
     if (status) atomicMax(status, static_cast<uint32_t>(MOK_ERR_TIMEOUT));
@@ -136,6 +136,114 @@ __device__ __forceinline__ void store_row_bf16(uint16_t *dst, int BN, const uint
 #pragma unroll
     for (int c = 0; c < 256; c += 8)
         if (c < BN) o[c / 8] = make_uint4(pk[c / 2], pk[c / 2 + 1], pk[c / 2 + 2], pk[c / 2 + 3]);
+}
+
+// FFN1 epilogue of one accumulator row (TMEM lane): columns [0,128) hold
+// a = x W_g^T and [128,256) b = x W_u^T for 128 columns of F starting at f0.
+// h = silu(a) b is stored BF16 or MXFP8 (one block of 32 along F per chunk,
+// quantised in registers) at row `grow` of h; training also stores a, b, h in
+// BF16.  Inference drains h into registers and calls release() before the
+// global stores.
+template <bool MX, typename Release>
+__device__ __forceinline__ void epi_ffn1(uint32_t trow, bool valid, int64_t grow, int f0, int F,
+                                         void *h, uint32_t *h_scales, int64_t h_rows,
+                                         uint16_t *saved_a, uint16_t *saved_b, uint16_t *saved_h,
+                                         Release &&release)
+{
+    uint32_t sword = 0;
+    if (!saved_a && !saved_b && !saved_h) {
+        // inference: h for the row's 128 columns into registers, release, store
+        uint32_t hq[64];  // BF16 pairs (64) or E4M3 quads (32)
+#pragma unroll
+        for (int c = 0; c < 128; c += 32) {
+            uint32_t gv[32], uv[32];
+            tmem_ld_32x32(trow + c, gv);
+            tmem_ld_32x32(trow + 128 + c, uv);
+            tmem_ld_wait();
+            float hv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float av = __uint_as_float(gv[i]);
+                hv[i] = av / (1.0f + __expf(-av)) * __uint_as_float(uv[i]);
+            }
+            if (!MX) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) hq[c / 2 + i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
+            } else {
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
+                const int x = mx_scale_exp(amax);
+                const float inv = mx_inv_scale(x);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    hq[c / 4 + i] = pack_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
+                                    (pack_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
+                sword |= static_cast<uint32_t>(x + 127) << (8 * (c >> 5));
+            }
+        }
+        release();
+        if (valid) {
+            const int64_t off = grow * F + f0;
+            if (!MX) {
+                uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(h) + off);
+#pragma unroll
+                for (int q = 0; q < 16; ++q)
+                    o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
+            } else {
+                uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(h) + off);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
+                h_scales[scale_word_row(f0 >> 7, grow, h_rows)] = sword;
+            }
+        }
+        return;
+    }
+    // training: a, b, h also stored (BF16); stores happen before the release
+    for (int c = 0; c < 128; c += 32) {
+        uint32_t gv[32], uv[32];
+        tmem_ld_32x32(trow + c, gv);
+        tmem_ld_32x32(trow + 128 + c, uv);
+        tmem_ld_wait();
+        float hv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float av = __uint_as_float(gv[i]);
+            hv[i] = av / (1.0f + __expf(-av)) * __uint_as_float(uv[i]);
+        }
+        if (valid) {
+            const int64_t off = grow * F + f0 + c;
+            if (saved_a) {
+                float t[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(gv[i]);
+                store_bf16x32(saved_a + off, t);
+            }
+            if (saved_b) {
+                float t[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) t[i] = __uint_as_float(uv[i]);
+                store_bf16x32(saved_b + off, t);
+            }
+            if (saved_h) store_bf16x32(saved_h + off, hv);
+            if (!MX) store_bf16x32(static_cast<uint16_t *>(h) + off, hv);
+            else sword |= quant_mx32(hv, static_cast<uint8_t *>(h) + off) << (8 * (c >> 5));
+        }
+    }
+    if (MX && valid) h_scales[scale_word_row(f0 >> 7, grow, h_rows)] = sword;
+}
+
+// Plain row epilogue: BN fp32 columns -> BF16 at dst (zeros when `zero`),
+// TMEM released before the stores.
+template <typename Release>
+__device__ __forceinline__ void epi_rows_bf16(uint32_t trow, int BN, bool zero, bool valid,
+                                              uint16_t *dst, Release &&release)
+{
+    uint32_t pk[128];
+    drain_row_bf16(trow, BN, zero, pk);
+    release();
+    if (valid) store_row_bf16(dst, BN, pk);
 }
 
 }  // namespace mok

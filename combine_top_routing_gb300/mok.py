@@ -135,11 +135,13 @@ class Config:
 
     @classmethod
     def from_workload(cls, w, **kw):
+        opts = dict(n_sources=w.n_sources,
+                    source_rows=w.source_rows if w.n_sources > 1 else None,
+                    ring_bytes=w.ring_bytes)
+        opts.update(kw)
         return cls(w.T, w.d, w.E, w.k, w.F,
                    MOK_ROUTER_SOFTMAX if w.router == "softmax" else MOK_ROUTER_SIGMOID,
-                   MOK_MXFP8 if w.dtype == "mxfp8" else MOK_BF16,
-                   n_sources=w.n_sources, source_rows=w.source_rows if w.n_sources > 1 else None,
-                   ring_bytes=w.ring_bytes, **kw)
+                   MOK_MXFP8 if w.dtype == "mxfp8" else MOK_BF16, **opts)
 
     @property
     def ref(self):

@@ -1,0 +1,106 @@
+"""The fused persistent forward (A7): one cooperative kernel with a gather
+role and a GEMM role handing minibatches over through on-GPU counters and a
+fixed-size token ring.
+
+  * bit-identical to the separate-kernel path (route_layout, dispatch,
+    expert_ffn, combine) -- every tile is the same instruction sequence;
+  * bit-identical across gather SM fractions {1/8, 1/4, 1/3}, minibatch
+    {64, 128, 256} and ring sizes down to 256 rows (many wraps) -- the
+    pages' determinism claim;
+  * a ring smaller than one minibatch is refused on the host;
+  * a device wait that runs out reports MOK_ERR_TIMEOUT through the status
+    word, and the context stays usable for the next call.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from combine_top_routing_gb300 import inputs as I
+from combine_top_routing_gb300 import mok
+from combine_top_routing_gb300.layer import MoELayer, scale_words
+from mokhelp import Routed, make_layer, sha
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "mx_skew_sources": I.Workload("mx_skew_sources", T=2048, d=512, E=32, k=8, F=384,
+                                  dtype="mxfp8", router="sigmoid", seed=61, zipf_alpha=0.46,
+                                  n_sources=8),
+    "bf16": I.Workload("bf16", T=1000, d=256, E=8, k=2, F=512, dtype="bf16",
+                       router="softmax", seed=62),
+}
+
+
+def _stepwise(layer):
+    """The same layer through the four step entry points."""
+    w = layer.w
+    R = Routed(layer)
+    rows = layer.rows_pad
+    if w.dtype == "mxfp8":
+        xe = torch.empty((rows, w.d), dtype=torch.uint8, device="cuda")
+        xs = torch.empty(scale_words(rows, w.d), dtype=torch.int32, device="cuda")
+    else:
+        xe = torch.empty((rows, w.d), dtype=torch.bfloat16, device="cuda")
+        xs = None
+    mok.dispatch(layer.cfg, layer.x_src, R.ids, R.offsets, R.pad_offsets, R.row_tok, R.row_j, xe, xs)
+    ystage = torch.empty((w.T, w.k, w.d), dtype=torch.bfloat16, device="cuda")
+    mok.expert_ffn(layer.cfg, xe, xs, layer.wstruct, R.offsets, R.pad_offsets, R.row_tok, R.row_j,
+                   ystage, None, None, None, layer.ws)
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    mok.combine(layer.cfg, ystage, R.gates, out)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fused_equals_stepwise_bit_exact(name):
+    w = CASES[name]
+    layer, _ = make_layer(w)
+    fused = layer.forward().clone()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(fused, _stepwise(layer))
+
+
+def test_fused_bit_identical_across_splits_minibatches_rings():
+    w = CASES["mx_skew_sources"]
+    inp = I.make_inputs(w, device="cuda")
+    row_bytes = w.d + w.d // 32
+    hashes = {}
+    for frac, mb, ring_rows in itertools.product((0.125, 0.25, 1 / 3), (64, 128, 256), (0, 256, 1024)):
+        layer = MoELayer(w, inp, gather_sm_fraction=frac, minibatch_rows=mb,
+                         ring_bytes=ring_rows * row_bytes)
+        out = layer.forward()
+        torch.cuda.synchronize()
+        assert layer.status() == 0, (frac, mb, ring_rows)
+        hashes[(frac, mb, ring_rows)] = sha(out)
+    assert len(set(hashes.values())) == 1, hashes
+
+
+def test_ring_smaller_than_a_minibatch_is_refused():
+    w = CASES["bf16"]
+    layer, _ = make_layer(w)
+    layer.cfg.c.ring_bytes = 100 * w.d * 2   # 100 rows < 256
+    with pytest.raises(mok.MokError) as ei:
+        layer.forward()
+    assert ei.value.code == mok.MOK_ERR_INVALID_ARG
+
+
+def test_device_timeout_is_reported_and_context_stays_usable():
+    w = CASES["mx_skew_sources"]
+    layer, _ = make_layer(w)
+    good = layer.forward().clone()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    # a 1 ns limit: the GEMM role cannot find its first minibatch gathered in time
+    layer.cfg.c.wait_limit_ns = 1
+    layer.forward()
+    torch.cuda.synchronize()
+    assert layer.status() == mok.MOK_ERR_TIMEOUT
+    layer.cfg.c.wait_limit_ns = 0
+    again = layer.forward()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(again, good)
