@@ -38,6 +38,8 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="also time the fused forward over gather SM fraction x minibatch")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
     p.add_argument("--set", action="append", default=[], metavar="FIELD=VALUE",
                    help="override a workload field (e.g. T=2048, E=32) for profiling runs")
@@ -320,22 +322,50 @@ def main():
         del tl
         torch.cuda.empty_cache()
 
-    # ---------------- the expert FFN (dominant kernels) timed alone, same stream
+    # ---------------- the dominant kernel (k_moe_fused) timed alone, same stream
     R = _route_for_ffn(layer)
-    ffn_iters = max(5, min(50, args.steps))
-    for _ in range(2):
-        _ffn(layer, R)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(ffn_iters):
-        _ffn(layer, R)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ffn_ms = e0.elapsed_time(e1) / ffn_iters
+    iters = max(5, min(50, args.steps))
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+
+    fused_ms = timed(lambda: mok.moe_fused(layer.cfg, layer.x_src, layer.wstruct, R.ids, R.gates,
+                                           R.counts, R.offsets, R.pad_offsets, R.row_tok, R.row_j,
+                                           R.ystage, layer.out, layer.ws))
+    ffn_ms = timed(lambda: _ffn(layer, R))
     flops = _layer_flops(w)
-    ffn_tflops = flops / (ffn_ms / 1e3) / 1e12
+    fused_tflops = flops / (fused_ms / 1e3) / 1e12
     bf16_peak = peaks.get("bf16_tflops", 1900.0)
     peak_tc = bf16_peak * (2.0 if w.dtype == "mxfp8" else 1.0)
+
+    sweep = None
+    if args.sweep:
+        sweep = []
+        for frac in (0.125, 0.25, 1 / 3):
+            for mb in (64, 128, 256):
+                lw = MoELayer(w, inp, gather_sm_fraction=frac, minibatch_rows=mb)
+                for _ in range(2):
+                    lw.forward()
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s0.record(stream)
+                for _ in range(iters):
+                    lw.forward()
+                s1.record(stream)
+                torch.cuda.synchronize()
+                if lw.status() != 0:
+                    raise RuntimeError("device status in sweep: " + mok.status_string(lw.status()))
+                sweep.append({"gather_sm_fraction": round(frac, 4), "minibatch_rows": mb,
+                              "ms_per_step": s0.elapsed_time(s1) / iters})
+                del lw
+                torch.cuda.empty_cache()
 
     # ---------------- end to end through the C ABI with host buffers
     x_host = torch.empty_like(inp["x"], device="cpu").pin_memory()
@@ -366,7 +396,7 @@ def main():
 
     if rank == 0:
         clocks = clk.summary(peaks.get("sm_max_mhz"))
-        launches_per_step = 10
+        launches_per_step = 8  # split, router GEMM, top-k, 4 layout passes, fused kernel
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
@@ -379,12 +409,16 @@ def main():
                        "l2": "inputs larger than L2 (expert weights %.1f GB)" %
                              (w.E * 3 * w.F * w.d * (1 if w.dtype == 'mxfp8' else 2) / 1e9),
                        "parallelism": f"replicas x{world}"},
-            "roofline": {"bound": "tensor", "achieved": ffn_tflops, "peak": peak_tc,
-                         "unit": "TFLOP/s", "frac": ffn_tflops / peak_tc, "traffic": None,
-                         "kernel": "k_gemm FFN1+FFN2 (expert_ffn)",
+            "roofline": {"bound": "tensor", "achieved": fused_tflops, "peak": peak_tc,
+                         "unit": "TFLOP/s", "frac": fused_tflops / peak_tc, "traffic": None,
+                         "kernel": "k_moe_fused (pull dispatch + FFN1 + FFN2 + combine)",
+                         "algorithmic": "6*S*d*F flops per launch",
                          "peak_source": f"{peak_src} bf16 burst"
                                         + (" x2 for fp8" if w.dtype == "mxfp8" else ""),
-                         "ms_per_launch": ffn_ms},
+                         "ms_per_launch": fused_ms},
+            "expert_ffn_separate_kernels": {"ms": ffn_ms,
+                                            "tflops": flops / (ffn_ms / 1e3) / 1e12},
+            "sweep": sweep,
             "layer_roofline": {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
                                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /
                                            peaks.get("hbm_gbs", 6800.0)},

@@ -439,6 +439,47 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     return cuda_status(e);
 }
 
+int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_weights *w,
+                  const int32_t *ids, const float *gates, const int32_t *counts,
+                  const int32_t *offsets, const int32_t *pad_offsets, const int32_t *row_tok,
+                  const uint8_t *row_j, void *ystage, void *out, void *ws, void *stream)
+{
+    Dims dm;
+    int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!w || !ids || !gates || !counts || !offsets || !pad_offsets || !row_tok || !row_j ||
+        !ystage || !out || !ws)
+        return MOK_ERR_INVALID_ARG;
+    const bool mx = dm.dtype == MOK_MXFP8;
+    if (mx && (!w->q_gate || !w->q_up || !w->q_down || !w->s_gate || !w->s_up || !w->s_down))
+        return MOK_ERR_INVALID_ARG;
+    if (!mx && (!w->w_gate || !w->w_up || !w->w_down)) return MOK_ERR_INVALID_ARG;
+    if (fused_ring_rows(dm, cfg->ring_bytes) < 256) return MOK_ERR_INVALID_ARG;
+    Sources src;
+    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    FwdWs fw;
+    fwd_ws_layout(dm, &fw);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t *status = at<uint32_t>(ws, fw.status);
+    if (cudaMemsetAsync(status, 0, 4, st) != cudaSuccess) return MOK_ERR_CUDA;
+    FusedIo io = {};
+    io.ids = ids;
+    io.counts = counts;
+    io.offsets = offsets;
+    io.pad_offsets = pad_offsets;
+    io.row_tok = row_tok;
+    io.row_j = row_j;
+    io.gates = gates;
+    io.ring = at<void>(ws, fw.xe);
+    io.ring_scales = mx ? at<uint32_t>(ws, fw.xe_scales) : nullptr;
+    io.h = at<void>(ws, fw.h);
+    io.h_scales = mx ? at<uint32_t>(ws, fw.h_scales) : nullptr;
+    io.ystage = static_cast<uint16_t *>(ystage);
+    io.out = static_cast<uint16_t *>(out);
+    io.counters = at<int>(ws, fw.counters);
+    return cuda_status(launch_fused(dm, cfg, src, io, w, status, wait_ns(cfg), st));
+}
+
 int mok_moe_backward(const mok_config *cfg, const void *const *x_src, const float *W_r,
                      const void *saved_ctx, const void *dY, const mok_weights *w, void *dX,
                      mok_weight_grads *dw, float *dgates, float *dlogits, float *dW_r, void *ws,

@@ -25,7 +25,8 @@ MOK_MAX_SOURCES = 64
 
 EXPORTS = [
     "mok_max_padded_rows", "mok_workspace_size", "mok_saved_ctx_layout", "mok_route_layout",
-    "mok_dispatch", "mok_expert_ffn", "mok_combine", "mok_moe_forward", "mok_moe_backward",
+    "mok_dispatch", "mok_expert_ffn", "mok_combine", "mok_moe_fused", "mok_moe_forward",
+    "mok_moe_backward",
     "mok_quantize_mx", "mok_transpose_bf16", "mok_reset_device_status", "mok_get_device_status",
     "mok_status_string", "mok_layout_static",
 ]
@@ -82,6 +83,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_dispatch.argtypes = [cfgp, vp] + [vp] * 8
         L.mok_expert_ffn.argtypes = [cfgp, vp, vp, ctypes.POINTER(MokWeights)] + [vp] * 10
         L.mok_combine.argtypes = [cfgp, vp, vp, vp, vp]
+        L.mok_moe_fused.argtypes = [cfgp, vp, ctypes.POINTER(MokWeights)] + [vp] * 11
         L.mok_moe_forward.argtypes = [cfgp, vp, vp, vp, ctypes.POINTER(MokWeights), vp, vp, vp, vp]
         L.mok_moe_backward.argtypes = [cfgp, vp, vp, vp, vp, ctypes.POINTER(MokWeights), vp,
                                        ctypes.POINTER(MokWeightGrads), vp, vp, vp, vp, vp]
@@ -203,6 +205,15 @@ def expert_ffn(cfg, xe, xe_scales, weights: MokWeights, offsets, pad_offsets, ro
 
 def combine(cfg, ystage, gates, out, stream=None):
     _check("mok_combine", lib().mok_combine(cfg.ref, _ptr(ystage), _ptr(gates), _ptr(out), _stream(stream)))
+
+
+def moe_fused(cfg, x_src, weights: MokWeights, ids, gates, counts, offsets, pad_offsets, row_tok,
+              row_j, ystage, out, ws, stream=None):
+    arr = _src_array(x_src)
+    _check("mok_moe_fused", lib().mok_moe_fused(
+        cfg.ref, arr, ctypes.byref(weights), _ptr(ids), _ptr(gates), _ptr(counts), _ptr(offsets),
+        _ptr(pad_offsets), _ptr(row_tok), _ptr(row_j), _ptr(ystage), _ptr(out), _ptr(ws),
+        _stream(stream)))
 
 
 def moe_forward(cfg, x_src, W_r, bias, weights: MokWeights, out, saved_ctx, ws, stream=None):

@@ -195,9 +195,30 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates,
                 void *out, void *stream);
 
 /*
- * The whole forward layer: route_layout, dispatch, expert FFN and combine,
- * enqueued back to back on one stream with no host round trip.
- * saved_ctx: device buffer of saved_ctx bytes (training) or NULL (inference).
+ * A3-A6 as ONE persistent cooperative kernel ([kucoin] §02: the megakernel
+ * splits the SMs between dispatch/combine/state and the expert FFN, hands
+ * minibatches over through on-GPU counters and reuses a fixed-size token ring
+ * buffer as soon as the experts are done with it).  From a layout made by
+ * mok_route_layout: cfg->gather_sm_fraction of the SMs (0: 1/4) start pulling
+ * rows (quantised when MXFP8) into a token ring of cfg->ring_bytes (0: no
+ * cap; it must hold 256 rows) in minibatches of cfg->minibatch_rows (0: 128);
+ * the other SMs run the FFN1 and FFN2 tiles as rows arrive; finally every SM
+ * combines.  The result is bit-identical to mok_dispatch + mok_expert_ffn +
+ * mok_combine for every split, minibatch and ring size.  ystage: device BF16
+ * [T,k,d]; out: device BF16 [T,d]; ws: fwd_ws bytes.  A ring below 256 rows
+ * returns MOK_ERR_INVALID_ARG; a bounded device wait that runs out sets
+ * MOK_ERR_TIMEOUT in the status word.
+ */
+int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_weights *w,
+                  const int32_t *ids, const float *gates, const int32_t *counts,
+                  const int32_t *offsets, const int32_t *pad_offsets, const int32_t *row_tok,
+                  const uint8_t *row_j, void *ystage, void *out, void *ws, void *stream);
+
+/*
+ * The whole forward layer: mok_route_layout then the fused persistent kernel
+ * of mok_moe_fused, enqueued back to back on one stream with no host round
+ * trip.  saved_ctx: device buffer of saved_ctx bytes (training: a, b, h,
+ * ystage and the routing are kept for mok_moe_backward) or NULL (inference).
  */
 int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float *W_r,
                     const float *bias, const mok_weights *w, void *out, void *saved_ctx,

@@ -104,3 +104,18 @@ def test_device_timeout_is_reported_and_context_stays_usable():
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert torch.equal(again, good)
+
+
+def test_moe_fused_entry_equals_forward():
+    w = CASES["mx_skew_sources"]
+    layer, _ = make_layer(w)
+    ref = layer.forward().clone()
+    R = Routed(layer)
+    ystage = torch.empty((w.T, w.k, w.d), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        mok.moe_fused(layer.cfg, layer.x_src, layer.wstruct, R.ids, R.gates, R.counts, R.offsets,
+                      R.pad_offsets, R.row_tok, R.row_j, ystage, out, layer.ws)
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert torch.equal(out, ref)
