@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *s_unit = reinterpret_cast<int *>(tmem_holder + 2);
     int *s_pad = reinterpret_cast<int *>(tmem_holder + 4);  // [E + 1]
+    uint32_t *stage_out = reinterpret_cast<uint32_t *>(s_pad + MOK_MAX_EXPERTS + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             if (f1) {
                 epi_ffn1<MX>(trow, valid, q, n * 128, a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b,
-                             a.saved_h, release);
+                             a.saved_h, stage_out + (warp - 2) * kStageWords, lane, release);
             } else {
                 uint16_t *dst = nullptr;
                 if (valid) {
@@ -441,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k + a.row_j[p]) * a.d +
                           n * a.BN2;
                 }
-                epi_rows_bf16(trow, a.BN2, false, valid, dst, release);
+                epi_rows_bf16(trow, a.BN2, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
+                              release);
             }
             if (!released) release();
             acc_phase ^= 1u;
@@ -499,7 +501,7 @@ template <bool MX>
 constexpr size_t fused_smem_bytes()
 {
     return 1024 + kStages * (kAStage + kBStage) + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0) +
-           (2 * kStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + (MOK_MAX_EXPERTS + 1) * 4;
+           (2 * kStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
 }
 
 template <bool MX>

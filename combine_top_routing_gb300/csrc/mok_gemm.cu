@@ -49,6 +49,10 @@ namespace {
 #define MOK_GEMM_CLUSTER 1
 #endif
 constexpr int kCluster = MOK_GEMM_CLUSTER;  // CTAs per cluster of the GEMM launch
+#ifndef MOK_GEMM_PAIR
+#define MOK_GEMM_PAIR 0
+#endif
+constexpr bool kPairGemm = MOK_GEMM_PAIR != 0;  // forward GEMMs on CTA pairs (cta_group::2)
 
 enum { MODE_ROUTER = 0, MODE_FFN1, MODE_FFN2, MODE_DGRAD2, MODE_DGRAD1, MODE_WGRAD };
 
@@ -159,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(tmem_holder + 4);  // [groups + 1]
+    uint32_t *stage_out = reinterpret_cast<uint32_t *>(prefix + MOK_MAX_EXPERTS + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -369,7 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int e = tl.group;
                 const int row_in_e = tl.m_blk * kBM + r;
                 epi_ffn1<MX>(trow, row_in_e < a.counts[e], a.pad_offsets[e] + row_in_e, tl.n_blk * 128,
-                             a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b, a.saved_h, release);
+                             a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b, a.saved_h,
+                             stage_out + (warp - 2) * kStageWords, lane, release);
             } else if constexpr (MODE == MODE_FFN2) {
                 const int e = tl.group;
                 const int row_in_e = tl.m_blk * kBM + r;
@@ -381,7 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t j = a.row_j[p];
                     dst = a.ystage + (t * a.k_top + j) * a.d + tl.n_blk * BN;
                 }
-                epi_rows_bf16(trow, BN, false, valid, dst, release);
+                epi_rows_bf16(trow, BN, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
+                              release);
             } else if constexpr (MODE == MODE_DGRAD2) {
                 // dh -> SwiGLU backward with the saved (BF16) a, b:
                 //   s = sigmoid(a), da = dh b s (1 + a (1 - s)), db = dh a s
@@ -434,20 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const bool valid = row_in_e < a.counts[e];
                 const int64_t grow = a.pad_offsets[e] + row_in_e;
                 uint16_t *dst = a.out_rows + grow * a.d + tl.n_blk * BN;
-                uint32_t pk[128];
-                drain_row_bf16(trow, BN, false, pk);
-                release();
-                if (valid) store_row_bf16(dst, BN, pk);
+                epi_rows_bf16(trow, BN, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
+                              release);
             } else {  // MODE_WGRAD
                 const int e = tl.group;
                 const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
                 uint16_t *dst = a.out_rows +
                                 (static_cast<int64_t>(e) * a.m_rows + tl.m_blk * kBM + r) * a.out_ld +
                                 tl.n_blk * BN;
-                uint32_t pk[128];
-                drain_row_bf16(trow, BN, empty_k, pk);
-                release();
-                store_row_bf16(dst, BN, pk);
+                epi_rows_bf16(trow, BN, empty_k, true, dst, stage_out + (warp - 2) * kStageWords, lane,
+                              release);
             }
             if (!released) release();
             acc_phase ^= 1u;
@@ -467,11 +470,301 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair variant of FFN1 / FFN2 (cta_group::2): clusters of two CTAs compute
+// a 256 x 256 tile -- each CTA loads its own 128 rows of A and one half of B
+// (FFN1: CTA 0 the 128 W_g rows, CTA 1 the 128 W_u rows; FFN2: 128 rows of
+// W_d each) into 32 KB stages, six stages deep.  The even CTA issues the MMAs
+// for the pair; the odd CTA forwards "stage loaded" to it with a remote
+// mbarrier arrive; the MMA commits release the stage and publish the
+// accumulator in both CTAs (multicast); both CTAs' epilogue warps hand the
+// accumulator back to the even CTA.  Every CTA of a pair walks the same tile
+// sequence; an odd last row tile of an expert is computed and discarded.
+// ---------------------------------------------------------------------------
+constexpr int kPStages = 6;
+constexpr int kPStage = kAStage + 128 * kBKBytes;  // 32 KB
+
+template <int MODE, bool MX>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_pair(const __grid_constant__ AMaps<2> am, const __grid_constant__ CUtensorMap tmB0,
+                const __grid_constant__ CUtensorMap tmB1, const GemmArgs a)
+{
+    static_assert(MODE == MODE_FFN1 || MODE == MODE_FFN2, "pair path: forward GEMMs");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sT = smem;  // stage s: A at s*32K, B half at s*32K + 16K
+    uint8_t *sSF = sT + kPStages * kPStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kPStages * (kSfaBytes + kSfbBytes) : 0));
+    uint64_t *full = bars;
+    uint64_t *empty = bars + kPStages;
+    uint64_t *peer_full = bars + 2 * kPStages;
+    uint64_t *acc_full = bars + 3 * kPStages;
+    uint64_t *acc_empty = acc_full + 1;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_empty + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    int *prefix = reinterpret_cast<int *>(tmem_holder + 4);
+    uint32_t *stage_out = reinterpret_cast<uint32_t *>(prefix + MOK_MAX_EXPERTS + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair = blockIdx.x >> 1;
+    const int npairs = gridDim.x >> 1;
+    const int groups = a.E;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&peer_full[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&am.m[0]);
+        prefetch_tmap(&tmB0);
+        prefetch_tmap(&tmB1);
+    }
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 2) {
+        const int per = (groups + 31) / 32;
+        const int g0 = lane * per;
+        int local = 0;
+        for (int g = g0; g < g0 + per && g < groups; ++g)
+            local += ((a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM + 1) / 2 * a.n_tiles;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int g = g0; g < g0 + per && g < groups; ++g) {
+            prefix[g] = run;
+            run += ((a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM + 1) / 2 * a.n_tiles;
+        }
+        if (lane == 31) prefix[groups] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int total = prefix[groups];
+    constexpr int kE = MX ? 128 : 64;
+    const uint32_t stage_bytes = kPStage + (MX ? kSfaBytes + kSfbBytes : 0);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------- TMA producer (both CTAs)
+            uint32_t stage = 0, phase = 0;
+            for (int tile = pair; tile < total; tile += npairs) {
+                const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
+                const int g = tl.group;
+                const int ya = a.pad_offsets[g] + (2 * tl.m_blk + static_cast<int>(rank)) * kBM;
+                int yb, ysf;
+                const CUtensorMap *bmap;
+                if constexpr (MODE == MODE_FFN1) {
+                    yb = g * a.b_rows_per_group + tl.n_blk * 128;
+                    ysf = yb;
+                    bmap = rank ? &tmB1 : &tmB0;
+                } else {
+                    ysf = g * a.b_rows_per_group + tl.n_blk * 256;
+                    yb = ysf + static_cast<int>(rank) * 128;
+                    bmap = &tmB0;
+                }
+                for (int ks = 0; ks < a.k_stages; ++ks) {
+                    if (!wait_bar(&empty[stage], phase ^ 1u, a.status, a.wait_ns, abort_flag)) goto producer_done;
+                    uint8_t *dA = sT + stage * kPStage;
+                    const int x = ks * kE;
+                    mbar_arrive_expect_tx(&full[stage], stage_bytes);
+                    tma_load_2d(dA, &am.m[0], &full[stage], x, ya);
+                    tma_load_2d(dA + kAStage, bmap, &full[stage], x, yb);
+                    if constexpr (MX) {
+                        uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
+                        // an odd CTA's row tile past the last expert segment is computed and
+                        // discarded: fetch some in-range scales for it
+                        const int ya_sf = ya < a.sfa_rows[0] ? ya : static_cast<int>(a.sfa_rows[0]) - kBM;
+                        bulk_load(dS, a.sfa[0] + scale_word(x, ya_sf, a.sfa_rows[0]), kSfaBytes, &full[stage]);
+                        if constexpr (MODE == MODE_FFN1) {
+                            bulk_load(dS + kSfaBytes, a.sfb[0] + scale_word(x, ysf, a.sfb_rows[0]), 512, &full[stage]);
+                            bulk_load(dS + kSfaBytes + 512, a.sfb[1] + scale_word(x, ysf, a.sfb_rows[1]), 512,
+                                      &full[stage]);
+                        } else {
+                            bulk_load(dS + kSfaBytes, a.sfb[0] + scale_word(x, ysf, a.sfb_rows[0]), 1024,
+                                      &full[stage]);
+                        }
+                    }
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 1) {
+            // ---------------------------------------- odd CTA: forward "stage loaded"
+            uint32_t stage = 0, phase = 0;
+            const uint32_t peer0 = mapa_shared(smem_u32(peer_full), 0);
+            for (int tile = pair; tile < total; tile += npairs) {
+                for (int ks = 0; ks < a.k_stages; ++ks) {
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto fwd_done;
+                    mbar_arrive_remote(peer0 + stage * 8);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        fwd_done:;
+        } else if (lane == 0) {
+            // ---------------------------------------- even CTA: MMA issue for the pair
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            const uint32_t idesc = idesc_bf16(2 * kBM, 256);
+            for (int tile = pair; tile < total; tile += npairs) {
+                if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
+                tc_fence_after();
+                for (int ks = 0; ks < a.k_stages; ++ks) {
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    if (!wait_bar(&peer_full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    tc_fence_after();
+                    const uint32_t aaddr = smem_u32(sT + stage * kPStage);
+                    const uint32_t baddr = aaddr + kAStage;
+                    const uint32_t sfa_col = tmem + kSfCol + stage * 16;
+                    const uint32_t sfb_col = sfa_col + 4;
+                    if (MX) {
+                        const uint32_t sbase = smem_u32(sSF + stage * (kSfaBytes + kSfbBytes));
+                        tmem_cp_32x128b_warpx4_pair(sfa_col, sdesc_sf(sbase));
+                        tmem_cp_32x128b_warpx4_pair(sfb_col, sdesc_sf(sbase + kSfaBytes));
+                        tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sdesc_sf(sbase + kSfaBytes + 512));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_k_sw128(aaddr + kk * 32);
+                        const uint64_t bd = sdesc_k_sw128(baddr + kk * 32);
+                        const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
+                        if (MX) mma_mxf8_pair(tmem, ad, bd, idesc_mxf8(2 * kBM, 256, kk, kk), sfa_col, sfb_col, accum);
+                        else mma_bf16_pair(tmem, ad, bd, idesc, accum);
+                    }
+                    tc_commit_pair(&empty[stage], 0x3);
+                    if (++stage == kPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit_pair(acc_full, 0x3);
+                acc_phase ^= 1u;
+            }
+        mma_done:;
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
+        uint32_t acc_phase = 0;
+        for (int tile = pair; tile < total; tile += npairs) {
+            const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
+            if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
+            tc_fence_after();
+            bool released = false;
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(acc_empty_leader);
+                released = true;
+            };
+            const int e = tl.group;
+            const int row_in_e = (2 * tl.m_blk + static_cast<int>(rank)) * kBM + r;
+            const bool valid = row_in_e < a.counts[e];
+            if constexpr (MODE == MODE_FFN1) {
+                epi_ffn1<MX>(trow, valid, a.pad_offsets[e] + row_in_e, tl.n_blk * 128, a.F, a.h, a.h_scales,
+                             a.h_rows, a.saved_a, a.saved_b, a.saved_h, stage_out + (warp - 2) * kStageWords,
+                             lane, release);
+            } else {
+                uint16_t *dst = nullptr;
+                if (valid) {
+                    const int64_t p = a.offsets[e] + row_in_e;
+                    dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k_top + a.row_j[p]) * a.d +
+                          tl.n_blk * 256;
+                }
+                epi_rows_bf16(trow, 256, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
+                              release);
+            }
+            if (!released) release();
+            acc_phase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no more remote arrives or multicast commits into either CTA
+    if (*abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+template <bool MX>
+constexpr size_t pair_smem_bytes()
+{
+    return 1024 + kPStages * kPStage + (MX ? kPStages * (kSfaBytes + kSfbBytes) : 0) +
+           (3 * kPStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+}
+
+template <int MODE, bool MX>
+cudaError_t launch_gemm_pair(const AMaps<2> &am, const CUtensorMap &b0, const CUtensorMap &b1,
+                             const GemmArgs &args, cudaStream_t st)
+{
+    constexpr size_t smem = pair_smem_bytes<MX>();
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int grid = 0;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(k_gemm_pair<MODE, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+        cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
+        int clusters = 0;
+        if (attr_err == cudaSuccess)
+            attr_err = cudaOccupancyMaxActiveClusters(&clusters, k_gemm_pair<MODE, MX>, &cfg);
+        grid = clusters * 2;
+        if (attr_err == cudaSuccess && grid == 0) attr_err = cudaErrorInvalidConfiguration;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.stream = st;
+    return cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE, MX>, am, b0, b1, args);
+}
+
 template <bool MX>
 constexpr size_t smem_bytes()
 {
     return 1024 + kStages * (kAStage + kBStage) + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0) +
-           (2 * kStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 1) * 4;
+           (2 * kStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
 }
 
 template <int MODE, bool MX>
@@ -625,8 +918,13 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
     g1.saved_a = saved_a;
     g1.saved_b = saved_b;
     g1.saved_h = saved_h;
-    cudaError_t err = mx ? launch_gemm<MODE_FFN1, true>(a1, bg, bu, g1, st)
-                         : launch_gemm<MODE_FFN1, false>(a1, bg, bu, g1, st);
+    cudaError_t err;
+    if (kPairGemm)
+        err = mx ? launch_gemm_pair<MODE_FFN1, true>(a1, bg, bu, g1, st)
+                 : launch_gemm_pair<MODE_FFN1, false>(a1, bg, bu, g1, st);
+    else
+        err = mx ? launch_gemm<MODE_FFN1, true>(a1, bg, bu, g1, st)
+                 : launch_gemm<MODE_FFN1, false>(a1, bg, bu, g1, st);
     if (err != cudaSuccess) return err;
 
     // GEMM2: y = h W_d^T scattered to ystage
@@ -642,6 +940,9 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
     g2.ystage = ystage;
     g2.row_tok = row_tok;
     g2.row_j = row_j;
+    if (kPairGemm && g2.BN == 256)
+        return mx ? launch_gemm_pair<MODE_FFN2, true>(a2, bd, bd, g2, st)
+                  : launch_gemm_pair<MODE_FFN2, false>(a2, bd, bd, g2, st);
     return mx ? launch_gemm<MODE_FFN2, true>(a2, bd, bd, g2, st)
               : launch_gemm<MODE_FFN2, false>(a2, bd, bd, g2, st);
 }

@@ -129,6 +129,42 @@ __device__ __forceinline__ void drain_row_bf16(uint32_t trow, int BN, bool zero,
     }
 }
 
+// Shared-memory staging for epilogue stores: 32 rows x 33 words per warp
+// (one padding word per row keeps the row-wise writes conflict-free).
+constexpr int kStageWords = 32 * 33;
+constexpr int kStageBytes = 4 * kStageWords * 4;  // four epilogue warps
+
+// Writes each lane's row -- nwords 32-bit words of pk (nwords a multiple of
+// 32) -- to dst (nullptr: skip the row) as contiguous 128-byte segments: one
+// 128-byte column slice of the warp's 32 rows at a time goes through `stage`,
+// then eight lanes store one row's slice, four rows per instruction.
+template <int MAXW>
+__device__ __forceinline__ void store_rows_staged(const uint32_t (&pk)[MAXW], int nwords, void *dst,
+                                                  uint32_t *stage, int lane)
+{
+    const unsigned long long d64 = reinterpret_cast<unsigned long long>(dst);
+#pragma unroll
+    for (int c0 = 0; c0 < MAXW; c0 += 32) {
+        if (c0 < nwords) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stage[lane * 33 + i] = pk[c0 + i];
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int row = j * 4 + (lane >> 3);
+                const int w = (lane & 7) * 4;
+                const unsigned long long rd = __shfl_sync(0xffffffffu, d64, row);
+                if (rd) {
+                    const uint32_t *sp = stage + row * 33 + w;
+                    *reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(rd) + (c0 + w) * 4) =
+                        make_uint4(sp[0], sp[1], sp[2], sp[3]);
+                }
+            }
+            __syncwarp();
+        }
+    }
+}
+
 // Stores BN packed BF16 values (16-byte stores).
 __device__ __forceinline__ void store_row_bf16(uint16_t *dst, int BN, const uint32_t (&pk)[128])
 {
@@ -148,7 +184,7 @@ template <bool MX, typename Release>
 __device__ __forceinline__ void epi_ffn1(uint32_t trow, bool valid, int64_t grow, int f0, int F,
                                          void *h, uint32_t *h_scales, int64_t h_rows,
                                          uint16_t *saved_a, uint16_t *saved_b, uint16_t *saved_h,
-                                         Release &&release)
+                                         uint32_t *stage, int lane, Release &&release)
 {
     uint32_t sword = 0;
     if (!saved_a && !saved_b && !saved_h) {
@@ -183,21 +219,12 @@ __device__ __forceinline__ void epi_ffn1(uint32_t trow, bool valid, int64_t grow
             }
         }
         release();
-        if (valid) {
-            const int64_t off = grow * F + f0;
-            if (!MX) {
-                uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(h) + off);
-#pragma unroll
-                for (int q = 0; q < 16; ++q)
-                    o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
-            } else {
-                uint4 *o = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(h) + off);
-#pragma unroll
-                for (int q = 0; q < 8; ++q)
-                    o[q] = make_uint4(hq[4 * q], hq[4 * q + 1], hq[4 * q + 2], hq[4 * q + 3]);
-                h_scales[scale_word_row(f0 >> 7, grow, h_rows)] = sword;
-            }
-        }
+        const int64_t off = grow * F + f0;
+        void *dst = valid ? (MX ? static_cast<void *>(static_cast<uint8_t *>(h) + off)
+                                : static_cast<void *>(static_cast<uint16_t *>(h) + off))
+                          : nullptr;
+        store_rows_staged(hq, MX ? 32 : 64, dst, stage, lane);
+        if (MX && valid) h_scales[scale_word_row(f0 >> 7, grow, h_rows)] = sword;
         return;
     }
     // training: a, b, h also stored (BF16); stores happen before the release
@@ -235,15 +262,16 @@ __device__ __forceinline__ void epi_ffn1(uint32_t trow, bool valid, int64_t grow
 }
 
 // Plain row epilogue: BN fp32 columns -> BF16 at dst (zeros when `zero`),
-// TMEM released before the stores.
+// TMEM released before the (staged, coalesced) stores.
 template <typename Release>
 __device__ __forceinline__ void epi_rows_bf16(uint32_t trow, int BN, bool zero, bool valid,
-                                              uint16_t *dst, Release &&release)
+                                              uint16_t *dst, uint32_t *stage, int lane,
+                                              Release &&release)
 {
     uint32_t pk[128];
     drain_row_bf16(trow, BN, zero, pk);
     release();
-    if (valid) store_row_bf16(dst, BN, pk);
+    store_rows_staged(pk, BN / 2, valid ? dst : nullptr, stage, lane);
 }
 
 }  // namespace mok
