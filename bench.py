@@ -63,6 +63,23 @@ def _dist():
     return rank, world, local
 
 
+def reduce_max(value: float, device=None) -> float:
+    """Max of `value` over the ranks of the default process group (the job's
+    time is its slowest rank's); the value itself when not distributed."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -288,11 +305,8 @@ def main():
     status = layer.status()
     if status != 0:
         raise RuntimeError(f"device status {mok.status_string(status)}")
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * w.T / (ms / 1e3)
+    ms = reduce_max(ms, "cuda")
+    value = job_throughput(w.T, world, ms)
 
     # ---------------- forward + backward (training layer: saved context)
     fb_ms = None
@@ -314,11 +328,7 @@ def main():
         torch.cuda.synchronize()
         if tl.status() != 0:
             raise RuntimeError("device status after backward: " + mok.status_string(tl.status()))
-        fb_ms = f0.elapsed_time(f1) / fb_steps
-        if world > 1:
-            t = torch.tensor([fb_ms], device="cuda")
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            fb_ms = float(t.item())
+        fb_ms = reduce_max(f0.elapsed_time(f1) / fb_steps, "cuda")
         del tl
         torch.cuda.empty_cache()
 
@@ -383,12 +393,8 @@ def main():
         _e2e_step(layer, x_host, out_host)
     s1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = s0.elapsed_time(s1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_val = world * w.T / (e2e_ms / 1e3)
+    e2e_ms = reduce_max(s0.elapsed_time(s1) / e2e_steps, "cuda")
+    e2e_val = job_throughput(w.T, world, e2e_ms)
 
     base = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -423,7 +429,7 @@ def main():
                                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /
                                            peaks.get("hbm_gbs", 6800.0)},
             "fwd_bwd": None if fb_ms is None else {
-                "value": world * w.T / (fb_ms / 1e3), "unit": "tokens/s", "ms_per_step": fb_ms,
+                "value": job_throughput(w.T, world, fb_ms), "unit": "tokens/s", "ms_per_step": fb_ms,
                 "tensor_frac": 3 * flops / (fb_ms / 1e3) / 1e12 / peak_tc},
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2},
