@@ -177,6 +177,20 @@ def _layer_bytes(w):
     return weights + x + xe + h + ystage + out
 
 
+def _dispatch_bytes(w):
+    """Algorithmic HBM bytes of the pull dispatch: every token row read once,
+    every slot row written once (codes + scales), the row index read."""
+    e = 1 if w.dtype == "mxfp8" else 2
+    sc = 1 / 32 if w.dtype == "mxfp8" else 0
+    return w.T * w.d * 2 + w.S * w.d * (e + sc) + w.S * 4
+
+
+def _combine_bytes(w):
+    """Algorithmic HBM bytes of the weighted combine: every staged y row and
+    gate read once, every output row written once."""
+    return w.S * w.d * 2 + w.S * 4 + w.T * w.d * 2
+
+
 def run_reference(args):
     """The oracle as it stands, timed on the host cores on a bounded token sample."""
     rank, world, _ = _dist()
@@ -347,6 +361,17 @@ def main():
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / iters
 
+    # the HBM-bound steps on their own (separate kernels, same stream)
+    disp_ms = timed(lambda: mok.dispatch(layer.cfg, layer.x_src, R.ids, R.offsets, R.pad_offsets,
+                                         R.row_tok, R.row_j, R.xe, R.xs))
+    comb_ms = timed(lambda: mok.combine(layer.cfg, R.ystage, R.gates, layer.out))
+    hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    hbm_steps = {}
+    for name, ms_, nbytes in (("dispatch", disp_ms, _dispatch_bytes(w)),
+                              ("combine", comb_ms, _combine_bytes(w))):
+        gbs = nbytes / (ms_ / 1e3) / 1e9
+        hbm_steps[name] = {"ms": ms_, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+                           "peak_gbs": hbm_peak, "frac": gbs / hbm_peak}
     fused_ms = timed(lambda: mok.moe_fused(layer.cfg, layer.x_src, layer.wstruct, R.ids, R.gates,
                                            R.counts, R.offsets, R.pad_offsets, R.row_tok, R.row_j,
                                            R.ystage, layer.out, layer.ws))
@@ -424,6 +449,7 @@ def main():
                          "ms_per_launch": fused_ms},
             "expert_ffn_separate_kernels": {"ms": ffn_ms,
                                             "tflops": flops / (ffn_ms / 1e3) / 1e12},
+            "hbm_steps": hbm_steps,
             "sweep": sweep,
             "layer_roofline": {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
                                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /

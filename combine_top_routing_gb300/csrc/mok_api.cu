@@ -202,6 +202,20 @@ int encode_tmap_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner_el
     return r == CUDA_SUCCESS ? 0 : 1;
 }
 
+int encode_tmap_scales(CUtensorMap *m, const uint32_t *base, uint64_t rows, uint64_t K)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15) || rows % 128 || K % 128) return 1;
+    cuuint64_t dims[2] = {128, (K / 128) * (rows / 128)};
+    cuuint64_t strides[1] = {512};
+    cuuint32_t box[2] = {128, 1};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(base), dims, strides,
+                    box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : 1;
+}
+
 static uint64_t wait_ns(const mok_config *cfg)
 {
     return cfg->wait_limit_ns ? cfg->wait_limit_ns : 2000000000ull;

@@ -35,6 +35,8 @@
 // CTAs share B tiles and the group's rows through L2.
 #include <cuda_bf16.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "mok_internal.h"
@@ -52,7 +54,16 @@ constexpr int kCluster = MOK_GEMM_CLUSTER;  // CTAs per cluster of the GEMM laun
 #ifndef MOK_GEMM_PAIR
 #define MOK_GEMM_PAIR 0
 #endif
-constexpr bool kPairGemm = MOK_GEMM_PAIR != 0;  // forward GEMMs on CTA pairs (cta_group::2)
+// Forward expert GEMMs of the separate-kernel path on CTA pairs (cta_group::2):
+// the compiled default, overridden by the environment variable MOK_GEMM_PAIR
+// ("0" or "1") read at each launch.
+constexpr bool kPairGemm = MOK_GEMM_PAIR != 0;
+bool use_pair_gemm()
+{
+    const char *v = getenv("MOK_GEMM_PAIR");
+    if (v && (v[0] == '0' || v[0] == '1')) return v[0] == '1';
+    return kPairGemm;
+}
 
 enum { MODE_ROUTER = 0, MODE_FFN1, MODE_FFN2, MODE_DGRAD2, MODE_DGRAD1, MODE_WGRAD };
 
@@ -474,20 +485,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTA-pair variant of FFN1 / FFN2 (cta_group::2): clusters of two CTAs compute
 // a 256 x 256 tile -- each CTA loads its own 128 rows of A and one half of B
 // (FFN1: CTA 0 the 128 W_g rows, CTA 1 the 128 W_u rows; FFN2: 128 rows of
-// W_d each) into 32 KB stages, six stages deep.  The even CTA issues the MMAs
-// for the pair; the odd CTA forwards "stage loaded" to it with a remote
-// mbarrier arrive; the MMA commits release the stage and publish the
-// accumulator in both CTAs (multicast); both CTAs' epilogue warps hand the
-// accumulator back to the even CTA.  Every CTA of a pair walks the same tile
-// sequence; an odd last row tile of an expert is computed and discarded.
+// W_d each) into 32 KB stages, six stages deep, plus (MXFP8) its A rows'
+// scale tile and the scale tiles of all 256 B rows.  Every load of both CTAs
+// is a tensor-map copy whose completion is counted on the even CTA's "full"
+// barrier, which the even CTA arms for the bytes of both; the even CTA issues
+// the MMAs and scale copies for the pair; the MMA commits release the stage
+// and publish the accumulator in both CTAs (multicast); both CTAs' epilogue
+// warps hand the accumulator back to the even CTA.  Every CTA of a pair walks
+// the same tile sequence; an odd last row tile of an expert is computed and
+// discarded (its A rows and scales beyond the matrix read as zeros).
 // ---------------------------------------------------------------------------
 constexpr int kPStages = 6;
 constexpr int kPStage = kAStage + 128 * kBKBytes;  // 32 KB
 
+struct PairMaps {
+    CUtensorMap a, b0, b1;     // A rows; B rows (FFN1: W_g, W_u; FFN2: W_d twice)
+    CUtensorMap sa, sb0, sb1;  // scale tiles of A and of B (MXFP8 only)
+};
+
+// index of the scale tile of (k element x, row y) in a [rows, K] matrix
+__device__ __forceinline__ int sf_tile(int x, int y, int64_t rows)
+{
+    return static_cast<int>((x >> 7) * (rows >> 7) + (y >> 7));
+}
+
 template <int MODE, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_pair(const __grid_constant__ AMaps<2> am, const __grid_constant__ CUtensorMap tmB0,
-                const __grid_constant__ CUtensorMap tmB1, const GemmArgs a)
+    k_gemm_pair(const __grid_constant__ PairMaps pm, const GemmArgs a)
 {
     static_assert(MODE == MODE_FFN1 || MODE == MODE_FFN2, "pair path: forward GEMMs");
     extern __shared__ uint8_t smem_raw[];
@@ -498,8 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kPStages * (kSfaBytes + kSfbBytes) : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + kPStages;
-    uint64_t *peer_full = bars + 2 * kPStages;
-    uint64_t *acc_full = bars + 3 * kPStages;
+    uint64_t *acc_full = bars + 2 * kPStages;
     uint64_t *acc_empty = acc_full + 1;
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -517,7 +540,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kPStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&peer_full[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);
@@ -525,11 +547,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&am.m[0]);
-        prefetch_tmap(&tmB0);
-        prefetch_tmap(&tmB1);
+        prefetch_tmap(&pm.a);
+        prefetch_tmap(&pm.b0);
+        prefetch_tmap(&pm.b1);
+        if (MX) {
+            prefetch_tmap(&pm.sa);
+            prefetch_tmap(&pm.sb0);
+            prefetch_tmap(&pm.sb1);
+        }
     }
-    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive or load
     if (warp == 1) {
         tmem_alloc_pair(tmem_holder, kTmemCols);
         tmem_relinquish_pair();
@@ -559,12 +586,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const int total = prefix[groups];
     constexpr int kE = MX ? 128 : 64;
-    const uint32_t stage_bytes = kPStage + (MX ? kSfaBytes + kSfbBytes : 0);
+    // bytes one CTA lands per stage; the even CTA's barrier counts both CTAs'
+    const uint32_t cta_bytes = kPStage + (MX ? kSfaBytes + kSfbBytes : 0);
 
     if (warp == 0) {
         if (lane == 0) {
             // ---------------------------------------------- TMA producer (both CTAs)
             uint32_t stage = 0, phase = 0;
+            const uint32_t full0 = mapa_shared(smem_u32(full), 0);
             for (int tile = pair; tile < total; tile += npairs) {
                 const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
                 const int g = tl.group;
@@ -574,32 +603,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (MODE == MODE_FFN1) {
                     yb = g * a.b_rows_per_group + tl.n_blk * 128;
                     ysf = yb;
-                    bmap = rank ? &tmB1 : &tmB0;
+                    bmap = rank ? &pm.b1 : &pm.b0;
                 } else {
                     ysf = g * a.b_rows_per_group + tl.n_blk * 256;
                     yb = ysf + static_cast<int>(rank) * 128;
-                    bmap = &tmB0;
+                    bmap = &pm.b0;
                 }
                 for (int ks = 0; ks < a.k_stages; ++ks) {
                     if (!wait_bar(&empty[stage], phase ^ 1u, a.status, a.wait_ns, abort_flag)) goto producer_done;
                     uint8_t *dA = sT + stage * kPStage;
                     const int x = ks * kE;
-                    mbar_arrive_expect_tx(&full[stage], stage_bytes);
-                    tma_load_2d(dA, &am.m[0], &full[stage], x, ya);
-                    tma_load_2d(dA + kAStage, bmap, &full[stage], x, yb);
+                    const uint32_t fb = full0 + stage * 8;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * cta_bytes);
+                    tma_load_2d_pair(dA, &pm.a, fb, x, ya);
+                    tma_load_2d_pair(dA + kAStage, bmap, fb, x, yb);
                     if constexpr (MX) {
                         uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
-                        // an odd CTA's row tile past the last expert segment is computed and
-                        // discarded: fetch some in-range scales for it
-                        const int ya_sf = ya < a.sfa_rows[0] ? ya : static_cast<int>(a.sfa_rows[0]) - kBM;
-                        bulk_load(dS, a.sfa[0] + scale_word(x, ya_sf, a.sfa_rows[0]), kSfaBytes, &full[stage]);
+                        tma_load_2d_pair(dS, &pm.sa, fb, 0, sf_tile(x, ya, a.sfa_rows[0]));
                         if constexpr (MODE == MODE_FFN1) {
-                            bulk_load(dS + kSfaBytes, a.sfb[0] + scale_word(x, ysf, a.sfb_rows[0]), 512, &full[stage]);
-                            bulk_load(dS + kSfaBytes + 512, a.sfb[1] + scale_word(x, ysf, a.sfb_rows[1]), 512,
-                                      &full[stage]);
+                            tma_load_2d_pair(dS + kSfaBytes, &pm.sb0, fb, 0, sf_tile(x, ysf, a.sfb_rows[0]));
+                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.sb1, fb, 0, sf_tile(x, ysf, a.sfb_rows[1]));
                         } else {
-                            bulk_load(dS + kSfaBytes, a.sfb[0] + scale_word(x, ysf, a.sfb_rows[0]), 1024,
-                                      &full[stage]);
+                            tma_load_2d_pair(dS + kSfaBytes, &pm.sb0, fb, 0, sf_tile(x, ysf, a.sfb_rows[0]));
+                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.sb0, fb, 0,
+                                             sf_tile(x, ysf + 128, a.sfb_rows[0]));
                         }
                     }
                     if (++stage == kPStages) {
@@ -611,22 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         producer_done:;
         }
     } else if (warp == 1) {
-        if (lane == 0 && rank == 1) {
-            // ---------------------------------------- odd CTA: forward "stage loaded"
-            uint32_t stage = 0, phase = 0;
-            const uint32_t peer0 = mapa_shared(smem_u32(peer_full), 0);
-            for (int tile = pair; tile < total; tile += npairs) {
-                for (int ks = 0; ks < a.k_stages; ++ks) {
-                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto fwd_done;
-                    mbar_arrive_remote(peer0 + stage * 8);
-                    if (++stage == kPStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-            }
-        fwd_done:;
-        } else if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             // ---------------------------------------- even CTA: MMA issue for the pair
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             const uint32_t idesc = idesc_bf16(2 * kBM, 256);
@@ -635,7 +647,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int ks = 0; ks < a.k_stages; ++ks) {
                     if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
-                    if (!wait_bar(&peer_full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
                     tc_fence_after();
                     const uint32_t aaddr = smem_u32(sT + stage * kPStage);
                     const uint32_t baddr = aaddr + kAStage;
@@ -708,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();  // no more remote arrives or multicast commits into either CTA
+    cluster_sync_all();  // no more remote arrives, loads or multicast commits into either CTA
     if (*abort_flag) {
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
@@ -723,12 +734,11 @@ template <bool MX>
 constexpr size_t pair_smem_bytes()
 {
     return 1024 + kPStages * kPStage + (MX ? kPStages * (kSfaBytes + kSfbBytes) : 0) +
-           (3 * kPStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+           (2 * kPStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
 }
 
 template <int MODE, bool MX>
-cudaError_t launch_gemm_pair(const AMaps<2> &am, const CUtensorMap &b0, const CUtensorMap &b1,
-                             const GemmArgs &args, cudaStream_t st)
+cudaError_t launch_gemm_pair(const PairMaps &pm, const GemmArgs &args, cudaStream_t st)
 {
     constexpr size_t smem = pair_smem_bytes<MX>();
     static std::once_flag once;
@@ -757,7 +767,7 @@ cudaError_t launch_gemm_pair(const AMaps<2> &am, const CUtensorMap &b0, const CU
     if (attr_err != cudaSuccess) return attr_err;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.stream = st;
-    return cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE, MX>, am, b0, b1, args);
+    return cudaLaunchKernelEx(&cfg, k_gemm_pair<MODE, MX>, pm, args);
 }
 
 template <bool MX>
@@ -918,10 +928,26 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
     g1.saved_a = saved_a;
     g1.saved_b = saved_b;
     g1.saved_h = saved_h;
+    const bool pair = use_pair_gemm();
+    PairMaps p1 = {}, p2 = {};
+    if (pair) {
+        p1.a = a1.m[0];
+        p1.b0 = bg;
+        p1.b1 = bu;
+        p2.a = a2.m[0];
+        p2.b0 = p2.b1 = bd;
+        if (mx && (encode_tmap_scales(&p1.sa, xe_scales, dm.rows_pad, dm.d) ||
+                   encode_tmap_scales(&p1.sb0, w->s_gate, EF, dm.d) ||
+                   encode_tmap_scales(&p1.sb1, w->s_up, EF, dm.d) ||
+                   encode_tmap_scales(&p2.sa, h_scales, dm.rows_pad, dm.F) ||
+                   encode_tmap_scales(&p2.sb0, w->s_down, Ed, dm.F)))
+            return cudaErrorInvalidValue;
+        p2.sb1 = p2.sb0;
+        if (!mx) p1.sa = p1.sb0 = p1.sb1 = p2.sa = p2.sb0 = p2.sb1 = bd;  // unused
+    }
     cudaError_t err;
-    if (kPairGemm)
-        err = mx ? launch_gemm_pair<MODE_FFN1, true>(a1, bg, bu, g1, st)
-                 : launch_gemm_pair<MODE_FFN1, false>(a1, bg, bu, g1, st);
+    if (pair)
+        err = mx ? launch_gemm_pair<MODE_FFN1, true>(p1, g1, st) : launch_gemm_pair<MODE_FFN1, false>(p1, g1, st);
     else
         err = mx ? launch_gemm<MODE_FFN1, true>(a1, bg, bu, g1, st)
                  : launch_gemm<MODE_FFN1, false>(a1, bg, bu, g1, st);
@@ -940,9 +966,8 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
     g2.ystage = ystage;
     g2.row_tok = row_tok;
     g2.row_j = row_j;
-    if (kPairGemm && g2.BN == 256)
-        return mx ? launch_gemm_pair<MODE_FFN2, true>(a2, bd, bd, g2, st)
-                  : launch_gemm_pair<MODE_FFN2, false>(a2, bd, bd, g2, st);
+    if (pair && g2.BN == 256)
+        return mx ? launch_gemm_pair<MODE_FFN2, true>(p2, g2, st) : launch_gemm_pair<MODE_FFN2, false>(p2, g2, st);
     return mx ? launch_gemm<MODE_FFN2, true>(a2, bd, bd, g2, st)
               : launch_gemm<MODE_FFN2, false>(a2, bd, bd, g2, st);
 }

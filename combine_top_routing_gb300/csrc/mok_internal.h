@@ -165,5 +165,9 @@ int num_sms();
 // Encodes a 2-D tiled tensor map with 128-byte swizzle; returns 0 on success.
 int encode_tmap_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner_elems,
                    uint64_t rows, uint32_t box_inner, uint32_t box_rows);
+// Encodes a map over an MX scale array of a [rows, K] matrix viewed as
+// [(K/128) * (rows/128), 128] 32-bit words: map row i is the 512-byte scale
+// tile i (k-group i / (rows/128), row tile i % (rows/128)); box = one tile.
+int encode_tmap_scales(CUtensorMap *m, const uint32_t *base, uint64_t rows, uint64_t K);
 
 }  // namespace mok

@@ -99,17 +99,28 @@ __global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ ys
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t t = i / vec_per_tok;
         const int64_t c = i % vec_per_tok;
+        // all k slot loads in flight before the (ordered) accumulation
+        uint4 y[MOK_MAX_TOPK];
+        float g[MOK_MAX_TOPK];
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j < k) {
+                g[j] = __ldg(gates + t * k + j);
+                y[j] = __ldg(reinterpret_cast<const uint4 *>(ystage + (t * k + j) * d) + c);
+            }
+        }
         float acc[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const float g = __ldg(gates + t * k + j);
-            const uint4 y = __ldg(reinterpret_cast<const uint4 *>(ystage + (t * k + j) * d) + c);
-            const uint32_t w[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[2 * q] = fmaf(g, bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
-                acc[2 * q + 1] = fmaf(g, bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j < k) {
+                const uint32_t w[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    acc[2 * q] = fmaf(g[j], bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
+                    acc[2 * q + 1] = fmaf(g[j], bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
+                }
             }
         }
         uint4 o;
