@@ -364,10 +364,13 @@ def main():
     # the HBM-bound steps on their own (separate kernels, same stream)
     disp_ms = timed(lambda: mok.dispatch(layer.cfg, layer.x_src, R.ids, R.offsets, R.pad_offsets,
                                          R.row_tok, R.row_j, R.xe, R.xs))
+    disp_tok_ms = timed(lambda: mok.dispatch_by_token(layer.cfg, layer.x_src, R.ids, R.slot_pos, R.offsets,
+                                                      R.pad_offsets, R.xe, R.xs))
     comb_ms = timed(lambda: mok.combine(layer.cfg, R.ystage, R.gates, layer.out))
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     hbm_steps = {}
     for name, ms_, nbytes in (("dispatch", disp_ms, _dispatch_bytes(w)),
+                              ("dispatch_by_token", disp_tok_ms, _dispatch_bytes(w)),
                               ("combine", comb_ms, _combine_bytes(w))):
         gbs = nbytes / (ms_ / 1e3) / 1e9
         hbm_steps[name] = {"ms": ms_, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
@@ -384,7 +387,7 @@ def main():
     sweep = None
     if args.sweep:
         sweep = []
-        for frac in (0.125, 0.25, 1 / 3):
+        for frac in (0.0625, 0.125, 0.25, 1 / 3):
             for mb in (64, 128, 256):
                 lw = MoELayer(w, inp, gather_sm_fraction=frac, minibatch_rows=mb)
                 for _ in range(2):
@@ -450,6 +453,7 @@ def main():
             "expert_ffn_separate_kernels": {"ms": ffn_ms,
                                             "tflops": flops / (ffn_ms / 1e3) / 1e12},
             "hbm_steps": hbm_steps,
+            "fused_plan": mok.fused_plan(layer.cfg),
             "sweep": sweep,
             "layer_roofline": {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
                                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /

@@ -355,6 +355,21 @@ int mok_dispatch(const mok_config *cfg, const void *const *x_src, const int32_t 
                                        xe_scales, static_cast<cudaStream_t>(stream)));
 }
 
+int mok_dispatch_by_token(const mok_config *cfg, const void *const *x_src, const int32_t *ids,
+                          const int32_t *slot_pos, const int32_t *offsets, const int32_t *pad_offsets,
+                          void *xe, uint32_t *xe_scales, void *stream)
+{
+    Dims dm;
+    int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!ids || !slot_pos || !offsets || !pad_offsets || !xe) return MOK_ERR_INVALID_ARG;
+    if (dm.dtype == MOK_MXFP8 && !xe_scales) return MOK_ERR_INVALID_ARG;
+    Sources src;
+    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    return cuda_status(launch_dispatch_by_token(dm, src, ids, slot_pos, offsets, pad_offsets, xe, xe_scales,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int mok_expert_ffn(const mok_config *cfg, const void *xe, const uint32_t *xe_scales,
                    const mok_weights *w, const int32_t *offsets, const int32_t *pad_offsets,
                    const int32_t *row_tok, const uint8_t *row_j, void *ystage, void *saved_a,
@@ -451,6 +466,22 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     io.counters = at<int>(ws, fw.counters);
     e = launch_fused(dm, cfg, src, io, w, status, wait_ns(cfg), st);
     return cuda_status(e);
+}
+
+int mok_fused_plan(const mok_config *cfg, int *ctas, int *gather_ctas, int *minibatch_rows,
+                   int64_t *ring_rows)
+{
+    Dims dm;
+    const int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    int ng, mb;
+    const int grid = fused_ctas(dm, cfg, num_sms());
+    fused_knobs(dm, cfg, grid, &ng, &mb);
+    if (ctas) *ctas = grid;
+    if (gather_ctas) *gather_ctas = ng;
+    if (minibatch_rows) *minibatch_rows = mb;
+    if (ring_rows) *ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
+    return MOK_OK;
 }
 
 int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_weights *w,

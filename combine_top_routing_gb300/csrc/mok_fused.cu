@@ -41,6 +41,8 @@
 // schedule order (cooperative launch: all CTAs are resident).
 #include <cuda_bf16.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 
 #include "mok_internal.h"
@@ -128,6 +130,12 @@ __device__ __forceinline__ PTile decode_phase_tile(int t, const int *s_pad, int 
     return r;
 }
 
+// index of the MX scale tile of (k element x, row y) in a [rows, K] matrix
+__device__ __forceinline__ int sf_tile(int x, int y, int64_t rows)
+{
+    return static_cast<int>((x >> 7) * (rows >> 7) + (y >> 7));
+}
+
 // expert whose padded segment holds row q (last e with pad[e] <= q)
 __device__ __forceinline__ int expert_of_row(const int *s_pad, int E, int64_t q)
 {
@@ -138,6 +146,108 @@ __device__ __forceinline__ int expert_of_row(const int *s_pad, int E, int64_t q)
         else hi = mid;
     }
     return lo;
+}
+
+// Gather role of the fused forward: pull expert-ordered rows into the token
+// ring (quantised when MXFP8) in minibatches claimed from a global counter,
+// after the ring rows' previous occupants were loaded by every FFN1 tile, and
+// publish each 64-row half of a row tile in ready[].  Every thread of the CTA
+// calls it.
+template <bool MX>
+__device__ __forceinline__ void gather_rows(const FusedArgs &a, const int *s_pad, int64_t pad_end, int *s_unit,
+                                            volatile int *abort_flag, int *next_unit, int *ready,
+                                            int *consumed, int warp, int lane, int nwarps)
+{
+    const int units = static_cast<int>((pad_end + a.mb - 1) / a.mb);
+    const int ring_tiles = static_cast<int>(a.ring_rows / kBM);
+    for (;;) {
+        if (threadIdx.x == 0) *s_unit = atomicAdd(next_unit, 1);
+        __syncthreads();
+        const int u = *s_unit;
+        if (u >= units || *abort_flag) break;
+        const int64_t r0 = static_cast<int64_t>(u) * a.mb;
+        const int64_t r1 = r0 + a.mb < pad_end ? r0 + a.mb : pad_end;
+        if (threadIdx.x == 0) {
+            // the ring rows' previous occupants must have been loaded by every FFN1 tile
+            for (int64_t q = r0; q < r1; q += kBM) {
+                const int m_prev = static_cast<int>(q / kBM) - ring_tiles;
+                if (m_prev >= 0 && !spin_ge(&consumed[m_prev], a.NT1, a, abort_flag)) break;
+            }
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+        for (int64_t q = r0 + warp; q < r1; q += nwarps) {
+            const int e = expert_of_row(s_pad, a.E, q);
+            const int64_t local = q - s_pad[e];
+            if (local >= a.counts[e]) continue;  // padding row: nothing to pull
+            const int t = a.row_tok[a.offsets[e] + local];
+            const uint4 *in = reinterpret_cast<const uint4 *>(source_row(a.src, t, a.d));
+            const int64_t rr = q % a.ring_rows;
+            if (!MX) {
+                uint4 *o = reinterpret_cast<uint4 *>(a.ring + rr * a.d * 2);
+#pragma unroll 8
+                for (int c = lane; c < a.d / 8; c += 32) o[c] = __ldg(in + c);
+            } else {
+                uint8_t *codes_row = a.ring + rr * a.d;
+                for (int c0 = 0; c0 < a.d; c0 += 2048) {
+                    uint4 raw[8];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const int cu = c0 + 256 * w;
+                        const int nvalid = cu >= a.d ? 0 : (a.d - cu >= 256 ? 32 : 16);
+                        raw[w] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const int cu = c0 + 256 * w;
+                        if (cu < a.d)
+                            mx_quant_stretch(raw[w], lane, a.d - cu >= 256 ? 32 : 16, codes_row, cu,
+                                             a.ring_scales, rr, a.ring_rows);
+                    }
+                }
+            }
+        }
+        fence_proxy_async_global();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            for (int64_t q = r0; q < r1; q += 64)  // hand over in 64-row halves of row tiles
+                red_release_gpu_add(&ready[q / kBM], 1);
+        }
+    }
+    __syncthreads();
+}
+
+// Weighted combine of the fused forward: once every FFN2 tile has pushed its
+// rows (ffn2_done), each CTA combines a share of the tokens in the fixed j
+// order.  Every thread of the CTA calls it.
+__device__ __forceinline__ void combine_tokens(const FusedArgs &a, int *ffn2_done, int total_mt,
+                                               volatile int *abort_flag)
+{
+    if (threadIdx.x == 0 && !*abort_flag) spin_ge(ffn2_done, 4 * total_mt * a.NT2, a, abort_flag);
+    __syncthreads();
+    if (*abort_flag) return;
+    const int vec = a.d / 8;
+    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+        for (int c = threadIdx.x; c < vec; c += blockDim.x) {
+            float acc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (int j = 0; j < a.k; ++j) {
+                const float g = a.gates[t * a.k + j];
+                const uint4 y = *(reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c);
+                const uint32_t w[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] = fmaf(g, bf16_bits_to_float(w[i] & 0xFFFFu), acc[2 * i]);
+                    acc[2 * i + 1] = fmaf(g, bf16_bits_to_float(w[i] >> 16), acc[2 * i + 1]);
+                }
+            }
+            reinterpret_cast<uint4 *>(a.out + t * a.d)[c] =
+                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        }
+    }
 }
 
 template <bool MX>
@@ -212,66 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kE = MX ? 128 : 64;
 
     // ---------------------------------------------------------- gather role
-    if (static_cast<int>(blockIdx.x) < a.n_gather) {
-        const int units = static_cast<int>((pad_end + a.mb - 1) / a.mb);
-        const int ring_tiles = static_cast<int>(a.ring_rows / kBM);
-        for (;;) {
-            if (threadIdx.x == 0) *s_unit = atomicAdd(next_unit, 1);
-            __syncthreads();
-            const int u = *s_unit;
-            if (u >= units || *abort_flag) break;
-            const int64_t r0 = static_cast<int64_t>(u) * a.mb;
-            const int64_t r1 = r0 + a.mb < pad_end ? r0 + a.mb : pad_end;
-            if (threadIdx.x == 0) {
-                // the ring rows' previous occupants must have been loaded by every FFN1 tile
-                for (int64_t q = r0; q < r1; q += kBM) {
-                    const int m_prev = static_cast<int>(q / kBM) - ring_tiles;
-                    if (m_prev >= 0 && !spin_ge(&consumed[m_prev], a.NT1, a, abort_flag)) break;
-                }
-            }
-            __syncthreads();
-            if (*abort_flag) break;
-            for (int64_t q = r0 + warp; q < r1; q += kThreads / 32) {
-                const int e = expert_of_row(s_pad, a.E, q);
-                const int64_t local = q - s_pad[e];
-                if (local >= a.counts[e]) continue;  // padding row: nothing to pull
-                const int t = a.row_tok[a.offsets[e] + local];
-                const uint4 *in = reinterpret_cast<const uint4 *>(source_row(a.src, t, a.d));
-                const int64_t rr = q % a.ring_rows;
-                if (!MX) {
-                    uint4 *o = reinterpret_cast<uint4 *>(a.ring + rr * a.d * 2);
-#pragma unroll 8
-                    for (int c = lane; c < a.d / 8; c += 32) o[c] = __ldg(in + c);
-                } else {
-                    uint8_t *codes_row = a.ring + rr * a.d;
-                    for (int c0 = 0; c0 < a.d; c0 += 2048) {
-                        uint4 raw[8];
-#pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            const int cu = c0 + 256 * w;
-                            const int nvalid = cu >= a.d ? 0 : (a.d - cu >= 256 ? 32 : 16);
-                            raw[w] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
-                        }
-#pragma unroll
-                        for (int w = 0; w < 8; ++w) {
-                            const int cu = c0 + 256 * w;
-                            if (cu < a.d)
-                                mx_quant_stretch(raw[w], lane, a.d - cu >= 256 ? 32 : 16, codes_row, cu,
-                                                 a.ring_scales, rr, a.ring_rows);
-                        }
-                    }
-                }
-            }
-            fence_proxy_async_global();
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                __threadfence();
-                for (int64_t q = r0; q < r1; q += 64)  // hand over in 64-row halves of row tiles
-                    red_release_gpu_add(&ready[q / kBM], 1);
-            }
-        }
-        __syncthreads();
-    }
+    if (static_cast<int>(blockIdx.x) < a.n_gather)
+        gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
+                        kThreads / 32);
 
     // ------------------------------------------------------------ GEMM role
     if (warp == 0) {
@@ -471,30 +524,430 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ----------------------------------------------------- weighted combine
-    if (threadIdx.x == 0 && !*abort_flag) spin_ge(ffn2_done, 4 * total_mt * a.NT2, a, abort_flag);
+    combine_tokens(a, ffn2_done, total_mt, abort_flag);
+}
+
+// ---------------------------------------------------------------------------
+// The same forward with the GEMM role on CTA pairs (cta_group::2): clusters of
+// two CTAs compute 256-row x 256-column tiles -- two consecutive 128-row tiles
+// of one expert, each CTA loading its own rows and one half of B (FFN1: the
+// even CTA the W_g rows, the odd CTA the W_u rows; FFN2: 128 rows of W_d
+// each), with every load counted on the even CTA's barrier.  Per flop each SM
+// loads a third fewer bytes than with one CTA per tile.  The even CTA's
+// scheduler thread claims pair tiles from the global counter and hands their
+// ids to both CTAs through a cluster-wide queue; the even CTA issues the MMAs
+// and scale copies; both CTAs run the epilogue of their own rows.  When an
+// expert has an odd number of row tiles its last pair tile has a ghost odd
+// half: the odd CTA loads the even half's rows again (already waited for and
+// resident, so the loads hit L2), stores nothing and signals no counter.  Gather CTAs come in pairs and a pair
+// enters the GEMM role only once both of its CTAs have finished gathering, so
+// a pair never holds a tile while one of its CTAs waits in the gather role.
+// Tiles keep the single-CTA kernel's per-row arithmetic, so results are
+// bit-identical to it.
+// ---------------------------------------------------------------------------
+constexpr int kFPStages = 6;
+constexpr int kFPStage = kAStage + 128 * kBKBytes;  // 32 KB: A rows + one half of B
+
+struct FusedPairMaps {
+    CUtensorMap ring, g, u, h, dn;   // operands (as k_moe_fused)
+    CUtensorMap s_ring, s_g, s_u, s_h, s_dn;  // MX scale tiles (MXFP8 only)
+};
+
+// Pair tile t of one phase (NT N tiles per pair row): expert e, pair row j of
+// that expert (row tiles 2j and 2j + 1 of its segment), N tile n; the same
+// expert / band / N-tile / row order as decode_phase_tile, in pair rows.
+struct PPTile {
+    int e, j, n;
+};
+__device__ __forceinline__ PPTile decode_pair_tile(int t, const int *s_pp, int E, int NT, int band)
+{
+    int lo = 0, hi = E;  // last expert whose first tile index <= t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pp[mid] * NT <= t) lo = mid;
+        else hi = mid;
+    }
+    const int pr = s_pp[lo + 1] - s_pp[lo];
+    const int b = band < pr ? band : pr;
+    const int local = t - s_pp[lo] * NT;
+    const int jb = local / (b * NT);
+    const int bm = pr - jb * b < b ? pr - jb * b : b;
+    const int ll = local - jb * b * NT;
+    PPTile r;
+    r.e = lo;
+    r.n = ll / bm;
+    r.j = jb * b + ll % bm;
+    return r;
+}
+
+template <bool MX>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_moe_fused_pair(const __grid_constant__ FusedPairMaps pm, const __grid_constant__ FusedArgs a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sT = smem;
+    uint8_t *sSF = sT + kFPStages * kFPStage;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kFPStages * (kSfaBytes + kSfbBytes) : 0));
+    uint64_t *full = bars;
+    uint64_t *empty = bars + kFPStages;
+    uint64_t *acc_full = bars + 2 * kFPStages;
+    uint64_t *acc_empty = acc_full + 1;
+    uint64_t *tq_full = acc_empty + 1;
+    uint64_t *tq_empty = tq_full + kTQ;
+    int *tq = reinterpret_cast<int *>(tq_empty + kTQ);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(tq + kTQ);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    int *s_unit = reinterpret_cast<int *>(tmem_holder + 2);
+    int *s_pad = reinterpret_cast<int *>(tmem_holder + 4);   // [E + 1]
+    int *s_pp = s_pad + MOK_MAX_EXPERTS + 4;                 // [E + 1] pair-row prefix
+    uint32_t *stage_out = reinterpret_cast<uint32_t *>(s_pp + MOK_MAX_EXPERTS + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    int *next_tile = a.counters;
+    int *next_unit = a.counters + 1;
+    int *ffn2_done = a.counters + 2;
+    int *ready = a.counters + 3;
+    int *consumed = ready + a.max_mt;
+    int *h_done = consumed + a.max_mt;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kFPStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);  // four epilogue warps of each CTA
+        for (int i = 0; i < kTQ; ++i) {
+            mbar_init(&tq_full[i], 1);
+            mbar_init(&tq_empty[i], 10);  // even: MMA + 4 epilogue warps; odd: producer + 4 epilogue warps
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&pm.ring);
+        prefetch_tmap(&pm.g);
+        prefetch_tmap(&pm.u);
+        prefetch_tmap(&pm.h);
+        prefetch_tmap(&pm.dn);
+    }
+    for (int e = threadIdx.x; e <= a.E; e += blockDim.x) s_pad[e] = a.pad_offsets[e];
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive, store or load
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int e = 0; e < a.E; ++e) {
+            s_pp[e] = run;
+            run += ((s_pad[e + 1] - s_pad[e]) / kBM + 1) / 2;
+        }
+        s_pp[a.E] = run;
+    }
+    tc_fence_before();
     __syncthreads();
-    if (*abort_flag) return;
-    const int vec = a.d / 8;
-    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-        for (int c = threadIdx.x; c < vec; c += blockDim.x) {
-            float acc[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            for (int j = 0; j < a.k; ++j) {
-                const float g = a.gates[t * a.k + j];
-                const uint4 y = *(reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c);
-                const uint32_t w[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = fmaf(g, bf16_bits_to_float(w[i] & 0xFFFFu), acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(g, bf16_bits_to_float(w[i] >> 16), acc[2 * i + 1]);
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const int64_t pad_end = s_pad[a.E];
+    const int total_mt = static_cast<int>(pad_end / kBM);
+    const int total_pr = s_pp[a.E];
+    const int T1 = total_pr * a.NT1;
+    const int total_tiles = T1 + total_pr * a.NT2;
+    constexpr int kE = MX ? 128 : 64;
+    const int bandp = a.band1 >= (1 << 29) ? (1 << 30) : (a.band1 / 2 > 0 ? a.band1 / 2 : 1);
+
+    // ---------------------------------------------------------- gather role
+    if (static_cast<int>(blockIdx.x) < a.n_gather) {
+        gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
+                        kThreads / 32);
+        cluster_sync_all();  // the pair joins the GEMM role together
+    }
+
+    // what a pair tile means for this CTA: its row tile m (ghost: none), N tile
+    struct Job {
+        bool f1, ghost, ghost_odd;
+        int e, m0, n;
+    };
+    auto job_of = [&](int tile) {
+        Job jb;
+        jb.f1 = tile < T1;
+        const PPTile pt = jb.f1 ? decode_pair_tile(tile, s_pp, a.E, a.NT1, bandp)
+                                : decode_pair_tile(tile - T1, s_pp, a.E, a.NT2, 1 << 30);
+        jb.e = pt.e;
+        jb.n = pt.n;
+        jb.m0 = s_pad[pt.e] / kBM + 2 * pt.j;
+        jb.ghost_odd = jb.m0 + 1 >= s_pad[pt.e + 1] / kBM;
+        jb.ghost = rank == 1 && jb.ghost_odd;
+        return jb;
+    };
+    const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+
+    // ------------------------------------------------------------ GEMM role
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
+            const uint32_t tq_full_odd = mapa_shared(smem_u32(tq_full), 1);
+            const uint32_t tq_odd = mapa_shared(smem_u32(tq), 1);
+            const uint32_t tq_empty_even = mapa_shared(smem_u32(tq_empty), 0);
+            const uint32_t cta_bytes = kFPStage + (MX ? kSfaBytes + kSfbBytes : 0);
+            for (;;) {
+                int tile;
+                if (rank == 0) {
+                    // scheduler: claim the next pair tile and hand it to both CTAs
+                    tile = *abort_flag ? -1 : atomicAdd(next_tile, 1);
+                    if (tile >= total_tiles) tile = -1;
+                    if (!wait_bar(&tq_empty[qs], qphase ^ 1u, a.status, a.wait_ns, abort_flag)) tile = -1;
+                    tq[qs] = tile;
+                    st_shared_cluster(tq_odd + qs * 4, static_cast<uint32_t>(tile));
+                    mbar_arrive(&tq_full[qs]);
+                    mbar_arrive_remote(tq_full_odd + qs * 8);
+                } else {
+                    if (!wait_bar_cluster(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
+                    tile = tq[qs];
+                    mbar_arrive_remote(tq_empty_even + qs * 8);
+                }
+                if (++qs == kTQ) {
+                    qs = 0;
+                    qphase ^= 1u;
+                }
+                if (tile < 0) break;
+                const Job jb = job_of(tile);
+                const int m = jb.m0 + static_cast<int>(rank);
+                if (jb.e < 0 || jb.e >= a.E || m >= total_mt + 1 || jb.n < 0 || jb.n >= (jb.f1 ? a.NT1 : a.NT2)) {
+                    report_timeout(a.status, abort_flag);  // a schedule bug: stop, touch nothing
+                    break;
+                }
+                // a ghost half loads the even half's rows (resident, results discarded)
+                const int ma = jb.ghost ? jb.m0 : m;
+                if (jb.f1 ? !spin_ge(&ready[ma], 2, a, abort_flag) : !spin_ge(&h_done[ma], 4 * a.NT1, a, abort_flag))
+                    break;
+                fence_proxy_async_global();
+                const int kst = jb.f1 ? a.k1 : a.k2;
+                const int ya = jb.f1 ? static_cast<int>((static_cast<int64_t>(ma) * kBM) % a.ring_rows) : ma * kBM;
+                // B rows of this CTA's half, and the first B row of the tile (scales)
+                const int yb_tile = jb.f1 ? jb.e * a.F + jb.n * 128 : jb.e * a.d + jb.n * 256;
+                const int yb = jb.f1 ? yb_tile : yb_tile + static_cast<int>(rank) * 128;
+                const CUtensorMap *amap = jb.f1 ? &pm.ring : &pm.h;
+                const CUtensorMap *bmap = jb.f1 ? (rank ? &pm.u : &pm.g) : &pm.dn;
+                const CUtensorMap *samap = jb.f1 ? &pm.s_ring : &pm.s_h;
+                const int64_t arows = jb.f1 ? a.ring_rows : a.h_rows;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!wait_bar(&empty[stage], phase ^ 1u, a.status, a.wait_ns, abort_flag)) goto producer_done;
+                    uint8_t *dA = sT + stage * kFPStage;
+                    const int x = ks * kE;
+                    const uint32_t fb = full0 + stage * 8;
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * cta_bytes);
+                    tma_load_2d_pair(dA, amap, fb, x, ya);
+                    tma_load_2d_pair(dA + kAStage, bmap, fb, x, yb);
+                    if constexpr (MX) {
+                        uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
+                        tma_load_2d_pair(dS, samap, fb, 0, sf_tile(x, ya, arows));
+                        if (jb.f1) {
+                            tma_load_2d_pair(dS + kSfaBytes, &pm.s_g, fb, 0, sf_tile(x, yb_tile, a.EF));
+                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_u, fb, 0, sf_tile(x, yb_tile, a.EF));
+                        } else {
+                            tma_load_2d_pair(dS + kSfaBytes, &pm.s_dn, fb, 0, sf_tile(x, yb_tile, a.Ed));
+                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_dn, fb, 0, sf_tile(x, yb_tile + 128, a.Ed));
+                        }
+                    }
+                    if (++stage == kFPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
-            reinterpret_cast<uint4 *>(a.out + t * a.d)[c] =
-                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        producer_done:;
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ---------------------------------------- even CTA: MMA issue for the pair
+            uint32_t stage = 0, phase = 0, acc_phase = 0, qs = 0, qphase = 0;
+            for (;;) {
+                if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
+                const int tile = tq[qs];
+                mbar_arrive(&tq_empty[qs]);
+                if (++qs == kTQ) {
+                    qs = 0;
+                    qphase ^= 1u;
+                }
+                if (tile < 0) break;
+                const Job jb = job_of(tile);
+                const int kst = jb.f1 ? a.k1 : a.k2;
+                const uint32_t idesc = idesc_bf16(2 * kBM, 256);
+                if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
+                tc_fence_after();
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    tc_fence_after();
+                    if (jb.f1 && ks == kst - 1) {
+                        // every ring row of the pair's row tiles is now in shared memory
+                        __threadfence();
+                        red_release_gpu_add(&consumed[jb.m0], 1);
+                        if (!jb.ghost_odd) red_release_gpu_add(&consumed[jb.m0 + 1], 1);
+                    }
+                    const uint32_t aaddr = smem_u32(sT + stage * kFPStage);
+                    const uint32_t baddr = aaddr + kAStage;
+                    const uint32_t sfa_col = tmem + kSfCol + stage * 16;
+                    const uint32_t sfb_col = sfa_col + 4;
+                    if (MX) {
+                        const uint32_t sbase = smem_u32(sSF + stage * (kSfaBytes + kSfbBytes));
+                        tmem_cp_32x128b_warpx4_pair(sfa_col, sdesc_sf(sbase));
+                        tmem_cp_32x128b_warpx4_pair(sfb_col, sdesc_sf(sbase + kSfaBytes));
+                        tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sdesc_sf(sbase + kSfaBytes + 512));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sdesc_k_sw128(aaddr + kk * 32);
+                        const uint64_t bd = sdesc_k_sw128(baddr + kk * 32);
+                        const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
+                        if (MX) mma_mxf8_pair(tmem, ad, bd, idesc_mxf8(2 * kBM, 256, kk, kk), sfa_col, sfb_col, accum);
+                        else mma_bf16_pair(tmem, ad, bd, idesc, accum);
+                    }
+                    tc_commit_pair(&empty[stage], 0x3);
+                    if (++stage == kFPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                tc_commit_pair(acc_full, 0x3);
+                acc_phase ^= 1u;
+            }
+        mma_done:;
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        const uint32_t acc_empty_even = mapa_shared(smem_u32(acc_empty), 0);
+        const uint32_t tq_empty_even = mapa_shared(smem_u32(tq_empty), 0);
+        uint32_t acc_phase = 0, qs = 0, qphase = 0;
+        for (;;) {
+            if (!wait_bar_cluster(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
+            const int tile = tq[qs];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(tq_empty_even + qs * 8);
+            if (++qs == kTQ) {
+                qs = 0;
+                qphase ^= 1u;
+            }
+            if (tile < 0) break;
+            const Job jb = job_of(tile);
+            const int m = jb.m0 + static_cast<int>(rank);
+            const int64_t q = static_cast<int64_t>(m) * kBM + r;  // padded row of this thread
+            const int64_t row_in_e = q - s_pad[jb.e];
+            const bool valid = !jb.ghost && row_in_e < a.counts[jb.e];
+            if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
+            tc_fence_after();
+            bool released = false;
+            auto release = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(acc_empty_even);
+                released = true;
+            };
+            if (jb.f1) {
+                epi_ffn1<MX>(trow, valid, q, jb.n * 128, a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b,
+                             a.saved_h, stage_out + (warp - 2) * kStageWords, lane, release);
+            } else {
+                uint16_t *dst = nullptr;
+                if (valid) {
+                    const int64_t p = a.offsets[jb.e] + row_in_e;
+                    dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k + a.row_j[p]) * a.d + jb.n * 256;
+                }
+                epi_rows_bf16(trow, 256, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane, release);
+            }
+            if (!released) release();
+            acc_phase ^= 1u;
+            // publish this warp's quarter of the row tile (a ghost half has none)
+            if (!jb.ghost) {
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    red_release_gpu_add(jb.f1 ? &h_done[m] : ffn2_done, 1);
+                }
+            }
         }
     }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // no more remote arrives, stores, loads or multicast commits into either CTA
+    if (*abort_flag) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 1000000ull) __nanosleep(1000);
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+
+    // ----------------------------------------------------- weighted combine
+    combine_tokens(a, ffn2_done, total_mt, abort_flag);
+}
+
+template <bool MX>
+constexpr size_t fused_pair_smem_bytes()
+{
+    return 1024 + kFPStages * kFPStage + (MX ? kFPStages * (kSfaBytes + kSfbBytes) : 0) +
+           (2 * kFPStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + 2 * (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+}
+
+// Launch configuration of the pair kernel: its attributes are set once and its
+// grid is the number of CTA pairs that can be resident at once (the roles
+// wait on one another, so every CTA must be resident), at most one per SM.
+template <bool MX>
+cudaError_t fused_pair_setup(int *grid_out)
+{
+    constexpr size_t smem = fused_pair_smem_bytes<MX>();
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int grid = 0;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(k_moe_fused_pair<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(num_sms() / 2 * 2));
+        int clusters = 0;
+        if (attr_err == cudaSuccess) attr_err = cudaOccupancyMaxActiveClusters(&clusters, k_moe_fused_pair<MX>, &cfg);
+        grid = clusters * 2 <= num_sms() ? clusters * 2 : num_sms() / 2 * 2;
+        if (attr_err == cudaSuccess && grid < 4) attr_err = cudaErrorInvalidConfiguration;
+    });
+    *grid_out = grid;
+    return attr_err;
+}
+
+template <bool MX>
+cudaError_t launch_fused_pair_t(const FusedPairMaps &pm, const FusedArgs &args, int grid, cudaStream_t st)
+{
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = fused_pair_smem_bytes<MX>();
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_moe_fused_pair<MX>, pm, args);
 }
 
 template <bool MX>
@@ -534,7 +987,103 @@ cudaError_t launch_fused_t(const CUtensorMap &ring, const CUtensorMap &g, const 
     return cudaLaunchKernelEx(&cfg, k_moe_fused<MX>, ring, g, u, h, dn, args);
 }
 
+int gather_ctas(int sms, float frac)
+{
+    const int ng = static_cast<int>(frac * static_cast<float>(sms) + 0.5f);
+    return ng < 1 ? 1 : (ng > sms - 1 ? sms - 1 : ng);
+}
+
 }  // namespace
+
+// Shape-driven defaults of the fused forward's two knobs.  [kucoin] §03: when
+// the hidden size, top-k or expert size changes, the right minibatch and the
+// number of SMs on the communication side change with them; §02: one
+// minibatch should give the expert GEMM at least two full waves of tiles.
+//
+// Gather CTAs: the GEMM role must never wait for rows in FFN1.  Per padded row
+// the gather moves 2d bytes in and d (1 + 1/32) (MXFP8) or 2d (BF16) bytes
+// out, at about kGatherBytesPerSm per second on one gathering SM (the pull
+// dispatch measured on its own on GB300, all SMs pulling); FFN1 spends 4dF
+// flops on the row at about kGemmFlopsPerSm per second on one GEMM SM (the
+// fused forward measured on GB300).  n_gather / n_gemm must exceed the ratio
+// of the two per-row times; the default takes twice that ratio, clamped to
+// [1/16, 1/3] of the SMs (the gather CTAs join the GEMM role once the gather
+// is done, so a generous share costs little).
+int auto_gather_ctas(const Dims &dm, int sms)
+{
+    constexpr double kGatherBytesPerSm = 21e9;
+    const double gemm_flops_per_sm = dm.dtype == MOK_MXFP8 ? 9.4e12 : 8.6e12;
+    const double row_bytes = 2.0 * dm.d + (dm.dtype == MOK_MXFP8 ? dm.d * (1.0 + 1.0 / 32) : 2.0 * dm.d);
+    const double t_gather = row_bytes / kGatherBytesPerSm;
+    const double t_gemm = 4.0 * dm.d * static_cast<double>(dm.F) / gemm_flops_per_sm;
+    const double q = 2.0 * t_gather / t_gemm;  // n_gather / n_gemm
+    double frac = q / (1.0 + q);
+    frac = frac < 1.0 / 16 ? 1.0 / 16 : (frac > 1.0 / 3 ? 1.0 / 3 : frac);
+    return gather_ctas(sms, static_cast<float>(frac));
+}
+
+// Minibatch: [kucoin] wants one minibatch to give the expert GEMM two full
+// waves of tiles.  Here every 128-row tile is released as soon as its rows
+// have landed, and the gather CTAs each work on their own minibatch, so one
+// round of the gather role hands over n_gather minibatches, worth
+// n_gather * (mb / 128) * (F / 128) FFN1 tiles; the default is the smallest
+// hand-off (64, 128 or 256 rows) for which a round covers two waves of the
+// GEMM CTAs, else 256.  Smaller hand-offs let the first tiles start sooner.
+int auto_minibatch_rows(const Dims &dm, int gather_ctas, int gemm_ctas)
+{
+    const int64_t tiles_per_row_tile = dm.F / 128;
+    for (int mb = 64; mb < 256; mb *= 2)
+        if (static_cast<int64_t>(gather_ctas) * mb * tiles_per_row_tile >= 2LL * 128 * gemm_ctas) return mb;
+    return 256;
+}
+
+// CTA pairs need d a multiple of 256 (FFN2 pair tiles are 256 columns of d)
+// and, when the token ring is capped, a ring of at least four row tiles.  A
+// pair tile needs two row tiles that can straddle two gather units, and a
+// gather unit may only overwrite ring rows once every FFN1 tile of their band
+// has loaded them; with bands of B pair rows the wait is acyclic when
+// 2B <= R - U + 1 (R ring row tiles, U <= 2 row tiles per unit), which
+// B = R / 4 >= 1 satisfies for R >= 4.  Smaller rings run one CTA per tile.
+// Default: pairs for BF16 layers, one CTA per tile for MXFP8 layers -- on
+// GB300 the fused kernel's tensor pipe runs at the same rate either way, so
+// the ghost halves of experts with an odd number of row tiles (about half of
+// them at 512 rows per expert) make MXFP8 pairs slower (9.1 vs 8.1 ms on the
+// DeepSeek-V3 shape) while BF16 pairs gain (4.27 vs 4.33 ms on the Mixtral
+// shape).  MOK_FUSED_PAIR=1 / 0 in the environment forces either.
+bool fused_uses_pairs(const Dims &dm, const mok_config *cfg)
+{
+    if (dm.d % 256 != 0) return false;
+    const char *v = getenv("MOK_FUSED_PAIR");
+    if (v && v[0] == '0') return false;
+    if (!(v && v[0] == '1') && dm.dtype == MOK_MXFP8) return false;
+    const int64_t ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
+    return ring_rows >= dm.rows_pad || ring_rows / 128 >= 4;
+}
+
+int fused_ctas(const Dims &dm, const mok_config *cfg, int sms)
+{
+    if (!fused_uses_pairs(dm, cfg)) return sms;
+    int dev_count = 0, grid = 0;
+    if (cudaGetDeviceCount(&dev_count) == cudaSuccess && dev_count > 0 &&
+        (dm.dtype == MOK_MXFP8 ? fused_pair_setup<true>(&grid) : fused_pair_setup<false>(&grid)) == cudaSuccess)
+        return grid;
+    cudaGetLastError();  // no device here: clear the error, plan for every SM paired
+    return sms / 2 * 2;
+}
+
+// ctas: the CTAs of the launch (for the pair kernel, its grid)
+void fused_knobs(const Dims &dm, const mok_config *cfg, int ctas, int *gather, int *mb)
+{
+    *gather = cfg->gather_sm_fraction > 0.0f ? gather_ctas(ctas, cfg->gather_sm_fraction)
+                                             : auto_gather_ctas(dm, ctas);
+    if (fused_uses_pairs(dm, cfg)) {
+        // gather CTAs come in pairs; at least one pair stays in the GEMM role
+        *gather = (*gather + 1) / 2 * 2;
+        if (*gather > ctas - 2) *gather = ctas - 2;
+        if (*gather < 2) *gather = 2;
+    }
+    *mb = cfg->minibatch_rows ? cfg->minibatch_rows : auto_minibatch_rows(dm, *gather, ctas - *gather);
+}
 
 int64_t fused_ring_rows(const Dims &dm, size_t ring_bytes)
 {
@@ -592,11 +1141,13 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     a.saved_a = io.saved_a;
     a.saved_b = io.saved_b;
     a.saved_h = io.saved_h;
-    a.mb = cfg->minibatch_rows ? cfg->minibatch_rows : 128;
-    const int sms = num_sms();
-    const float frac = cfg->gather_sm_fraction > 0.0f ? cfg->gather_sm_fraction : 0.25f;
-    int ng = static_cast<int>(frac * static_cast<float>(sms) + 0.5f);
-    a.n_gather = ng < 1 ? 1 : (ng > sms - 1 ? sms - 1 : ng);
+    const bool pair = fused_uses_pairs(dm, cfg);
+    int grid = num_sms();
+    if (pair) {
+        const cudaError_t ge = mx ? fused_pair_setup<true>(&grid) : fused_pair_setup<false>(&grid);
+        if (ge != cudaSuccess) return ge;
+    }
+    fused_knobs(dm, cfg, grid, &a.n_gather, &a.mb);
     a.NT1 = dm.F / 128;
     a.BN2 = dm.d % 256 == 0 ? 256 : 128;
     a.NT2 = dm.d / a.BN2;
@@ -604,13 +1155,30 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     a.k2 = dm.F / static_cast<int>(box);
     // an uncapped ring never wraps: one band per expert (the separate-kernel
     // order); a capped ring holds two bands, so a band is always free to fill
-    a.band1 = ring_rows >= dm.rows_pad ? (1 << 30) : static_cast<int>(ring_rows / 128 / 2);
+    // (CTA pairs: bands of ring/4 pair rows, see fused_uses_pairs)
+    a.band1 = ring_rows >= dm.rows_pad ? (1 << 30)
+                                       : static_cast<int>(pair ? ring_rows / 128 / 4 * 2 : ring_rows / 128 / 2);
     a.counters = io.counters;
     a.max_mt = static_cast<int>(dm.rows_pad / 128);
     a.status = status;
     a.wait_ns = wait_ns;
+    FusedPairMaps pm = {};
+    if (pair) {
+        pm.ring = tr;
+        pm.g = tg;
+        pm.u = tu;
+        pm.h = th;
+        pm.dn = td;
+        if (mx && (encode_tmap_scales(&pm.s_ring, io.ring_scales, static_cast<uint64_t>(ring_rows), dm.d) ||
+                   encode_tmap_scales(&pm.s_g, w->s_gate, EF, dm.d) ||
+                   encode_tmap_scales(&pm.s_u, w->s_up, EF, dm.d) ||
+                   encode_tmap_scales(&pm.s_h, io.h_scales, dm.rows_pad, dm.F) ||
+                   encode_tmap_scales(&pm.s_dn, w->s_down, Ed, dm.F)))
+            return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaMemsetAsync(io.counters, 0, sizeof(int) * fused_counter_ints(dm), st);
     if (e != cudaSuccess) return e;
+    if (pair) return mx ? launch_fused_pair_t<true>(pm, a, grid, st) : launch_fused_pair_t<false>(pm, a, grid, st);
     return mx ? launch_fused_t<true>(tr, tg, tu, th, td, a, st)
               : launch_fused_t<false>(tr, tg, tu, th, td, a, st);
 }

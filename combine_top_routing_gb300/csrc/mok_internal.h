@@ -94,6 +94,10 @@ cudaError_t launch_dispatch(const Dims &dm, const Sources &src, const int32_t *i
                             const int32_t *offsets, const int32_t *pad_offsets,
                             const int32_t *row_tok, const uint8_t *row_j, void *xe,
                             uint32_t *xe_scales, cudaStream_t st);
+cudaError_t launch_dispatch_by_token(const Dims &dm, const Sources &src, const int32_t *ids,
+                                     const int32_t *slot_pos, const int32_t *offsets,
+                                     const int32_t *pad_offsets, void *xe, uint32_t *xe_scales,
+                                     cudaStream_t st);
 cudaError_t launch_combine(const Dims &dm, const uint16_t *ystage, const float *gates,
                            uint16_t *out, cudaStream_t st);
 cudaError_t launch_quant_mx(const uint16_t *src, int64_t batch, int64_t rows, int64_t K,
@@ -157,6 +161,16 @@ struct FusedIo {
     int *counters;            // fused_counter_ints(dm) ints
 };
 int64_t fused_ring_rows(const Dims &dm, size_t ring_bytes);
+// Defaults of the fused forward's knobs when the config leaves them 0.
+int auto_gather_ctas(const Dims &dm, int sms);
+int auto_minibatch_rows(const Dims &dm, int gather_ctas, int gemm_ctas);
+// Whether the fused forward runs its GEMM role on CTA pairs (d a multiple of
+// 256 and an uncapped ring or one of at least 4 row tiles; the environment
+// variable MOK_FUSED_PAIR=0 turns it off), and its CTAs.
+bool fused_uses_pairs(const Dims &dm, const mok_config *cfg);
+int fused_ctas(const Dims &dm, const mok_config *cfg, int sms);
+// The knobs one fused launch of `ctas` CTAs uses: gather CTAs and minibatch rows.
+void fused_knobs(const Dims &dm, const mok_config *cfg, int ctas, int *gather_ctas, int *minibatch_rows);
 int fused_counter_ints(const Dims &dm);
 cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &src, const FusedIo &io,
                          const mok_weights *w, uint32_t *status, uint64_t wait_ns, cudaStream_t st);

@@ -86,6 +86,105 @@ cudaError_t launch_dispatch(const Dims &dm, const Sources &src, const int32_t *i
 }
 
 // ---------------------------------------------------------------------------
+// A3 with one read per token: warp w takes token t, reads its row from its
+// source once (and quantises it once, MXFP8) and writes it into each of the
+// token's k slot rows.  This is the receiver's pull with one request per token
+// instead of one per slot -- on several GPUs, one pull per (token, destination
+// rank) placed into every local expert the token selected.  The output bytes
+// are k_dispatch's; HBM reads drop from S rows to T rows.
+// ---------------------------------------------------------------------------
+template <bool MX>
+__global__ void __launch_bounds__(256) k_dispatch_by_token(const Sources src, int T, int d, int k,
+                                                           const int32_t *__restrict__ ids,
+                                                           const int32_t *__restrict__ slot_pos,
+                                                           const int32_t *__restrict__ offsets,
+                                                           const int32_t *__restrict__ pad_offsets,
+                                                           void *xe, uint32_t *__restrict__ xe_scales,
+                                                           int64_t rows_pad)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
+         t += warps) {
+        int64_t q[MOK_MAX_TOPK];
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j < k) {
+                const int e = ids[t * k + j];
+                q[j] = pad_offsets[e] + (slot_pos[t * k + j] - offsets[e]);
+            }
+        }
+        const uint4 *in = reinterpret_cast<const uint4 *>(source_row(src, static_cast<int>(t), d));
+        if (!MX) {
+            for (int c0 = 0; c0 < d / 8; c0 += 128) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = c0 + 32 * u + lane;
+                    v[u] = c < d / 8 ? __ldg(in + c) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+                    if (j < k) {
+                        uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xe) + q[j] * d);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int c = c0 + 32 * u + lane;
+                            if (c < d / 8) out[c] = v[u];
+                        }
+                    }
+                }
+            }
+        } else {
+            for (int c0 = 0; c0 < d; c0 += 1024) {
+                uint4 raw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int cu = c0 + 256 * u;
+                    const int nvalid = cu >= d ? 0 : (d - cu >= 256 ? 32 : 16);
+                    raw[u] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int cu = c0 + 256 * u;
+                    if (cu >= d) continue;
+                    const int nvalid = d - cu >= 256 ? 32 : 16;
+                    uint2 codes;
+                    uint32_t word;
+                    mx_quant8(raw[u], lane, codes, word);
+#pragma unroll
+                    for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+                        if (j < k) {
+                            uint8_t *row = static_cast<uint8_t *>(xe) + q[j] * d;
+                            if (lane < nvalid) *reinterpret_cast<uint2 *>(row + cu + 8 * lane) = codes;
+                            if ((lane & 15) == 0 && lane < nvalid)
+                                xe_scales[mx_word_index((cu + 8 * lane) >> 7, q[j], rows_pad)] = word;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_dispatch_by_token(const Dims &dm, const Sources &src, const int32_t *ids,
+                                     const int32_t *slot_pos, const int32_t *offsets,
+                                     const int32_t *pad_offsets, void *xe, uint32_t *xe_scales,
+                                     cudaStream_t st)
+{
+    const int threads = 256;
+    const int64_t need = (static_cast<int64_t>(dm.T) + 7) / 8;
+    const int blocks = static_cast<int>(need < 32 * num_sms() ? need : 32 * num_sms());
+    if (dm.dtype == MOK_MXFP8)
+        k_dispatch_by_token<true><<<blocks, threads, 0, st>>>(src, dm.T, dm.d, dm.k, ids, slot_pos, offsets,
+                                                              pad_offsets, xe, xe_scales, dm.rows_pad);
+    else
+        k_dispatch_by_token<false><<<blocks, threads, 0, st>>>(src, dm.T, dm.d, dm.k, ids, slot_pos, offsets,
+                                                               pad_offsets, xe, xe_scales, dm.rows_pad);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
 // A6 combine: out[t, c] = bf16( fold_j fmaf(g_tj, y_tj[c], acc) ), acc from 0,
 // j = 0..k-1 in order.  One thread per 8 columns of one token.
 // ---------------------------------------------------------------------------

@@ -125,6 +125,27 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank)
     return r;
 }
 
+// 32-bit store to shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ void st_shared_cluster(uint32_t cluster_addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// try_wait with cluster-scope acquire: sees what another CTA of the cluster
+// wrote before its release-arrive on this barrier.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Arrive on an mbarrier of another CTA of the cluster (release, cluster scope).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
@@ -436,15 +457,12 @@ __device__ __forceinline__ int64_t mx_word_index(int64_t g, int64_t r, int64_t r
     return (g * (rows >> 7) + (r >> 7)) * 128 + (r & 31) * 4 + ((r & 127) >> 5);
 }
 
-// One warp quantises one 256-element stretch of a row: lane l converts
-// elements [8l, 8l+8), lanes 4b..4b+3 share MX block b, the amax is reduced
-// over those four lanes, and lanes 0 and 16 write the scale words of the two
-// 128-wide k-groups.  A 128-element tail passes nvalid = 16: every lane takes
-// part in the shuffles, lanes 16..31 write nothing.
-__device__ __forceinline__ void mx_quant_stretch(const uint4 raw, int lane, int nvalid,
-                                                 uint8_t *codes_row, int64_t col0,
-                                                 uint32_t *scales, int64_t scale_row,
-                                                 int64_t scale_rows)
+// One warp quantises one 256-element stretch of a row, in registers: lane l
+// converts elements [8l, 8l+8) into `codes` (8 E4M3 bytes), lanes 4b..4b+3
+// share MX block b and reduce its amax over those four lanes; on return
+// every lane's `word` holds the four scale bytes of its 128-wide k-group
+// (lanes 0..15: the first, 16..31: the second).  All 32 lanes must call it.
+__device__ __forceinline__ void mx_quant8(const uint4 raw, int lane, uint2 &codes, uint32_t &word)
 {
     float f[8];
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -460,14 +478,27 @@ __device__ __forceinline__ void mx_quant_stretch(const uint4 raw, int lane, int 
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const int x = mx_scale_exp(amax);
     const float inv = mx_inv_scale(x);
-    uint2 out;
-    out.x = pack_e4m3x2(f[0] * inv, f[1] * inv) | (pack_e4m3x2(f[2] * inv, f[3] * inv) << 16);
-    out.y = pack_e4m3x2(f[4] * inv, f[5] * inv) | (pack_e4m3x2(f[6] * inv, f[7] * inv) << 16);
-    if (lane < nvalid) *reinterpret_cast<uint2 *>(codes_row + col0 + 8 * lane) = out;
+    codes.x = pack_e4m3x2(f[0] * inv, f[1] * inv) | (pack_e4m3x2(f[2] * inv, f[3] * inv) << 16);
+    codes.y = pack_e4m3x2(f[4] * inv, f[5] * inv) | (pack_e4m3x2(f[6] * inv, f[7] * inv) << 16);
     // scale byte of block (lane/4) sits at byte (lane/4) % 4 of its k-group word
-    uint32_t word = static_cast<uint32_t>(x + 127) << (8 * ((lane >> 2) & 3));
+    word = static_cast<uint32_t>(x + 127) << (8 * ((lane >> 2) & 3));
     word |= __shfl_xor_sync(0xffffffffu, word, 4);
     word |= __shfl_xor_sync(0xffffffffu, word, 8);
+}
+
+// mx_quant8 plus the stores: codes at codes_row[col0 + 8l ..], the scale words
+// of the stretch's two k-groups at row scale_row of the tile layout.  A
+// 128-element tail passes nvalid = 16: every lane takes part in the shuffles,
+// lanes 16..31 write nothing.
+__device__ __forceinline__ void mx_quant_stretch(const uint4 raw, int lane, int nvalid,
+                                                 uint8_t *codes_row, int64_t col0,
+                                                 uint32_t *scales, int64_t scale_row,
+                                                 int64_t scale_rows)
+{
+    uint2 out;
+    uint32_t word;
+    mx_quant8(raw, lane, out, word);
+    if (lane < nvalid) *reinterpret_cast<uint2 *>(codes_row + col0 + 8 * lane) = out;
     if ((lane & 15) == 0 && lane < nvalid) {
         const int64_t g = (col0 + 8 * lane) >> 7;
         scales[mx_word_index(g, scale_row, scale_rows)] = word;

@@ -44,6 +44,25 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint32_
     }
 }
 
+// wait_bar with cluster-scope acquire (barriers another CTA arrives on after
+// writing into this CTA's shared memory).
+__device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity, uint32_t *status,
+                                                 uint64_t wait_ns, volatile int *abort_flag)
+{
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > wait_ns) {
+                report_timeout(status, abort_flag);
+                return false;
+            }
+        }
+    }
+}
+
 __device__ __forceinline__ void store_bf16x32(uint16_t *dst, const float *v)
 {
     uint4 *o = reinterpret_cast<uint4 *>(dst);

@@ -28,7 +28,7 @@ EXPORTS = [
     "mok_dispatch", "mok_expert_ffn", "mok_combine", "mok_moe_fused", "mok_moe_forward",
     "mok_moe_backward",
     "mok_quantize_mx", "mok_transpose_bf16", "mok_reset_device_status", "mok_get_device_status",
-    "mok_status_string", "mok_layout_static",
+    "mok_status_string", "mok_layout_static", "mok_fused_plan", "mok_dispatch_by_token",
 ]
 
 
@@ -81,6 +81,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_saved_ctx_layout.argtypes = [cfgp, ctypes.POINTER(MokCtxLayout)]
         L.mok_route_layout.argtypes = [cfgp, vp] + [vp] * 13
         L.mok_dispatch.argtypes = [cfgp, vp] + [vp] * 8
+        L.mok_dispatch_by_token.argtypes = [cfgp, vp] + [vp] * 7
         L.mok_expert_ffn.argtypes = [cfgp, vp, vp, ctypes.POINTER(MokWeights)] + [vp] * 10
         L.mok_combine.argtypes = [cfgp, vp, vp, vp, vp]
         L.mok_moe_fused.argtypes = [cfgp, vp, ctypes.POINTER(MokWeights)] + [vp] * 11
@@ -90,6 +91,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp]
         L.mok_transpose_bf16.argtypes = [vp, i64, i64, i64, vp, vp]
         L.mok_layout_static.argtypes = [cfgp] + [vp] * 8
+        L.mok_fused_plan.argtypes = [cfgp, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(i64)]
         L.mok_reset_device_status.argtypes = [vp, vp]
         L.mok_get_device_status.argtypes = [vp, vp]
         L.mok_status_string.argtypes = [ctypes.c_int]
@@ -187,6 +190,13 @@ def dispatch(cfg, x_src, ids, offsets, pad_offsets, row_tok, row_j, xe, xe_scale
         _ptr(xe), _ptr(xe_scales), _stream(stream)))
 
 
+def dispatch_by_token(cfg, x_src, ids, slot_pos, offsets, pad_offsets, xe, xe_scales, stream=None):
+    arr = _src_array(x_src)
+    _check("mok_dispatch_by_token", lib().mok_dispatch_by_token(
+        cfg.ref, arr, _ptr(ids), _ptr(slot_pos), _ptr(offsets), _ptr(pad_offsets), _ptr(xe),
+        _ptr(xe_scales), _stream(stream)))
+
+
 def weights_struct(w: dict) -> MokWeights:
     s = MokWeights()
     for name, _ in MokWeights._fields_:
@@ -254,6 +264,14 @@ def layout_static(cfg, ids, counts, offsets, pad_offsets, slot_pos, row_tok, row
     _check("mok_layout_static", lib().mok_layout_static(
         cfg.ref, _ptr(ids), _ptr(counts), _ptr(offsets), _ptr(pad_offsets), _ptr(slot_pos),
         _ptr(row_tok), _ptr(row_j), _stream(stream)))
+
+
+def fused_plan(cfg) -> dict:
+    """CTAs, gather CTAs, minibatch rows and ring rows the fused forward will use."""
+    c, g, m, r = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    _check("mok_fused_plan", lib().mok_fused_plan(cfg.ref, ctypes.byref(c), ctypes.byref(g), ctypes.byref(m),
+                                                  ctypes.byref(r)))
+    return {"ctas": c.value, "gather_ctas": g.value, "minibatch_rows": m.value, "ring_rows": r.value}
 
 
 def reset_device_status(ws, stream=None):

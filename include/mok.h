@@ -80,7 +80,7 @@ typedef struct {
                                       source s at row r, sources in token order */
     const int *source_rows;        /* host [n_sources] rows per source (NULL if 1) */
     int minibatch_rows;            /* rows per hand-off chunk of the fused forward:
-                                      64 | 128 | 256 (0 = 128) */
+                                      64 | 128 | 256 (0 = from the shape) */
     float gather_sm_fraction;      /* SMs given to the gather/combine role in the
                                       fused forward (0 = automatic) */
     size_t ring_bytes;             /* token ring of the fused forward (0 = no cap) */
@@ -169,6 +169,21 @@ int mok_dispatch(const mok_config *cfg, const void *const *x_src, const int32_t 
                  uint32_t *xe_scales, void *stream);
 
 /*
+ * A3 with one read per token: the same bytes as mok_dispatch (xe, and the
+ * xe_scales when MXFP8), but each token's row is read from its source once
+ * (and quantised once) and written into each of its k slot rows:
+ * pad_offsets[e] + slot_pos[t, j] - offsets[e] for e = ids[t, j].  [kucoin]
+ * §02's pull with one request per token instead of one per slot (on several
+ * GPUs: one pull per token and destination rank, placed into every local
+ * expert the token selected).  HBM reads drop from T*k rows to T rows.
+ * slot_pos: device int32 [T, k] from mok_route_layout; other arguments as
+ * mok_dispatch.
+ */
+int mok_dispatch_by_token(const mok_config *cfg, const void *const *x_src, const int32_t *ids,
+                          const int32_t *slot_pos, const int32_t *offsets,
+                          const int32_t *pad_offsets, void *xe, uint32_t *xe_scales, void *stream);
+
+/*
  * A4 + A5: per-expert SwiGLU FFN as grouped GEMMs on the tensor cores
  * ([kucoin] §01: grouped GEMM over organised input; §02: MXFP8 fused into
  * the grouped GEMM and SwiGLU; push combine: each result goes straight to
@@ -199,9 +214,10 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates,
  * splits the SMs between dispatch/combine/state and the expert FFN, hands
  * minibatches over through on-GPU counters and reuses a fixed-size token ring
  * buffer as soon as the experts are done with it).  From a layout made by
- * mok_route_layout: cfg->gather_sm_fraction of the SMs (0: 1/4) start pulling
- * rows (quantised when MXFP8) into a token ring of cfg->ring_bytes (0: no
- * cap; it must hold 256 rows) in minibatches of cfg->minibatch_rows (0: 128);
+ * mok_route_layout: cfg->gather_sm_fraction of the SMs (0: chosen from the
+ * shape, see mok_fused_plan) start pulling rows (quantised when MXFP8) into a
+ * token ring of cfg->ring_bytes (0: no cap; it must hold 256 rows) in
+ * minibatches of cfg->minibatch_rows (0: chosen from the shape);
  * the other SMs run the FFN1 and FFN2 tiles as rows arrive; finally every SM
  * combines.  The result is bit-identical to mok_dispatch + mok_expert_ffn +
  * mok_combine for every split, minibatch and ring size.  ystage: device BF16
@@ -213,6 +229,25 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
                   const int32_t *ids, const float *gates, const int32_t *counts,
                   const int32_t *offsets, const int32_t *pad_offsets, const int32_t *row_tok,
                   const uint8_t *row_j, void *ystage, void *out, void *ws, void *stream);
+
+/*
+ * The launch plan of the fused forward for this config on the current device,
+ * host only (no device work): its CTAs (one per SM), the CTAs that start in
+ * the gather role, the minibatch (rows per hand-off) and the token ring's
+ * rows.  A knob the config
+ * leaves 0 is chosen from the shape ([kucoin] §03: the right minibatch and
+ * number of communication SMs change with the hidden size, top-k and expert
+ * size; §02: one minibatch should give the expert GEMM two full waves of
+ * tiles): gather CTAs from the ratio of the per-row gather time to the
+ * per-row FFN1 time on one SM (twice that ratio, within 1/16..1/3 of the
+ * SMs; even when the GEMM role runs on CTA pairs); minibatch = the smallest
+ * of 64, 128, 256 rows for which one round of the gather role (one
+ * minibatch per gather CTA, every 128-row tile released as soon as it has
+ * landed) hands over two waves of FFN1 tiles to the GEMM CTAs, else 256.
+ * Any output may be NULL.
+ */
+int mok_fused_plan(const mok_config *cfg, int *ctas, int *gather_ctas, int *minibatch_rows,
+                   int64_t *ring_rows);
 
 /*
  * The whole forward layer: mok_route_layout then the fused persistent kernel

@@ -97,3 +97,40 @@ def test_saved_ctx_layout_is_aligned_and_ordered():
     offs = [getattr(lay, f) for f in fields]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs)
+
+
+def _plan(**kw):
+    return mok.fused_plan(_cfg(**kw))
+
+
+def test_fused_plan_honours_explicit_knobs():
+    # d = 384: one CTA per tile, gather CTAs = round(fraction x CTAs)
+    p = _plan(gather_sm_fraction=0.25, minibatch_rows=64, ring_bytes=1 << 20, T=4096, d_model=384)
+    assert p["gather_ctas"] == int(0.25 * p["ctas"] + 0.5)
+    assert p["minibatch_rows"] == 64
+    # 1 MiB of BF16 rows of 384 elements = 1365 rows -> 1280 (multiple of 256)
+    assert p["ring_rows"] == 1280
+    # d = 256, BF16: CTA pairs, an even CTA count and gather CTAs rounded up to a pair
+    q = _plan(gather_sm_fraction=0.25, ring_bytes=1 << 20, T=4096)
+    assert q["ctas"] % 2 == 0 and q["gather_ctas"] % 2 == 0
+    assert q["gather_ctas"] == (int(0.25 * q["ctas"] + 0.5) + 1) // 2 * 2
+    # 1 MiB of BF16 rows of 256 elements = 2048 rows; an uncapped ring holds every padded row
+    assert q["ring_rows"] == 2048
+    assert _plan()["ring_rows"] == mok.max_padded_rows(_cfg())
+
+
+def test_fused_plan_shape_rules():
+    # gather share: per-row gather time over per-row FFN1 time grows as F shrinks
+    wide = _plan(d_model=4096, d_ff=14336, n_experts=8, top_k=2, T=8192)
+    narrow = _plan(d_model=7168, d_ff=2048, n_experts=256, top_k=8, T=16384, dtype=1)
+    for p in (wide, narrow):
+        assert p["ctas"] / 16 - 1 <= p["gather_ctas"] <= p["ctas"] / 3 + 1
+    assert narrow["gather_ctas"] > wide["gather_ctas"]
+    # minibatch: the smallest of 64/128/256 rows for which one gather round
+    # (a minibatch per gather CTA) hands over two waves of FFN1 tiles
+    for F in (128, 512, 2048, 14336):
+        for frac in (0.0625, 0.25):
+            p = _plan(d_ff=F, d_model=1024, gather_sm_fraction=frac)
+            g, gemm = p["gather_ctas"], p["ctas"] - p["gather_ctas"]
+            want = next((mb for mb in (64, 128) if g * mb * (F // 128) >= 2 * 128 * gemm), 256)
+            assert p["minibatch_rows"] == want, (F, frac, p)

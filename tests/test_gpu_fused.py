@@ -30,6 +30,9 @@ CASES = {
                                   n_sources=8),
     "bf16": I.Workload("bf16", T=1000, d=256, E=8, k=2, F=512, dtype="bf16",
                        router="softmax", seed=62),
+    # d not a multiple of 256: the GEMM role runs one CTA per tile
+    "mx_d384": I.Workload("mx_d384", T=640, d=384, E=16, k=4, F=256, dtype="mxfp8",
+                          router="sigmoid", seed=63),
 }
 
 
@@ -62,6 +65,25 @@ def test_fused_equals_stepwise_bit_exact(name):
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert torch.equal(fused, _stepwise(layer))
+
+
+@pytest.mark.parametrize("name", ["mx_skew_sources", "bf16"])
+def test_fused_cta_pairs_equal_single_cta_bit_exact(name, monkeypatch):
+    """d a multiple of 256: the GEMM role on CTA pairs (256-row tiles, ghost
+    odd halves for experts with an odd number of row tiles) gives the same
+    bits as one CTA per 128-row tile."""
+    w = CASES[name]
+    layer, _ = make_layer(w)
+    monkeypatch.setenv("MOK_FUSED_PAIR", "1")
+    paired = layer.forward().clone()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert mok.fused_plan(layer.cfg)["gather_ctas"] % 2 == 0
+    monkeypatch.setenv("MOK_FUSED_PAIR", "0")
+    single = layer.forward().clone()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(paired, single)
 
 
 def test_fused_bit_identical_across_splits_minibatches_rings():

@@ -62,6 +62,33 @@ def test_dispatch_bit_exact(name):
     assert np.all(ids.reshape(-1)[np.argsort(R.slot_pos.cpu().numpy().reshape(-1))] == e_of_p)
 
 
+@pytest.mark.parametrize("name", list(CASES))
+def test_dispatch_by_token_equals_pull_dispatch(name):
+    """One read per token, written into its k slots: the same bytes (codes,
+    scales, padding rows untouched) as the per-slot pull."""
+    w = CASES[name]
+    layer, _ = make_layer(w)
+    R = Routed(layer)
+    rows = layer.rows_pad
+    outs = []
+    for by_token in (False, True):
+        if w.dtype == "mxfp8":
+            xe = torch.zeros((rows, w.d), dtype=torch.uint8, device="cuda")
+            sc = torch.zeros(scale_words(rows, w.d), dtype=torch.int32, device="cuda")
+        else:
+            xe = torch.zeros((rows, w.d), dtype=torch.bfloat16, device="cuda")
+            sc = None
+        if by_token:
+            mok.dispatch_by_token(layer.cfg, layer.x_src, R.ids, R.slot_pos, R.offsets, R.pad_offsets, xe, sc)
+        else:
+            mok.dispatch(layer.cfg, layer.x_src, R.ids, R.offsets, R.pad_offsets, R.row_tok, R.row_j, xe, sc)
+        torch.cuda.synchronize()
+        outs.append((xe, sc))
+    assert torch.equal(outs[0][0], outs[1][0])
+    if w.dtype == "mxfp8":
+        assert torch.equal(outs[0][1], outs[1][1])
+
+
 @pytest.mark.parametrize("E,rows,K", [(2, 256, 384), (3, 384, 256), (1, 128, 128)])
 def test_weight_quantiser_bit_exact_both_blockings(E, rows, K):
     g = torch.Generator(device="cuda")
