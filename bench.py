@@ -177,6 +177,35 @@ def _layer_bytes(w):
     return weights + x + xe + h + ystage + out
 
 
+# DRAM bytes (read + write) per launch of the fused kernel, from one ncu capture
+# (`--metrics dram__bytes_read.sum,dram__bytes_write.sum`, one pass) of
+# `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-backward [--workload W]`,
+# summarised in profiles/k_moe_fused_traffic.md, keyed by workload and CTA pairs, with a
+# hash of the kernel's sources at capture time: once the kernel changes, traffic is null.
+FUSED_TRAFFIC = {
+    ("mixtral_bf16", 1): {"bytes": 4991344384 + 789386240, "src_sha": "9ab36cf3c30c41da"},
+    ("dsv3_mxfp8", 0): {"bytes": 16929836544 + 3376385024, "src_sha": "9ab36cf3c30c41da"},
+    ("dsv3_skew_ep", 0): {"bytes": 17442530816 + 3373137664, "src_sha": "9ab36cf3c30c41da"},
+}
+FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h")
+
+
+def _fused_src_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in FUSED_SOURCES:
+        with open(os.path.join(ROOT, "combine_top_routing_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _fused_traffic(workload: str, pairs: int):
+    e = FUSED_TRAFFIC.get((workload, pairs))
+    if e is None or e["src_sha"] != _fused_src_sha():
+        return None
+    return e["bytes"]
+
+
 def _dispatch_bytes(w):
     """Algorithmic HBM bytes of the pull dispatch: every token row read once,
     every slot row written once (codes + scales), the row index read."""
@@ -375,6 +404,7 @@ def main():
         gbs = nbytes / (ms_ / 1e3) / 1e9
         hbm_steps[name] = {"ms": ms_, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
                            "peak_gbs": hbm_peak, "frac": gbs / hbm_peak}
+    plan = mok.fused_plan(layer.cfg)
     fused_ms = timed(lambda: mok.moe_fused(layer.cfg, layer.x_src, layer.wstruct, R.ids, R.gates,
                                            R.counts, R.offsets, R.pad_offsets, R.row_tok, R.row_j,
                                            R.ystage, layer.out, layer.ws))
@@ -444,8 +474,11 @@ def main():
                              (w.E * 3 * w.F * w.d * (1 if w.dtype == 'mxfp8' else 2) / 1e9),
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": fused_tflops, "peak": peak_tc,
-                         "unit": "TFLOP/s", "frac": fused_tflops / peak_tc, "traffic": None,
-                         "kernel": "k_moe_fused (pull dispatch + FFN1 + FFN2 + combine)",
+                         "unit": "TFLOP/s", "frac": fused_tflops / peak_tc,
+                         "traffic": _fused_traffic(w.name, plan["cta_pairs"]),
+                         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + write.sum)",
+                         "kernel": ("k_moe_fused_pair" if plan["cta_pairs"] else "k_moe_fused")
+                                   + " (pull dispatch + FFN1 + FFN2 + combine)",
                          "algorithmic": "6*S*d*F flops per launch",
                          "peak_source": f"{peak_src} bf16 burst"
                                         + (" x2 for fp8" if w.dtype == "mxfp8" else ""),
@@ -453,7 +486,7 @@ def main():
             "expert_ffn_separate_kernels": {"ms": ffn_ms,
                                             "tflops": flops / (ffn_ms / 1e3) / 1e12},
             "hbm_steps": hbm_steps,
-            "fused_plan": mok.fused_plan(layer.cfg),
+            "fused_plan": plan,
             "sweep": sweep,
             "layer_roofline": {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
                                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /

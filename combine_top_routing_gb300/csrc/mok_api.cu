@@ -468,8 +468,8 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     return cuda_status(e);
 }
 
-int mok_fused_plan(const mok_config *cfg, int *ctas, int *gather_ctas, int *minibatch_rows,
-                   int64_t *ring_rows)
+int mok_fused_plan(const mok_config *cfg, int *ctas, int *cta_pairs, int *gather_ctas,
+                   int *minibatch_rows, int64_t *ring_rows)
 {
     Dims dm;
     const int rc = check_config(cfg, &dm);
@@ -478,6 +478,7 @@ int mok_fused_plan(const mok_config *cfg, int *ctas, int *gather_ctas, int *mini
     const int grid = fused_ctas(dm, cfg, num_sms());
     fused_knobs(dm, cfg, grid, &ng, &mb);
     if (ctas) *ctas = grid;
+    if (cta_pairs) *cta_pairs = fused_uses_pairs(dm, cfg) ? 1 : 0;
     if (gather_ctas) *gather_ctas = ng;
     if (minibatch_rows) *minibatch_rows = mb;
     if (ring_rows) *ring_rows = fused_ring_rows(dm, cfg->ring_bytes);

@@ -230,17 +230,28 @@ __device__ __forceinline__ void combine_tokens(const FusedArgs &a, int *ffn2_don
     const int vec = a.d / 8;
     for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
         for (int c = threadIdx.x; c < vec; c += blockDim.x) {
+            // all k slot loads in flight before the (ordered) accumulation
+            uint4 yv[MOK_MAX_TOPK];
+            float g[MOK_MAX_TOPK];
+#pragma unroll
+            for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+                if (j < a.k) {
+                    g[j] = a.gates[t * a.k + j];
+                    yv[j] = *(reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c);
+                }
+            }
             float acc[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-            for (int j = 0; j < a.k; ++j) {
-                const float g = a.gates[t * a.k + j];
-                const uint4 y = *(reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c);
-                const uint32_t w[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[2 * i] = fmaf(g, bf16_bits_to_float(w[i] & 0xFFFFu), acc[2 * i]);
-                    acc[2 * i + 1] = fmaf(g, bf16_bits_to_float(w[i] >> 16), acc[2 * i + 1]);
+            for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+                if (j < a.k) {
+                    const uint32_t w[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc[2 * i] = fmaf(g[j], bf16_bits_to_float(w[i] & 0xFFFFu), acc[2 * i]);
+                        acc[2 * i + 1] = fmaf(g[j], bf16_bits_to_float(w[i] >> 16), acc[2 * i + 1]);
+                    }
                 }
             }
             reinterpret_cast<uint4 *>(a.out + t * a.d)[c] =

@@ -91,8 +91,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp]
         L.mok_transpose_bf16.argtypes = [vp, i64, i64, i64, vp, vp]
         L.mok_layout_static.argtypes = [cfgp] + [vp] * 8
-        L.mok_fused_plan.argtypes = [cfgp, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
-                                     ctypes.POINTER(ctypes.c_int), ctypes.POINTER(i64)]
+        L.mok_fused_plan.argtypes = [cfgp] + [ctypes.POINTER(ctypes.c_int)] * 4 + [ctypes.POINTER(i64)]
         L.mok_reset_device_status.argtypes = [vp, vp]
         L.mok_get_device_status.argtypes = [vp, vp]
         L.mok_status_string.argtypes = [ctypes.c_int]
@@ -267,11 +266,12 @@ def layout_static(cfg, ids, counts, offsets, pad_offsets, slot_pos, row_tok, row
 
 
 def fused_plan(cfg) -> dict:
-    """CTAs, gather CTAs, minibatch rows and ring rows the fused forward will use."""
-    c, g, m, r = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
-    _check("mok_fused_plan", lib().mok_fused_plan(cfg.ref, ctypes.byref(c), ctypes.byref(g), ctypes.byref(m),
-                                                  ctypes.byref(r)))
-    return {"ctas": c.value, "gather_ctas": g.value, "minibatch_rows": m.value, "ring_rows": r.value}
+    """CTAs, CTA pairs (0/1), gather CTAs, minibatch rows and ring rows the fused forward will use."""
+    c, p, g, m, r = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_int64()
+    _check("mok_fused_plan", lib().mok_fused_plan(cfg.ref, ctypes.byref(c), ctypes.byref(p), ctypes.byref(g),
+                                                  ctypes.byref(m), ctypes.byref(r)))
+    return {"ctas": c.value, "cta_pairs": p.value, "gather_ctas": g.value, "minibatch_rows": m.value,
+            "ring_rows": r.value}
 
 
 def reset_device_status(ws, stream=None):

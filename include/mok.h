@@ -232,9 +232,12 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
 
 /*
  * The launch plan of the fused forward for this config on the current device,
- * host only (no device work): its CTAs (one per SM), the CTAs that start in
- * the gather role, the minibatch (rows per hand-off) and the token ring's
- * rows.  A knob the config
+ * host only (no device work): its CTAs (at most one per SM), whether its
+ * GEMM role runs on CTA pairs (1) or one CTA per tile (0), the CTAs that
+ * start in the gather role, the minibatch (rows per hand-off) and the token
+ * ring's rows.  CTA pairs are used for BF16 layers with d a multiple of 256
+ * and an uncapped ring or one of at least 512 rows (the environment variable
+ * MOK_FUSED_PAIR = 0 / 1 forces either where the shape allows).  A knob the config
  * leaves 0 is chosen from the shape ([kucoin] §03: the right minibatch and
  * number of communication SMs change with the hidden size, top-k and expert
  * size; §02: one minibatch should give the expert GEMM two full waves of
@@ -246,8 +249,8 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
  * landed) hands over two waves of FFN1 tiles to the GEMM CTAs, else 256.
  * Any output may be NULL.
  */
-int mok_fused_plan(const mok_config *cfg, int *ctas, int *gather_ctas, int *minibatch_rows,
-                   int64_t *ring_rows);
+int mok_fused_plan(const mok_config *cfg, int *ctas, int *cta_pairs, int *gather_ctas,
+                   int *minibatch_rows, int64_t *ring_rows);
 
 /*
  * The whole forward layer: mok_route_layout then the fused persistent kernel

@@ -112,11 +112,15 @@ def test_fused_plan_honours_explicit_knobs():
     assert p["ring_rows"] == 1280
     # d = 256, BF16: CTA pairs, an even CTA count and gather CTAs rounded up to a pair
     q = _plan(gather_sm_fraction=0.25, ring_bytes=1 << 20, T=4096)
+    assert q["cta_pairs"] == 1 and p["cta_pairs"] == 0
     assert q["ctas"] % 2 == 0 and q["gather_ctas"] % 2 == 0
     assert q["gather_ctas"] == (int(0.25 * q["ctas"] + 0.5) + 1) // 2 * 2
     # 1 MiB of BF16 rows of 256 elements = 2048 rows; an uncapped ring holds every padded row
     assert q["ring_rows"] == 2048
     assert _plan()["ring_rows"] == mok.max_padded_rows(_cfg())
+    # MXFP8 layers and rings below 512 rows run one CTA per tile
+    assert _plan(dtype=1)["cta_pairs"] == 0
+    assert _plan(ring_bytes=256 * 256 * 2, T=4096)["cta_pairs"] == 0
 
 
 def test_fused_plan_shape_rules():

@@ -28,6 +28,12 @@ SMALL = {
                                   dtype="bf16", router="sigmoid", seed=34),
     "mx_one_token": I.Workload("mx_one_token", T=1, d=128, E=4, k=4, F=128, dtype="mxfp8",
                                router="softmax", seed=35),
+    # degenerate routing: one expert takes every token (gate 1, three row tiles,
+    # so the CTA-pair tiles end in a ghost half) and top-1 over four experts
+    "bf16_single_expert": I.Workload("bf16_single_expert", T=300, d=256, E=1, k=1, F=256,
+                                     dtype="bf16", router="softmax", seed=36),
+    "mx_top1": I.Workload("mx_top1", T=257, d=256, E=4, k=1, F=128, dtype="mxfp8",
+                          router="sigmoid", seed=37),
 }
 
 

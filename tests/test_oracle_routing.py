@@ -55,6 +55,21 @@ def test_router_brute_force_k3_e6(kind):
         assert list(r["ids"][t]) == _brute_topk(r["scores"][t], 3)
 
 
+@pytest.mark.parametrize("kind", [O.SOFTMAX, O.SIGMOID])
+def test_router_top1_is_argmax_with_unit_gate(kind):
+    # k = 1: the expert of largest score (ties to the lower id), and the
+    # renormalised gate of a single chosen expert is exactly 1; E = 1 routes
+    # every token to expert 0.
+    rng = np.random.default_rng(13)
+    x = rng.standard_normal((40, 12))
+    Wr = rng.standard_normal((5, 12))
+    r = O.router(x, Wr, None, 1, kind)
+    assert np.array_equal(r["ids"][:, 0], np.argmax(x @ Wr.T, axis=1))
+    assert np.all(r["gates"] == 1.0)
+    r1 = O.router(x, Wr[:1], None, 1, kind)
+    assert np.all(r1["ids"] == 0) and np.all(r1["gates"] == 1.0)
+
+
 def test_router_tie_goes_to_lower_id():
     # d = 1, x = 1: the logits are the router weights themselves.
     x = np.ones((1, 1))
