@@ -183,9 +183,9 @@ def _layer_bytes(w):
 # summarised in profiles/k_moe_fused_traffic.md, keyed by workload and CTA pairs, with a
 # hash of the kernel's sources at capture time: once the kernel changes, traffic is null.
 FUSED_TRAFFIC = {
-    ("mixtral_bf16", 1): {"bytes": 4991344384 + 789386240, "src_sha": "9ab36cf3c30c41da"},
-    ("dsv3_mxfp8", 0): {"bytes": 16929836544 + 3376385024, "src_sha": "9ab36cf3c30c41da"},
-    ("dsv3_skew_ep", 0): {"bytes": 17442530816 + 3373137664, "src_sha": "9ab36cf3c30c41da"},
+    ("mixtral_bf16", 1): {"bytes": 4774168832 + 789335040, "src_sha": "d644173b3c1b5d12"},
+    ("dsv3_mxfp8", 0): {"bytes": 17054084096 + 3360613632, "src_sha": "d644173b3c1b5d12"},
+    ("dsv3_skew_ep", 0): {"bytes": 17312438528 + 3360461312, "src_sha": "d644173b3c1b5d12"},
 }
 FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h")
 

@@ -148,18 +148,104 @@ __device__ __forceinline__ int expert_of_row(const int *s_pad, int E, int64_t q)
     return lo;
 }
 
+// MXFP8 quantisation of elements [c0, c0 + 1024) of a BF16 row held in shared
+// memory, one MX block of 32 per lane (the arithmetic of mx_quant_stretch,
+// laid out for instruction-level parallelism): lane l reads block l as four
+// 16-byte pieces in a rotated order (conflict-free: each read by the warp is
+// four wavefronts), takes the block's amax in registers, writes its 32 codes
+// and, with two shuffles, lanes 4g write the scale words of the chunk's
+// k-groups.  A tail chunk (d - c0 < 1024) leaves the lanes past it idle
+// except for the shuffles.
+__device__ __forceinline__ void mx_quant_block_per_lane(const uint8_t *row, int c0, int d, int lane,
+                                                        uint8_t *codes_row, uint32_t *scales,
+                                                        int64_t scale_row, int64_t scale_rows)
+{
+    const int nblk = (d - c0) >= 1024 ? 32 : (d - c0) / 32;
+    const bool on = lane < nblk;
+    const int rot = (lane >> 1) & 3;
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[q] = make_uint4(0, 0, 0, 0);
+        if (on) v[q] = *reinterpret_cast<const uint4 *>(row + (c0 + 32 * lane) * 2 + 16 * ((q + rot) & 3));
+    }
+    float f[32];
+#pragma unroll
+    for (int p2 = 0; p2 < 4; ++p2) {
+        const int qp = (p2 - rot) & 3;  // the read that fetched piece p2
+        uint4 src = v[0];
+        if (qp == 1) src = v[1];
+        if (qp == 2) src = v[2];
+        if (qp == 3) src = v[3];
+        const uint32_t w[4] = {src.x, src.y, src.z, src.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[8 * p2 + 2 * i] = bf16_bits_to_float(w[i] & 0xFFFFu);
+            f[8 * p2 + 2 * i + 1] = bf16_bits_to_float(w[i] >> 16);
+        }
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    const int x = mx_scale_exp(amax);
+    const float inv = mx_inv_scale(x);
+    uint32_t code[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        code[i] = pack_e4m3x2(f[4 * i] * inv, f[4 * i + 1] * inv) |
+                  (pack_e4m3x2(f[4 * i + 2] * inv, f[4 * i + 3] * inv) << 16);
+    if (on) {
+        uint4 *o = reinterpret_cast<uint4 *>(codes_row + c0 + 32 * lane);
+        o[0] = make_uint4(code[0], code[1], code[2], code[3]);
+        o[1] = make_uint4(code[4], code[5], code[6], code[7]);
+    }
+    // scale byte of block l at byte l % 4 of the word of k-group (c0 + 32 l) / 128
+    uint32_t word = static_cast<uint32_t>(x + 127) << (8 * (lane & 3));
+    word |= __shfl_xor_sync(0xffffffffu, word, 1);
+    word |= __shfl_xor_sync(0xffffffffu, word, 2);
+    if (on && (lane & 3) == 0)
+        scales[mx_word_index((c0 + 32 * lane) >> 7, scale_row, scale_rows)] = word;
+}
+
 // Gather role of the fused forward: pull expert-ordered rows into the token
 // ring (quantised when MXFP8) in minibatches claimed from a global counter,
 // after the ring rows' previous occupants were loaded by every FFN1 tile, and
 // publish each 64-row half of a row tile in ready[].  Every thread of the CTA
 // calls it.
+//
+// Rows are staged through shared memory: the GEMM stage buffers (`stage`,
+// unused while this CTA gathers) hold up to 16 source rows, each fetched by
+// one bulk copy completing on its own mbarrier, so ~190 KB of row reads are in
+// flight per SM while the six warps quantise (MXFP8) or copy (BF16) the rows
+// already landed.  A row too large for two slots is read directly.
 template <bool MX>
 __device__ __forceinline__ void gather_rows(const FusedArgs &a, const int *s_pad, int64_t pad_end, int *s_unit,
                                             volatile int *abort_flag, int *next_unit, int *ready,
-                                            int *consumed, int warp, int lane, int nwarps)
+                                            int *consumed, int warp, int lane, int nwarps,
+                                            uint8_t *stage, int stage_bytes)
 {
     const int units = static_cast<int>((pad_end + a.mb - 1) / a.mb);
     const int ring_tiles = static_cast<int>(a.ring_rows / kBM);
+    // staging layout: 16 mbarriers, the unit's row and token lists, then slots
+    constexpr int kHdr = 2304;
+    const int row_bytes = a.d * 2;
+    const int slot_bytes = (row_bytes + 127) & ~127;
+    int ns = (stage_bytes - kHdr) / slot_bytes;
+    ns = ns > 16 ? 16 : ns;
+    const bool staged = ns >= 2;
+    uint64_t *gbar = reinterpret_cast<uint64_t *>(stage);
+    int *lst_q = reinterpret_cast<int *>(stage + 128);  // [256] padded rows of the unit with a token
+    int *lst_t = lst_q + 256;                            // [256] their tokens
+    int *s_n = lst_t + 256;
+    uint8_t *slots = stage + kHdr;
+    if (staged) {
+        if (threadIdx.x == 0) {
+            for (int j = 0; j < ns; ++j) mbar_init(&gbar[j], 1);
+            fence_barrier_init();
+        }
+        __syncthreads();
+    }
+    uint32_t base = 0;  // rows this CTA has staged so far: slot = base % ns, parity = (base / ns) & 1
     for (;;) {
         if (threadIdx.x == 0) *s_unit = atomicAdd(next_unit, 1);
         __syncthreads();
@@ -176,33 +262,94 @@ __device__ __forceinline__ void gather_rows(const FusedArgs &a, const int *s_pad
         }
         __syncthreads();
         if (*abort_flag) break;
-        for (int64_t q = r0 + warp; q < r1; q += nwarps) {
-            const int e = expert_of_row(s_pad, a.E, q);
-            const int64_t local = q - s_pad[e];
-            if (local >= a.counts[e]) continue;  // padding row: nothing to pull
-            const int t = a.row_tok[a.offsets[e] + local];
-            const uint4 *in = reinterpret_cast<const uint4 *>(source_row(a.src, t, a.d));
-            const int64_t rr = q % a.ring_rows;
-            if (!MX) {
-                uint4 *o = reinterpret_cast<uint4 *>(a.ring + rr * a.d * 2);
-#pragma unroll 8
-                for (int c = lane; c < a.d / 8; c += 32) o[c] = __ldg(in + c);
-            } else {
-                uint8_t *codes_row = a.ring + rr * a.d;
-                for (int c0 = 0; c0 < a.d; c0 += 2048) {
-                    uint4 raw[8];
+        if (staged) {
+            // the unit's rows that hold a token (padding rows: nothing to pull)
+            if (threadIdx.x == 0) *s_n = 0;
+            __syncthreads();
+            for (int i = threadIdx.x; i < static_cast<int>(r1 - r0); i += blockDim.x) {
+                const int64_t q = r0 + i;
+                const int e = expert_of_row(s_pad, a.E, q);
+                const int64_t local = q - s_pad[e];
+                if (local < a.counts[e]) {
+                    const int idx = atomicAdd(s_n, 1);
+                    lst_q[idx] = static_cast<int>(q);
+                    lst_t[idx] = a.row_tok[a.offsets[e] + local];
+                }
+            }
+            __syncthreads();
+            const int n = *s_n;
+            auto issue = [&](int i) {
+                const int slot = static_cast<int>((base + static_cast<uint32_t>(i)) % static_cast<uint32_t>(ns));
+                mbar_arrive_expect_tx(&gbar[slot], static_cast<uint32_t>(row_bytes));
+                bulk_load(slots + slot * slot_bytes, source_row(a.src, lst_t[i], a.d), static_cast<uint32_t>(row_bytes),
+                          &gbar[slot]);
+            };
+            if (threadIdx.x == 0)
+                for (int i = 0; i < n && i < ns; ++i) issue(i);
+            for (int i = warp; i < n; i += nwarps) {
+                const uint32_t g = base + static_cast<uint32_t>(i);
+                const int slot = static_cast<int>(g % static_cast<uint32_t>(ns));
+                if (!wait_bar(&gbar[slot], (g / static_cast<uint32_t>(ns)) & 1u, a.status, a.wait_ns, abort_flag)) break;
+                const uint8_t *row = slots + slot * slot_bytes;
+                const int64_t rr = lst_q[i] % a.ring_rows;
+                if (!MX) {
+                    uint4 *o = reinterpret_cast<uint4 *>(a.ring + rr * a.d * 2);
+                    const uint4 *in = reinterpret_cast<const uint4 *>(row);
+                    for (int c = lane; c < a.d / 8; c += 32) o[c] = in[c];
+                } else {
+                    uint8_t *codes_row = a.ring + rr * a.d;
+                    for (int c0 = 0; c0 < a.d; c0 += 1024)
+                        mx_quant_block_per_lane(row, c0, a.d, lane, codes_row, a.ring_scales, rr, a.ring_rows);
+                }
+                // this warp's reads of the slot come before the next bulk copy into it
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0 && i + ns < n) issue(i + ns);
+            }
+            base += static_cast<uint32_t>(n);
+        } else {
+            for (int64_t q = r0 + warp; q < r1; q += nwarps) {
+                const int e = expert_of_row(s_pad, a.E, q);
+                const int64_t local = q - s_pad[e];
+                if (local >= a.counts[e]) continue;  // padding row: nothing to pull
+                const int t = a.row_tok[a.offsets[e] + local];
+                const uint4 *in = reinterpret_cast<const uint4 *>(source_row(a.src, t, a.d));
+                const int64_t rr = q % a.ring_rows;
+                // 16 vectors of 16 bytes per lane in flight (8 KB per warp): a gather
+                // CTA runs six warps and the row reads miss L2, so the loads in
+                // flight set the gather rate
+                if (!MX) {
+                    uint4 *o = reinterpret_cast<uint4 *>(a.ring + rr * a.d * 2);
+                    for (int c0 = 0; c0 < a.d / 8; c0 += 512) {
+                        uint4 v[16];
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        const int cu = c0 + 256 * w;
-                        const int nvalid = cu >= a.d ? 0 : (a.d - cu >= 256 ? 32 : 16);
-                        raw[w] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
+                        for (int u = 0; u < 16; ++u) {
+                            const int c = c0 + 32 * u + lane;
+                            v[u] = c < a.d / 8 ? __ldg(in + c) : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            const int c = c0 + 32 * u + lane;
+                            if (c < a.d / 8) o[c] = v[u];
+                        }
                     }
+                } else {
+                    uint8_t *codes_row = a.ring + rr * a.d;
+                    for (int c0 = 0; c0 < a.d; c0 += 4096) {
+                        uint4 raw[16];
 #pragma unroll
-                    for (int w = 0; w < 8; ++w) {
-                        const int cu = c0 + 256 * w;
-                        if (cu < a.d)
-                            mx_quant_stretch(raw[w], lane, a.d - cu >= 256 ? 32 : 16, codes_row, cu,
-                                             a.ring_scales, rr, a.ring_rows);
+                        for (int w = 0; w < 16; ++w) {
+                            const int cu = c0 + 256 * w;
+                            const int nvalid = cu >= a.d ? 0 : (a.d - cu >= 256 ? 32 : 16);
+                            raw[w] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
+                        }
+#pragma unroll
+                        for (int w = 0; w < 16; ++w) {
+                            const int cu = c0 + 256 * w;
+                            if (cu < a.d)
+                                mx_quant_stretch(raw[w], lane, a.d - cu >= 256 ? 32 : 16, codes_row, cu,
+                                                 a.ring_scales, rr, a.ring_rows);
+                        }
                     }
                 }
             }
@@ -216,6 +363,13 @@ __device__ __forceinline__ void gather_rows(const FusedArgs &a, const int *s_pad
         }
     }
     __syncthreads();
+    if (staged) {
+        // the staging bytes go back to the GEMM role's TMA loads
+        if (threadIdx.x == 0 && !*abort_flag)
+            for (int j = 0; j < ns; ++j) mbar_inval(&gbar[j]);
+        fence_proxy_async_shared();
+        __syncthreads();
+    }
 }
 
 // Weighted combine of the fused forward: once every FFN2 tile has pushed its
@@ -335,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- gather role
     if (static_cast<int>(blockIdx.x) < a.n_gather)
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
-                        kThreads / 32);
+                        kThreads / 32, smem, kStages * (kAStage + kBStage));
 
     // ------------------------------------------------------------ GEMM role
     if (warp == 0) {
@@ -675,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------- gather role
     if (static_cast<int>(blockIdx.x) < a.n_gather) {
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
-                        kThreads / 32);
+                        kThreads / 32, smem, kFPStages * kFPStage);
         cluster_sync_all();  // the pair joins the GEMM role together
     }
 
