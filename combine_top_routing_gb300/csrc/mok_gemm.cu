@@ -515,7 +515,7 @@ template <int MODE, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_pair(const __grid_constant__ PairMaps pm, const GemmArgs a)
 {
-    static_assert(MODE == MODE_FFN1 || MODE == MODE_FFN2, "pair path: forward GEMMs");
+    static_assert(MODE == MODE_FFN1 || MODE == MODE_FFN2 || MODE == MODE_WGRAD, "pair path: FFN1, FFN2, WGRAD");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -567,8 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int per = (groups + 31) / 32;
         const int g0 = lane * per;
         int local = 0;
-        for (int g = g0; g < g0 + per && g < groups; ++g)
-            local += ((a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM + 1) / 2 * a.n_tiles;
+        // WGRAD: a fixed (X / 256) x (Y / 256) tiles per expert; FFN: pair rows x N tiles
+        auto pair_tiles = [&](int g) {
+            if constexpr (MODE == MODE_WGRAD) return a.m_rows / (2 * kBM) * a.n_tiles;
+            else return ((a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM + 1) / 2 * a.n_tiles;
+        };
+        for (int g = g0; g < g0 + per && g < groups; ++g) local += pair_tiles(g);
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -578,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int run = incl - local;
         for (int g = g0; g < g0 + per && g < groups; ++g) {
             prefix[g] = run;
-            run += ((a.pad_offsets[g + 1] - a.pad_offsets[g]) / kBM + 1) / 2 * a.n_tiles;
+            run += pair_tiles(g);
         }
         if (lane == 31) prefix[groups] = incl;
     }
@@ -599,10 +603,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = pair; tile < total; tile += npairs) {
                 const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
                 const int g = tl.group;
-                const int ya = a.pad_offsets[g] + (2 * tl.m_blk + static_cast<int>(rank)) * kBM;
+                const int kst = tile_k_stages<MODE, MX>(a, g);
+                // WGRAD: A rows over X, B rows over Y, K along the expert's token rows
+                const int x0 = MODE == MODE_WGRAD ? a.pad_offsets[g] : 0;
+                const int ya = MODE == MODE_WGRAD ? (2 * tl.m_blk + static_cast<int>(rank)) * kBM
+                                                  : a.pad_offsets[g] + (2 * tl.m_blk + static_cast<int>(rank)) * kBM;
                 int yb, ysf;
                 const CUtensorMap *bmap;
-                if constexpr (MODE == MODE_FFN1) {
+                if constexpr (MODE == MODE_WGRAD) {
+                    ysf = tl.n_blk * 256;
+                    yb = ysf + static_cast<int>(rank) * 128;
+                    bmap = &pm.b0;
+                } else if constexpr (MODE == MODE_FFN1) {
                     yb = g * a.b_rows_per_group + tl.n_blk * 128;
                     ysf = yb;
                     bmap = rank ? &pm.b1 : &pm.b0;
@@ -611,10 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     yb = ysf + static_cast<int>(rank) * 128;
                     bmap = &pm.b0;
                 }
-                for (int ks = 0; ks < a.k_stages; ++ks) {
+                for (int ks = 0; ks < kst; ++ks) {
                     if (!wait_bar(&empty[stage], phase ^ 1u, a.status, a.wait_ns, abort_flag)) goto producer_done;
                     uint8_t *dA = sT + stage * kPStage;
-                    const int x = ks * kE;
+                    const int x = x0 + ks * kE;
                     const uint32_t fb = full0 + stage * 8;
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * cta_bytes);
                     tma_load_2d_pair(dA, &pm.a, fb, x, ya);
@@ -645,9 +657,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             const uint32_t idesc = idesc_bf16(2 * kBM, 256);
             for (int tile = pair; tile < total; tile += npairs) {
+                const int kst = tile_k_stages<MODE, MX>(a, decode_tile(tile, prefix, groups, a.n_tiles).group);
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
-                for (int ks = 0; ks < a.k_stages; ++ks) {
+                for (int ks = 0; ks < kst; ++ks) {
                     if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
                     tc_fence_after();
                     const uint32_t aaddr = smem_u32(sT + stage * kPStage);
@@ -699,12 +712,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             const int e = tl.group;
             const int row_in_e = (2 * tl.m_blk + static_cast<int>(rank)) * kBM + r;
-            const bool valid = row_in_e < a.counts[e];
-            if constexpr (MODE == MODE_FFN1) {
+            if constexpr (MODE == MODE_WGRAD) {
+                // dW row (expert e, X row) and 256 columns; zeros for an expert without rows
+                const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
+                uint16_t *dst = a.out_rows + (static_cast<int64_t>(e) * a.m_rows + row_in_e) * a.out_ld +
+                                tl.n_blk * 256;
+                epi_rows_bf16(trow, 256, empty_k, true, dst, stage_out + (warp - 2) * kStageWords, lane, release);
+            } else if constexpr (MODE == MODE_FFN1) {
+                const bool valid = row_in_e < a.counts[e];
                 epi_ffn1<MX>(trow, valid, a.pad_offsets[e] + row_in_e, tl.n_blk * 128, a.F, a.h, a.h_scales,
                              a.h_rows, a.saved_a, a.saved_b, a.saved_h, stage_out + (warp - 2) * kStageWords,
                              lane, release);
             } else {
+                const bool valid = row_in_e < a.counts[e];
                 uint16_t *dst = nullptr;
                 if (valid) {
                     const int64_t p = a.offsets[e] + row_in_e;
@@ -1056,6 +1076,25 @@ cudaError_t launch_wgrad(const Dims &dm, const void *A_T, const uint32_t *A_s, i
     am.n = 1;
     GemmArgs g = base_args(dm, status, wait_ns);
     g.pad_offsets = pad_offsets;
+    if (use_pair_gemm() && a_rows % 256 == 0 && b_rows % 256 == 0) {
+        // CTA pairs: 256 dW rows x 256 columns per pair tile
+        PairMaps pm = {};
+        pm.a = am.m[0];
+        pm.b0 = pm.b1 = bm;
+        if (mx && (encode_tmap_scales(&pm.sa, A_s, static_cast<uint64_t>(a_rows), static_cast<uint64_t>(dm.rows_pad)) ||
+                   encode_tmap_scales(&pm.sb0, B_s, static_cast<uint64_t>(b_rows), static_cast<uint64_t>(dm.rows_pad))))
+            return cudaErrorInvalidValue;
+        pm.sb1 = pm.sb0;
+        if (!mx) pm.sa = pm.sb0 = pm.sb1 = bm;  // unused
+        g.BN = 256;
+        g.n_tiles = static_cast<int>(b_rows / 256);
+        g.m_rows = static_cast<int>(a_rows);
+        g.sfa_rows[0] = a_rows;
+        g.sfb_rows[0] = g.sfb_rows[1] = b_rows;
+        g.out_rows = dW;
+        g.out_ld = b_rows;
+        return mx ? launch_gemm_pair<MODE_WGRAD, true>(pm, g, st) : launch_gemm_pair<MODE_WGRAD, false>(pm, g, st);
+    }
     g.BN = b_rows % 256 == 0 ? 256 : 128;
     g.n_tiles = static_cast<int>(b_rows / g.BN);
     g.m_rows = static_cast<int>(a_rows);

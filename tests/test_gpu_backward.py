@@ -28,6 +28,9 @@ SMALL = {
                              router="sigmoid", seed=43, n_sources=4),
     "bf16_many_empty": I.Workload("bf16_many_empty", T=16, d=256, E=64, k=2, F=256,
                                   dtype="bf16", router="sigmoid", seed=44),
+    # d and F multiples of 256: every weight-gradient GEMM runs on CTA pairs
+    "mx_pairs": I.Workload("mx_pairs", T=600, d=512, E=16, k=4, F=512, dtype="mxfp8",
+                           router="sigmoid", seed=45),
 }
 
 
@@ -82,9 +85,21 @@ def test_backward_small_full_parity(name):
     dWg = np.stack([g["experts"][e]["dWg"] for e in range(w.E)])
     dWu = np.stack([g["experts"][e]["dWu"] for e in range(w.E)])
     dWd = np.stack([g["experts"][e]["dWd"] for e in range(w.E)])
-    check_close(bf16_np(layer.grads["d_gate"]), dWg, what="dW_g")
-    check_close(bf16_np(layer.grads["d_up"]), dWu, what="dW_u")
-    check_close(bf16_np(layer.grads["d_down"]), dWd, what="dW_d")
+    if w.dtype == "mxfp8":
+        # End to end, the oracle's own h and dy can differ from the GPU's by one
+        # BF16 ulp, and the weight-gradient GEMMs re-quantise them to MXFP8 along
+        # the tokens: one flipped E4M3 code moves one dW element by up to 1/8 of
+        # that product, so only the relative L2 bound applies to the chain.  The
+        # element bound holds at the step boundary: the GPU's own saved operands
+        # through the oracle's weight-gradient step.
+        check_close(bf16_np(layer.grads["d_gate"]), dWg, mabs=np.inf, what="dW_g (chain)")
+        check_close(bf16_np(layer.grads["d_up"]), dWu, mabs=np.inf, what="dW_u (chain)")
+        check_close(bf16_np(layer.grads["d_down"]), dWd, mabs=np.inf, what="dW_d (chain)")
+        _check_wgrad_step(layer, inp, w, ids, range(w.E))
+    else:
+        check_close(bf16_np(layer.grads["d_gate"]), dWg, what="dW_g")
+        check_close(bf16_np(layer.grads["d_up"]), dWu, what="dW_u")
+        check_close(bf16_np(layer.grads["d_down"]), dWd, what="dW_d")
     counts = np.bincount(ids.reshape(-1), minlength=w.E)
     for e in np.where(counts == 0)[0]:
         assert not layer.grads["d_gate"][e].any() and not layer.grads["d_down"][e].any()
@@ -109,8 +124,26 @@ def test_backward_full_size_sampled():
     check_close(f32_np(layer.dlogits[tk]), g["dlogits"], what="dlogits")
 
     # weight gradients of sampled experts from the GPU's step-boundary operands
+    counts = layer.ctx_view("counts", torch.int32, (w.E,)).cpu().numpy()
+    sampled = (int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30))))
+    _check_wgrad_step(layer, inp, w, ids, sampled)
+    for e in sampled:
+        # router weight gradient of e: only tokens routed to e carry dlogits[:, e]
+        sel = np.where((ids == e).any(1))[0]
+        sc = f32_np(layer.ctx_view("sel_scores", torch.float32, (w.T, w.k)))
+        scores = np.zeros((len(sel), w.E))
+        np.put_along_axis(scores, ids[sel].astype(np.int64), sc[sel], 1)
+        rb = O.router_bwd(x[sel], Wr, scores, ids[sel], gates[sel], f32_np(layer.dgates)[sel], _kind(w))
+        check_close(f32_np(layer.dW_r[e]), rb["dWr"][e], what=f"dW_r[{e}]")
+
+
+def _check_wgrad_step(layer, inp, w, ids, experts):
+    """B4 at its step boundary: the GPU's saved h and its dy, da, db rows and
+    the tokens' x rows through the oracle's weight-gradient step, for the
+    given experts, against the GPU's dW."""
     bw = layer.bws
     R = layer.rows_pad
+    x = bf16_np(inp["x"])
     counts = layer.ctx_view("counts", torch.int32, (w.E,)).cpu().numpy()
     pad = layer.ctx_view("pad_offsets", torch.int32, (w.E + 1,)).cpu().numpy()
     off = layer.ctx_view("offsets", torch.int32, (w.E + 1,)).cpu().numpy()
@@ -120,7 +153,9 @@ def test_backward_full_size_sampled():
     dy_rows = bw[fields["dy"]:fields["dy"] + R * w.d * 2].view(torch.bfloat16).view(R, w.d)
     da = bw[fields["da"]:fields["da"] + R * w.F * 2].view(torch.bfloat16).view(R, w.F)
     db = bw[fields["db"]:fields["db"] + R * w.F * 2].view(torch.bfloat16).view(R, w.F)
-    for e in (int(np.argmax(counts)), int(np.argmin(np.where(counts > 0, counts, 1 << 30)))):
+    for e in experts:
+        if counts[e] == 0:
+            continue
         rows = slice(int(pad[e]), int(pad[e]) + int(counts[e]))
         toks = row_tok[off[e]:off[e] + counts[e]]
         ref = O.expert_wgrad(bf16_np(dy_rows[rows]), bf16_np(h[rows]), bf16_np(da[rows]),
@@ -128,13 +163,6 @@ def test_backward_full_size_sampled():
         check_close(bf16_np(layer.grads["d_down"][e]), ref["dWd"], what=f"dW_d[{e}]")
         check_close(bf16_np(layer.grads["d_gate"][e]), ref["dWg"], what=f"dW_g[{e}]")
         check_close(bf16_np(layer.grads["d_up"][e]), ref["dWu"], what=f"dW_u[{e}]")
-        # router weight gradient of e: only tokens routed to e carry dlogits[:, e]
-        sel = np.where((ids == e).any(1))[0]
-        sc = f32_np(layer.ctx_view("sel_scores", torch.float32, (w.T, w.k)))
-        scores = np.zeros((len(sel), w.E))
-        np.put_along_axis(scores, ids[sel].astype(np.int64), sc[sel], 1)
-        rb = O.router_bwd(x[sel], Wr, scores, ids[sel], gates[sel], f32_np(layer.dgates)[sel], _kind(w))
-        check_close(f32_np(layer.dW_r[e]), rb["dWr"][e], what=f"dW_r[{e}]")
 
 
 def _bwd_offsets(layer):
@@ -165,3 +193,23 @@ def test_backward_bit_reproducible():
                     sha(layer.dW_r), sha(layer.dgates)))
     torch.cuda.synchronize()
     assert len(hashes) == 1
+
+
+@pytest.mark.parametrize("name", ["mx_pairs", "bf16_many_empty", "mx_sources"])
+def test_wgrad_cta_pairs_equal_single_cta(name, monkeypatch):
+    """The weight-gradient GEMMs on CTA pairs (256 dW rows per pair tile)
+    give the same bits as one CTA per 128-row tile, experts without rows
+    included (their dW blocks are zero)."""
+    w = SMALL[name]
+    layer, inp = make_layer(w, training=True)
+    layer.prepare_backward()
+    layer.forward()
+    grads = {}
+    for pair in ("0", "1"):
+        monkeypatch.setenv("MOK_GEMM_PAIR", pair)
+        layer.backward(inp["dY"])
+        torch.cuda.synchronize()
+        grads[pair] = {k: v.clone() for k, v in layer.grads.items()}
+        grads[pair]["dX"] = layer.dX.clone()
+    for k in grads["0"]:
+        assert torch.equal(grads["0"][k], grads["1"][k]), k
