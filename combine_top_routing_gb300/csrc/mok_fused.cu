@@ -647,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto release = [&]() {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
+                if (lane == 0) mbar_arrive_relaxed(acc_empty);
                 released = true;
             };
             if (f1) {
@@ -1013,7 +1013,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto release = [&]() {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(acc_empty_even);
+                if (lane == 0) mbar_arrive_remote_relaxed(acc_empty_even);
                 released = true;
             };
             if (jb.f1) {

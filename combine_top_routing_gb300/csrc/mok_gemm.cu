@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto release = [&]() {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
+                if (lane == 0) mbar_arrive_relaxed(acc_empty);
                 released = true;
             };
             if constexpr (MODE == MODE_ROUTER) {
@@ -707,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto release = [&]() {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_remote(acc_empty_leader);
+                if (lane == 0) mbar_arrive_remote_relaxed(acc_empty_leader);
                 released = true;
             };
             const int e = tl.group;
