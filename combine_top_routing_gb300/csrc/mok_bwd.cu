@@ -125,49 +125,61 @@ __global__ void __launch_bounds__(256) k_transpose_rows(
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_offsets,
     const int32_t *__restrict__ row_tok, int64_t rows_pad, void *out, uint32_t *__restrict__ out_s)
 {
-    __shared__ uint16_t tile[32][256 + 8];
-    __shared__ int32_t s_pad[MOK_MAX_EXPERTS + 1];
+    // A 256-row x 64-column tile: every row read is one 128-byte line, held
+    // transposed in shared memory as 64 rows of 256 tokens whose 8-token chunks
+    // are XOR-swizzled by the row (chunk t/8 of column c at chunk (t/8) ^ (c % 32)),
+    // so that the transposing writes and the 16-byte row reads stay near
+    // conflict-free.
+    __shared__ __align__(16) uint16_t tile[64][256];
+    __shared__ const uint16_t *s_row[256];
     const int64_t q0 = static_cast<int64_t>(blockIdx.y) * 256;
-    const int c0 = blockIdx.x * 32;
-    for (int e = threadIdx.x; e <= E; e += blockDim.x) s_pad[e] = pad_offsets[e];
-    __syncthreads();
-    if (q0 >= s_pad[E]) return;  // beyond the last expert segment: never read
-    for (int i = threadIdx.x; i < 256 * 4; i += blockDim.x) {
-        const int rr = i >> 2, cc = (i & 3) * 8;
-        const int64_t q = q0 + rr;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (q < s_pad[E]) {
+    const int c0 = blockIdx.x * 64;
+    const int64_t pad_end = pad_offsets[E];
+    if (q0 >= pad_end) return;  // beyond the last expert segment: never read
+    {
+        // source row of padded row q0 + threadIdx.x (null: padding, reads as zeros)
+        const int64_t q = q0 + threadIdx.x;
+        const uint16_t *row = nullptr;
+        if (q < pad_end) {
             int lo = 0, hi = E;  // expert segment holding q
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (s_pad[mid] <= q) lo = mid;
+                if (pad_offsets[mid] <= q) lo = mid;
                 else hi = mid;
             }
-            const int64_t local = q - s_pad[lo];
+            const int64_t local = q - pad_offsets[lo];
             if (local < counts[lo]) {
-                const uint16_t *row;
                 if (GATHER) row = source_row(src, row_tok[offsets[lo] + local], C);
                 else row = in + q * C;
-                v = __ldg(reinterpret_cast<const uint4 *>(row + c0 + cc));
             }
         }
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        s_row[threadIdx.x] = row;
+    }
+    __syncthreads();
+    // 8 threads per row (16 bytes each), 32 rows per pass, all 8 passes in flight
+    const int cc = (threadIdx.x & 7) * 8;
+    uint4 v[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const uint16_t *row = s_row[p * 32 + (threadIdx.x >> 3)];
+        v[p] = row ? __ldg(reinterpret_cast<const uint4 *>(row + c0 + cc)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        const int r = p * 32 + (threadIdx.x >> 3);
+        const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
 #pragma unroll
         for (int q2 = 0; q2 < 4; ++q2) {
-            tile[cc + 2 * q2][rr] = static_cast<uint16_t>(w[q2] & 0xFFFFu);
-            tile[cc + 2 * q2 + 1][rr] = static_cast<uint16_t>(w[q2] >> 16);
+            const int c = cc + 2 * q2;
+            tile[c][(((r >> 3) ^ (c & 31)) << 3) | (r & 7)] = static_cast<uint16_t>(w[q2] & 0xFFFFu);
+            tile[c + 1][(((r >> 3) ^ ((c + 1) & 31)) << 3) | (r & 7)] = static_cast<uint16_t>(w[q2] >> 16);
         }
     }
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int oc = warp; oc < 32; oc += blockDim.x >> 5) {
+    for (int oc = warp; oc < 64; oc += blockDim.x >> 5) {
         const int64_t orow = c0 + oc;
-        const uint16_t *tp = &tile[oc][8 * lane];
-        uint4 raw;
-        raw.x = tp[0] | (static_cast<uint32_t>(tp[1]) << 16);
-        raw.y = tp[2] | (static_cast<uint32_t>(tp[3]) << 16);
-        raw.z = tp[4] | (static_cast<uint32_t>(tp[5]) << 16);
-        raw.w = tp[6] | (static_cast<uint32_t>(tp[7]) << 16);
+        const uint4 raw = *reinterpret_cast<const uint4 *>(&tile[oc][(lane ^ (oc & 31)) << 3]);
         if (MX) {
             mx_quant_stretch(raw, lane, 32, static_cast<uint8_t *>(out) + orow * rows_pad, q0, out_s,
                              orow, C);
@@ -297,7 +309,7 @@ cudaError_t launch_transpose_rows(const Dims &dm, const uint16_t *in, const Sour
                                   const int32_t *pad_offsets, const int32_t *row_tok, void *out,
                                   uint32_t *out_s, cudaStream_t st)
 {
-    dim3 grid(static_cast<unsigned>(C / 32), static_cast<unsigned>(dm.rows_pad / 256));
+    dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(dm.rows_pad / 256));
     const bool mx = dm.dtype == MOK_MXFP8;
     Sources empty_src = {};
     const Sources &s = src ? *src : empty_src;
