@@ -497,8 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 // the same tile sequence; an odd last row tile of an expert is computed and
 // discarded (its A rows and scales beyond the matrix read as zeros).
 // ---------------------------------------------------------------------------
-constexpr int kPStages = 6;
 constexpr int kPStage = kAStage + 128 * kBKBytes;  // 32 KB
+
+// Shape of the pair kernel per mode.  WGRAD tiles have a K of only the
+// expert's token rows (~2-3 stages) and a 64 KB output per CTA, so they are
+// paced by the epilogue: 8 epilogue warps (two per TMEM lane quarter, 128
+// columns each) and 4 stages; the other modes run 4 epilogue warps and 6 stages.
+template <int MODE>
+struct PairShape {
+    static constexpr int kEpiWarps = MODE == MODE_WGRAD ? 8 : 4;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr int kStages = MODE == MODE_WGRAD ? 4 : 6;
+};
 
 struct PairMaps {
     CUtensorMap a, b0, b1;     // A rows; B rows (FFN1: W_g, W_u; FFN2: W_d twice)
@@ -512,9 +522,11 @@ __device__ __forceinline__ int sf_tile(int x, int y, int64_t rows)
 }
 
 template <int MODE, bool MX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
     k_gemm_pair(const __grid_constant__ PairMaps pm, const GemmArgs a)
 {
+    constexpr int kPStages = PairShape<MODE>::kStages;
+    constexpr int kEpiWarps = PairShape<MODE>::kEpiWarps;
     static_assert(MODE == MODE_FFN1 || MODE == MODE_FFN2 || MODE == MODE_WGRAD, "pair path: FFN1, FFN2, WGRAD");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -544,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 8);
+        mbar_init(acc_empty, 2 * kEpiWarps);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -696,7 +708,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------- epilogue (both CTAs)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
-        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        // 8 epilogue warps: warps 2-5 take columns [0, 128), warps 6-9 [128, 256)
+        const int ecol = kEpiWarps == 8 ? ((warp - 2) >> 2) * 128 : 0;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(ecol);
         const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < total; tile += npairs) {
@@ -716,8 +730,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // dW row (expert e, X row) and 256 columns; zeros for an expert without rows
                 const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
                 uint16_t *dst = a.out_rows + (static_cast<int64_t>(e) * a.m_rows + row_in_e) * a.out_ld +
-                                tl.n_blk * 256;
-                epi_rows_bf16(trow, 256, empty_k, true, dst, stage_out + (warp - 2) * kStageWords, lane, release);
+                                tl.n_blk * 256 + ecol;
+                epi_rows_bf16(trow, 256 / (kEpiWarps / 4), empty_k, true, dst, stage_out + (warp - 2) * kStageWords,
+                              lane, release);
             } else if constexpr (MODE == MODE_FFN1) {
                 const bool valid = row_in_e < a.counts[e];
                 epi_ffn1<MX>(trow, valid, a.pad_offsets[e] + row_in_e, tl.n_blk * 128, a.F, a.h, a.h_scales,
@@ -752,17 +767,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool MX>
+template <int MODE, bool MX>
 constexpr size_t pair_smem_bytes()
 {
-    return 1024 + kPStages * kPStage + (MX ? kPStages * (kSfaBytes + kSfbBytes) : 0) +
-           (2 * kPStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+    constexpr int st = PairShape<MODE>::kStages;
+    return 1024 + st * kPStage + (MX ? st * (kSfaBytes + kSfbBytes) : 0) + (2 * st + 2) * 8 + 16 +
+           (MOK_MAX_EXPERTS + 4) * 4 + PairShape<MODE>::kEpiWarps * kStageWords * 4;
 }
 
 template <int MODE, bool MX>
 cudaError_t launch_gemm_pair(const PairMaps &pm, const GemmArgs &args, cudaStream_t st)
 {
-    constexpr size_t smem = pair_smem_bytes<MX>();
+    constexpr size_t smem = pair_smem_bytes<MODE, MX>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int grid = 0;
@@ -772,7 +788,7 @@ cudaError_t launch_gemm_pair(const PairMaps &pm, const GemmArgs &args, cudaStrea
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(PairShape<MODE>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
