@@ -440,18 +440,19 @@ def main():
     x_host.copy_(inp["x"].cpu())
     out_host = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
-    for _ in range(2):
-        _e2e_step(layer, x_host, out_host)
+    pipe = PipelinedE2E(layer, x_host, out_host)
+    for i in range(2):
+        pipe.step(i)
     torch.cuda.synchronize()
     barrier()
-    t0 = time.perf_counter()
-    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s0.record(stream)
-    for _ in range(e2e_steps):
-        _e2e_step(layer, x_host, out_host)
-    s1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(s0.elapsed_time(s1) / e2e_steps, "cuda")
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        pipe.step(i)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max((time.perf_counter() - t0) * 1e3 / e2e_steps, "cuda")
+    if layer.status() != 0:
+        raise RuntimeError("device status after the end-to-end steps: " + mok.status_string(layer.status()))
     e2e_val = job_throughput(w.T, world, e2e_ms)
 
     base = None
@@ -495,7 +496,10 @@ def main():
                 "value": job_throughput(w.T, world, fb_ms), "unit": "tokens/s", "ms_per_step": fb_ms,
                 "tensor_frac": 3 * flops / (fb_ms / 1e3) / 1e12 / peak_tc},
             "e2e": {"value": e2e_val, "unit": "tokens/s",
-                    "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2},
+                    "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2,
+                    "how": "mok_moe_forward per step from pinned host x to pinned host out; copy-in, "
+                           "layer and copy-out on three streams with two device buffers (host wall "
+                           "time over the steps)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "cpu_baseline": base,
@@ -545,15 +549,51 @@ def _ffn(layer, r):
                    r.row_j, r.ystage, None, None, None, layer.ws)
 
 
-def _e2e_step(layer, x_host, out_host):
-    layer.x.copy_(x_host, non_blocking=True)
-    if len(layer.x_src) > 1:
-        n = len(layer.x_src)
-        rows = layer.x.shape[0] // n
-        for s, buf in enumerate(layer.x_src):
-            buf.copy_(layer.x[s * rows:(s + 1) * rows], non_blocking=True)
-    layer.forward()
-    out_host.copy_(layer.out, non_blocking=True)
+class PipelinedE2E:
+    """End to end through the C ABI from pinned host memory: every step copies
+    its input rows host -> device, runs the layer (mok_moe_forward) and copies
+    its output device -> host.  Three streams (copy in, compute, copy out) and
+    two device input / output buffers let step i+1's upload and step i-1's
+    read-back overlap step i's layer; events order every buffer's reuse."""
+
+    def __init__(self, layer, x_host, out_host):
+        import torch
+        self.layer, self.x_host, self.out_host = layer, x_host, out_host
+        w = layer.w
+        self.s_c = torch.cuda.current_stream()
+        self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        rows = w.T // w.n_sources
+        self.src = [[torch.empty((rows, w.d), dtype=torch.bfloat16, device="cuda") for _ in range(w.n_sources)]
+                    for _ in range(2)]
+        self.rows = rows
+        self.out = [torch.empty_like(layer.out) for _ in range(2)]
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_used = [torch.cuda.Event() for _ in range(2)]
+        self.ev_read = [torch.cuda.Event() for _ in range(2)]
+        self.used = [False, False]
+
+    def step(self, i):
+        import torch
+        from combine_top_routing_gb300 import mok
+        b = i % 2
+        lay = self.layer
+        with torch.cuda.stream(self.s_in):
+            if self.used[b]:
+                self.s_in.wait_event(self.ev_used[b])  # the layer that read this buffer is done
+            for s, buf in enumerate(self.src[b]):
+                buf.copy_(self.x_host[s * self.rows:(s + 1) * self.rows], non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+        self.s_c.wait_event(self.ev_in[b])
+        if self.used[b]:
+            self.s_c.wait_event(self.ev_read[b])  # this output buffer has been read back
+        mok.moe_forward(lay.cfg, self.src[b], lay.W_r, lay.bias, lay.wstruct, self.out[b], None, lay.ws,
+                        stream=self.s_c)
+        self.ev_used[b].record(self.s_c)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.ev_used[b])
+            self.out_host.copy_(self.out[b], non_blocking=True)
+            self.ev_read[b].record(self.s_out)
+        self.used[b] = True
 
 
 if __name__ == "__main__":
