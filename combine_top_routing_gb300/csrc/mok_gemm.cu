@@ -411,6 +411,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t grow = a.pad_offsets[e] + row_in_e;
                 const int f0 = tl.n_blk * BN;
                 uint32_t wa = 0, wb = 0;
+                // the saved a, b of the next 32 columns are loaded while this
+                // chunk is processed (software pipeline over the row's chunks)
+                uint4 na[4], nb[4];
+                if (valid) {
+                    const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + grow * a.F + f0);
+                    const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + grow * a.F + f0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        na[q] = __ldg(pa + q);
+                        nb[q] = __ldg(pb + q);
+                    }
+                }
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32(trow + c, v);
@@ -418,8 +430,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (valid) {
                         const int64_t off = grow * a.F + f0 + c;
                         float av[32], bv[32], da[32], db[32];
-                        load_bf16x32(a.in_a + off, av);
-                        load_bf16x32(a.in_b + off, bv);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t ua[4] = {na[q].x, na[q].y, na[q].z, na[q].w};
+                            const uint32_t ub[4] = {nb[q].x, nb[q].y, nb[q].z, nb[q].w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                av[8 * q + 2 * i] = bf16_bits_to_float(ua[i] & 0xFFFFu);
+                                av[8 * q + 2 * i + 1] = bf16_bits_to_float(ua[i] >> 16);
+                                bv[8 * q + 2 * i] = bf16_bits_to_float(ub[i] & 0xFFFFu);
+                                bv[8 * q + 2 * i + 1] = bf16_bits_to_float(ub[i] >> 16);
+                            }
+                        }
+                        if (c + 32 < BN) {
+                            const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + off + 32);
+                            const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + off + 32);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                na[q] = __ldg(pa + q);
+                                nb[q] = __ldg(pb + q);
+                            }
+                        }
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
                             const float dh = __uint_as_float(v[i]);
