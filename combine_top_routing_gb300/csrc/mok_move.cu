@@ -186,59 +186,68 @@ cudaError_t launch_dispatch_by_token(const Dims &dm, const Sources &src, const i
 
 // ---------------------------------------------------------------------------
 // A6 combine: out[t, c] = bf16( fold_j fmaf(g_tj, y_tj[c], acc) ), acc from 0,
-// j = 0..k-1 in order.  One thread per 8 columns of one token.
+// j = 0..k-1 in order.  One thread per 16 columns of one token; KMAX >= k
+// sizes the register buffer of slot loads.
 // ---------------------------------------------------------------------------
+template <int KMAX>
 __global__ void __launch_bounds__(256) k_combine(const uint16_t *__restrict__ ystage,
                                                  const float *__restrict__ gates, int T, int k,
                                                  int d, uint16_t *__restrict__ out)
 {
-    const int64_t vec_per_tok = d / 8;
+    // two adjacent 8-column vectors per thread: 2k slot loads in flight
+    const int64_t vec_per_tok = d / 16;
     const int64_t n = static_cast<int64_t>(T) * vec_per_tok;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t t = i / vec_per_tok;
-        const int64_t c = i % vec_per_tok;
-        // all k slot loads in flight before the (ordered) accumulation
-        uint4 y[MOK_MAX_TOPK];
-        float g[MOK_MAX_TOPK];
+        const int64_t c = (i % vec_per_tok) * 2;
+        uint4 y[KMAX][2];
+        float g[KMAX];
 #pragma unroll
-        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
             if (j < k) {
                 g[j] = __ldg(gates + t * k + j);
-                y[j] = __ldg(reinterpret_cast<const uint4 *>(ystage + (t * k + j) * d) + c);
+                const uint4 *row = reinterpret_cast<const uint4 *>(ystage + (t * k + j) * d) + c;
+                y[j][0] = __ldg(row);
+                y[j][1] = __ldg(row + 1);
             }
         }
-        float acc[8];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        for (int h = 0; h < 2; ++h) {
+            float acc[8];
 #pragma unroll
-        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
-            if (j < k) {
-                const uint32_t w[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    acc[2 * q] = fmaf(g[j], bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
-                    acc[2 * q + 1] = fmaf(g[j], bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
+            for (int j = 0; j < KMAX; ++j) {
+                if (j < k) {
+                    const uint32_t w[4] = {y[j][h].x, y[j][h].y, y[j][h].z, y[j][h].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = fmaf(g[j], bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
+                        acc[2 * q + 1] = fmaf(g[j], bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
+                    }
                 }
             }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            reinterpret_cast<uint4 *>(out + t * d)[c + h] = o;
         }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        reinterpret_cast<uint4 *>(out + t * d)[c] = o;
     }
 }
 
 cudaError_t launch_combine(const Dims &dm, const uint16_t *ystage, const float *gates,
                            uint16_t *out, cudaStream_t st)
 {
-    const int64_t n = static_cast<int64_t>(dm.T) * (dm.d / 8);
+    const int64_t n = static_cast<int64_t>(dm.T) * (dm.d / 16);
     const int threads = 256;
     const int64_t need = (n + threads - 1) / threads;
     const int blocks = static_cast<int>(need < 64 * num_sms() ? need : 64 * num_sms());
-    k_combine<<<blocks, threads, 0, st>>>(ystage, gates, dm.T, dm.k, dm.d, out);
+    if (dm.k <= 2) k_combine<2><<<blocks, threads, 0, st>>>(ystage, gates, dm.T, dm.k, dm.d, out);
+    else if (dm.k <= 4) k_combine<4><<<blocks, threads, 0, st>>>(ystage, gates, dm.T, dm.k, dm.d, out);
+    else k_combine<MOK_MAX_TOPK><<<blocks, threads, 0, st>>>(ystage, gates, dm.T, dm.k, dm.d, out);
     return cudaGetLastError();
 }
 
