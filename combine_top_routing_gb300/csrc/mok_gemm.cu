@@ -544,6 +544,17 @@ struct PairShape {
 struct PairMaps {
     CUtensorMap a, b0, b1;     // A rows; B rows (FFN1: W_g, W_u; FFN2: W_d twice)
     CUtensorMap sa, sb0, sb1;  // scale tiles of A and of B (MXFP8 only)
+    CUtensorMap out;           // WGRAD: dW [E * m_rows, N] BF16, 32-row x 64-column boxes
+};
+
+// WGRAD epilogue: every epilogue warp owns 32 dW rows x (256 / (warps / 4))
+// columns per tile, stored through shared-memory boxes of 32 x 64 BF16 (4 KB,
+// 128-byte swizzled) by TMA.
+template <int MODE>
+struct PairOut {
+    static constexpr int kCols = MODE == MODE_WGRAD ? 256 / (PairShape<MODE>::kEpiWarps / 4) : 0;
+    static constexpr int kBoxes = kCols / 64;
+    static constexpr int kWarpBytes = kBoxes * 4096;
 };
 
 // index of the scale tile of (k element x, row y) in a [rows, K] matrix
@@ -563,7 +574,8 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sT = smem;  // stage s: A at s*32K, B half at s*32K + 16K
-    uint8_t *sSF = sT + kPStages * kPStage;
+    uint8_t *sOut = sT + kPStages * kPStage;  // WGRAD output boxes (1024-byte aligned)
+    uint8_t *sSF = sOut + kEpiWarps * PairOut<MODE>::kWarpBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kPStages * (kSfaBytes + kSfbBytes) : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + kPStages;
@@ -758,12 +770,34 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
             const int e = tl.group;
             const int row_in_e = (2 * tl.m_blk + static_cast<int>(rank)) * kBM + r;
             if constexpr (MODE == MODE_WGRAD) {
-                // dW row (expert e, X row) and 256 columns; zeros for an expert without rows
+                // dW rows (expert e) x this warp's columns; zeros for an expert without rows.
+                // The accumulator is released once it is in registers; the rows go to this
+                // warp's boxes (lane = row, 16-byte chunk c of a 128-byte box row at
+                // c ^ (row & 7): the SWIZZLE_128B layout) and leave by TMA stores.
+                constexpr int kCols = PairOut<MODE>::kCols;
                 const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
-                uint16_t *dst = a.out_rows + (static_cast<int64_t>(e) * a.m_rows + row_in_e) * a.out_ld +
-                                tl.n_blk * 256 + ecol;
-                epi_rows_bf16(trow, 256 / (kEpiWarps / 4), empty_k, true, dst, stage_out + (warp - 2) * kStageWords,
-                              lane, release);
+                uint32_t pk[128];
+                drain_row_bf16(trow, kCols, empty_k, pk);
+                release();
+                uint8_t *box = sOut + (warp - 2) * PairOut<MODE>::kWarpBytes;
+                if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's boxes have been read
+                __syncwarp();
+                const uint32_t rbase = smem_u32(box) + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                for (int bx = 0; bx < PairOut<MODE>::kBoxes; ++bx)
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(rbase + bx * 4096 + ((c ^ (lane & 7)) << 4), pk[bx * 32 + 4 * c],
+                                     pk[bx * 32 + 4 * c + 1], pk[bx * 32 + 4 * c + 2], pk[bx * 32 + 4 * c + 3]);
+                fence_proxy_async_shared();
+                __syncwarp();
+                if (lane == 0) {
+                    const int x = tl.n_blk * 256 + ecol;
+                    const int y = e * a.m_rows + (2 * tl.m_blk + static_cast<int>(rank)) * kBM + quarter * 32;
+#pragma unroll
+                    for (int bx = 0; bx < PairOut<MODE>::kBoxes; ++bx) tma_store_2d(&pm.out, box + bx * 4096, x + 64 * bx, y);
+                    bulk_commit_group();
+                }
             } else if constexpr (MODE == MODE_FFN1) {
                 const bool valid = row_in_e < a.counts[e];
                 epi_ffn1<MX>(trow, valid, a.pad_offsets[e] + row_in_e, tl.n_blk * 128, a.F, a.h, a.h_scales,
@@ -782,6 +816,10 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
             }
             if (!released) release();
             acc_phase ^= 1u;
+        }
+        if constexpr (MODE == MODE_WGRAD) {
+            if (lane == 0) bulk_wait_group<0>();  // this warp's dW stores are complete
+            __syncwarp();
         }
     }
 
@@ -802,8 +840,9 @@ template <int MODE, bool MX>
 constexpr size_t pair_smem_bytes()
 {
     constexpr int st = PairShape<MODE>::kStages;
-    return 1024 + st * kPStage + (MX ? st * (kSfaBytes + kSfbBytes) : 0) + (2 * st + 2) * 8 + 16 +
-           (MOK_MAX_EXPERTS + 4) * 4 + PairShape<MODE>::kEpiWarps * kStageWords * 4;
+    constexpr int ew = PairShape<MODE>::kEpiWarps;
+    return 1024 + st * kPStage + ew * PairOut<MODE>::kWarpBytes + (MX ? st * (kSfaBytes + kSfbBytes) : 0) +
+           (2 * st + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + (MODE == MODE_WGRAD ? 0 : ew * kStageWords * 4);
 }
 
 template <int MODE, bool MX>
@@ -1133,6 +1172,9 @@ cudaError_t launch_wgrad(const Dims &dm, const void *A_T, const uint32_t *A_s, i
             return cudaErrorInvalidValue;
         pm.sb1 = pm.sb0;
         if (!mx) pm.sa = pm.sb0 = pm.sb1 = bm;  // unused
+        if (encode_tmap_2d(&pm.out, dW, false, static_cast<uint64_t>(b_rows),
+                           static_cast<uint64_t>(dm.E) * static_cast<uint64_t>(a_rows), 64, 32))
+            return cudaErrorInvalidValue;
         g.BN = 256;
         g.n_tiles = static_cast<int>(b_rows / 256);
         g.m_rows = static_cast<int>(a_rows);
