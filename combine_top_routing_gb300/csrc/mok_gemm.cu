@@ -538,7 +538,7 @@ template <int MODE>
 struct PairShape {
     static constexpr int kEpiWarps = MODE == MODE_WGRAD ? 8 : 4;
     static constexpr int kThreads = 64 + 32 * kEpiWarps;
-    static constexpr int kStages = MODE == MODE_WGRAD ? 4 : 6;
+    static constexpr int kStages = MODE == MODE_WGRAD ? 5 : 6;
 };
 
 struct PairMaps {
@@ -548,13 +548,13 @@ struct PairMaps {
 };
 
 // WGRAD epilogue: every epilogue warp owns 32 dW rows x (256 / (warps / 4))
-// columns per tile, stored through shared-memory boxes of 32 x 64 BF16 (4 KB,
-// 128-byte swizzled) by TMA.
+// columns per tile, stored 64 columns at a time through one shared-memory box
+// of 32 x 64 BF16 (4 KB, 128-byte swizzled) by TMA.
 template <int MODE>
 struct PairOut {
     static constexpr int kCols = MODE == MODE_WGRAD ? 256 / (PairShape<MODE>::kEpiWarps / 4) : 0;
     static constexpr int kBoxes = kCols / 64;
-    static constexpr int kWarpBytes = kBoxes * 4096;
+    static constexpr int kWarpBytes = MODE == MODE_WGRAD ? 4096 : 0;
 };
 
 // index of the scale tile of (k element x, row y) in a [rows, K] matrix
@@ -780,23 +780,23 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
                 drain_row_bf16(trow, kCols, empty_k, pk);
                 release();
                 uint8_t *box = sOut + (warp - 2) * PairOut<MODE>::kWarpBytes;
-                if (lane == 0) bulk_wait_group_read<0>();  // the previous tile's boxes have been read
-                __syncwarp();
                 const uint32_t rbase = smem_u32(box) + static_cast<uint32_t>(lane) * 128u;
+                const int x = tl.n_blk * 256 + ecol;
+                const int y = e * a.m_rows + (2 * tl.m_blk + static_cast<int>(rank)) * kBM + quarter * 32;
 #pragma unroll
-                for (int bx = 0; bx < PairOut<MODE>::kBoxes; ++bx)
+                for (int bx = 0; bx < PairOut<MODE>::kBoxes; ++bx) {
+                    if (lane == 0) bulk_wait_group_read<0>();  // the box's previous store has read it
+                    __syncwarp();
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        st_shared_v4(rbase + bx * 4096 + ((c ^ (lane & 7)) << 4), pk[bx * 32 + 4 * c],
-                                     pk[bx * 32 + 4 * c + 1], pk[bx * 32 + 4 * c + 2], pk[bx * 32 + 4 * c + 3]);
-                fence_proxy_async_shared();
-                __syncwarp();
-                if (lane == 0) {
-                    const int x = tl.n_blk * 256 + ecol;
-                    const int y = e * a.m_rows + (2 * tl.m_blk + static_cast<int>(rank)) * kBM + quarter * 32;
-#pragma unroll
-                    for (int bx = 0; bx < PairOut<MODE>::kBoxes; ++bx) tma_store_2d(&pm.out, box + bx * 4096, x + 64 * bx, y);
-                    bulk_commit_group();
+                        st_shared_v4(rbase + ((c ^ (lane & 7)) << 4), pk[bx * 32 + 4 * c], pk[bx * 32 + 4 * c + 1],
+                                     pk[bx * 32 + 4 * c + 2], pk[bx * 32 + 4 * c + 3]);
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&pm.out, box, x + 64 * bx, y);
+                        bulk_commit_group();
+                    }
                 }
             } else if constexpr (MODE == MODE_FFN1) {
                 const bool valid = row_in_e < a.counts[e];
