@@ -584,7 +584,8 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(acc_empty + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
     int *prefix = reinterpret_cast<int *>(tmem_holder + 4);
-    uint32_t *stage_out = reinterpret_cast<uint32_t *>(prefix + MOK_MAX_EXPERTS + 4);
+    uint32_t *stage_out = reinterpret_cast<uint32_t *>(prefix + MOK_MAX_EXPERTS + 4);  // FFN epilogues
+    int *s_pad = prefix + MOK_MAX_EXPERTS + 4;  // WGRAD: the experts' K ranges (pad_offsets)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -640,6 +641,8 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
             run += pair_tiles(g);
         }
         if (lane == 31) prefix[groups] = incl;
+        if constexpr (MODE == MODE_WGRAD)
+            for (int g = lane; g <= groups; g += 32) s_pad[g] = a.pad_offsets[g];
     }
     tc_fence_before();
     __syncthreads();
@@ -649,6 +652,28 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
     constexpr int kE = MX ? 128 : 64;
     // bytes one CTA lands per stage; the even CTA's barrier counts both CTAs'
     const uint32_t cta_bytes = kPStage + (MX ? kSfaBytes + kSfbBytes : 0);
+    // Tile and K stages of a tile index.  WGRAD: every expert has the same
+    // (X / 256) x (Y / 256) tiles, so the expert is one division away and its K
+    // range sits in shared memory (a few stages per tile leave no room for a
+    // global load on the issue path).
+    const int wmt = MODE == MODE_WGRAD ? a.m_rows / (2 * kBM) : 1;
+    const int wper = wmt * a.n_tiles;
+    auto locate = [&](int tile) {
+        Tile t;
+        if constexpr (MODE == MODE_WGRAD) {
+            t.group = tile / wper;
+            const int local = tile - t.group * wper;
+            t.n_blk = local / wmt;
+            t.m_blk = local - t.n_blk * wmt;
+        } else {
+            t = decode_tile(tile, prefix, groups, a.n_tiles);
+        }
+        return t;
+    };
+    auto k_stages_of = [&](int g) {
+        if constexpr (MODE == MODE_WGRAD) return (s_pad[g + 1] - s_pad[g]) / kE;
+        else return a.k_stages;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -656,11 +681,11 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
             uint32_t stage = 0, phase = 0;
             const uint32_t full0 = mapa_shared(smem_u32(full), 0);
             for (int tile = pair; tile < total; tile += npairs) {
-                const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
+                const Tile tl = locate(tile);
                 const int g = tl.group;
-                const int kst = tile_k_stages<MODE, MX>(a, g);
+                const int kst = k_stages_of(g);
                 // WGRAD: A rows over X, B rows over Y, K along the expert's token rows
-                const int x0 = MODE == MODE_WGRAD ? a.pad_offsets[g] : 0;
+                const int x0 = MODE == MODE_WGRAD ? s_pad[g] : 0;
                 const int ya = MODE == MODE_WGRAD ? (2 * tl.m_blk + static_cast<int>(rank)) * kBM
                                                   : a.pad_offsets[g] + (2 * tl.m_blk + static_cast<int>(rank)) * kBM;
                 int yb, ysf;
@@ -712,7 +737,7 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             const uint32_t idesc = idesc_bf16(2 * kBM, 256);
             for (int tile = pair; tile < total; tile += npairs) {
-                const int kst = tile_k_stages<MODE, MX>(a, decode_tile(tile, prefix, groups, a.n_tiles).group);
+                const int kst = k_stages_of(locate(tile).group);
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kst; ++ks) {
@@ -757,7 +782,7 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
         const uint32_t acc_empty_leader = mapa_shared(smem_u32(acc_empty), 0);
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < total; tile += npairs) {
-            const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
+            const Tile tl = locate(tile);
             if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
             tc_fence_after();
             bool released = false;
@@ -775,7 +800,7 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
                 // warp's boxes (lane = row, 16-byte chunk c of a 128-byte box row at
                 // c ^ (row & 7): the SWIZZLE_128B layout) and leave by TMA stores.
                 constexpr int kCols = PairOut<MODE>::kCols;
-                const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
+                const bool empty_k = s_pad[e + 1] == s_pad[e];
                 uint32_t pk[128];
                 drain_row_bf16(trow, kCols, empty_k, pk);
                 release();
@@ -842,7 +867,8 @@ constexpr size_t pair_smem_bytes()
     constexpr int st = PairShape<MODE>::kStages;
     constexpr int ew = PairShape<MODE>::kEpiWarps;
     return 1024 + st * kPStage + ew * PairOut<MODE>::kWarpBytes + (MX ? st * (kSfaBytes + kSfbBytes) : 0) +
-           (2 * st + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + (MODE == MODE_WGRAD ? 0 : ew * kStageWords * 4);
+           (2 * st + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 +
+           (MODE == MODE_WGRAD ? (MOK_MAX_EXPERTS + 4) * 4 : ew * kStageWords * 4);
 }
 
 template <int MODE, bool MX>
