@@ -120,72 +120,97 @@ __global__ void __launch_bounds__(256) k_rev_combine(
 // holds (x via the sources) instead of from a row buffer.
 // ---------------------------------------------------------------------------
 template <bool MX, bool GATHER>
-__global__ void __launch_bounds__(256) k_transpose_rows(
+__global__ void __launch_bounds__(256, 3) k_transpose_rows(
     const uint16_t *__restrict__ in, Sources src, int C, int E, const int32_t *__restrict__ counts,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ pad_offsets,
-    const int32_t *__restrict__ row_tok, int64_t rows_pad, void *out, uint32_t *__restrict__ out_s)
+    const int32_t *__restrict__ row_tok, int64_t rows_pad, void *out, uint32_t *__restrict__ out_s,
+    int col_tiles)
 {
-    // A 256-row x 64-column tile: every row read is one 128-byte line, held
-    // transposed in shared memory as 64 rows of 256 tokens whose 8-token chunks
-    // are XOR-swizzled by the row (chunk t/8 of column c at chunk (t/8) ^ (c % 32)),
-    // so that the transposing writes and the 16-byte row reads stay near
-    // conflict-free.
-    __shared__ __align__(16) uint16_t tile[64][256];
+    // A 256-row tile and col_tiles 64-column tiles of it, one after the other.
+    // Every row read is one 128-byte line.  A thread holds 8 columns of two
+    // adjacent rows and writes them transposed as 32-bit (row 2p, row 2p + 1)
+    // pairs: shared word (c, p) sits at c * 128 + (p ^ 4 * ((c / 8) % 8)), so
+    // that the 32 lanes of a transposing store (4 row pairs x 8 column groups)
+    // and of a 16-byte read along one column (32 aligned groups of 4 pairs)
+    // each hit 32 different banks.  The next column tile's loads are in flight
+    // while this one is written.
+    __shared__ __align__(16) uint32_t tileT[64][128];
     __shared__ const uint16_t *s_row[256];
+    __shared__ int s_seg[2];
     const int64_t q0 = static_cast<int64_t>(blockIdx.y) * 256;
-    const int c0 = blockIdx.x * 64;
     const int64_t pad_end = pad_offsets[E];
     if (q0 >= pad_end) return;  // beyond the last expert segment: never read
+    // The expert segments holding rows q0 and q0 + 128: segments start on
+    // 128-row boundaries, so each 128-row half lies in one.  One round of loads,
+    // every thread testing a few experts, instead of a binary search per row.
+    if (threadIdx.x < 2) s_seg[threadIdx.x] = -1;
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int lo = pad_offsets[e], hi = pad_offsets[e + 1];
+        if (lo <= q0 && q0 < hi) s_seg[0] = e;
+        if (lo <= q0 + 128 && q0 + 128 < hi) s_seg[1] = e;
+    }
+    __syncthreads();
     {
         // source row of padded row q0 + threadIdx.x (null: padding, reads as zeros)
         const int64_t q = q0 + threadIdx.x;
+        const int e = s_seg[threadIdx.x >> 7];
         const uint16_t *row = nullptr;
-        if (q < pad_end) {
-            int lo = 0, hi = E;  // expert segment holding q
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (pad_offsets[mid] <= q) lo = mid;
-                else hi = mid;
-            }
-            const int64_t local = q - pad_offsets[lo];
-            if (local < counts[lo]) {
-                if (GATHER) row = source_row(src, row_tok[offsets[lo] + local], C);
+        if (e >= 0) {
+            const int64_t local = q - pad_offsets[e];
+            if (local < counts[e]) {
+                if (GATHER) row = source_row(src, row_tok[offsets[e] + local], C);
                 else row = in + q * C;
             }
         }
         s_row[threadIdx.x] = row;
     }
     __syncthreads();
-    // 8 threads per row (16 bytes each), 32 rows per pass, all 8 passes in flight
-    const int cc = (threadIdx.x & 7) * 8;
-    uint4 v[8];
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const uint16_t *row = s_row[p * 32 + (threadIdx.x >> 3)];
-        v[p] = row ? __ldg(reinterpret_cast<const uint4 *>(row + c0 + cc)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int r = p * 32 + (threadIdx.x >> 3);
-        const uint32_t w[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
-#pragma unroll
-        for (int q2 = 0; q2 < 4; ++q2) {
-            const int c = cc + 2 * q2;
-            tile[c][(((r >> 3) ^ (c & 31)) << 3) | (r & 7)] = static_cast<uint16_t>(w[q2] & 0xFFFFu);
-            tile[c + 1][(((r >> 3) ^ ((c + 1) & 31)) << 3) | (r & 7)] = static_cast<uint16_t>(w[q2] >> 16);
-        }
-    }
-    __syncthreads();
+    // 8 threads per row pair (16 bytes of each row), 32 row pairs per pass, all
+    // 4 passes (8 rows of 16 bytes) in flight
+    const int cg = threadIdx.x & 7;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int oc = warp; oc < 64; oc += blockDim.x >> 5) {
-        const int64_t orow = c0 + oc;
-        const uint4 raw = *reinterpret_cast<const uint4 *>(&tile[oc][(lane ^ (oc & 31)) << 3]);
-        if (MX) {
-            mx_quant_stretch(raw, lane, 32, static_cast<uint8_t *>(out) + orow * rows_pad, q0, out_s,
-                             orow, C);
-        } else {
-            reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + orow * rows_pad + q0)[lane] = raw;
+    const int ct0 = blockIdx.x * col_tiles;
+    const int nct = min(col_tiles, C / 64 - ct0);
+    uint4 v[8];
+    auto load = [&](int c0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rp = i * 32 + (threadIdx.x >> 3);
+            const uint16_t *r0 = s_row[2 * rp], *r1 = s_row[2 * rp + 1];
+            v[2 * i] = r0 ? __ldg(reinterpret_cast<const uint4 *>(r0 + c0 + cg * 8)) : make_uint4(0, 0, 0, 0);
+            v[2 * i + 1] = r1 ? __ldg(reinterpret_cast<const uint4 *>(r1 + c0 + cg * 8)) : make_uint4(0, 0, 0, 0);
         }
+    };
+    load(ct0 * 64);
+    for (int t = 0; t < nct; ++t) {
+        const int c0 = (ct0 + t) * 64;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int rp = i * 32 + (threadIdx.x >> 3);
+            const uint32_t a[4] = {v[2 * i].x, v[2 * i].y, v[2 * i].z, v[2 * i].w};
+            const uint32_t b[4] = {v[2 * i + 1].x, v[2 * i + 1].y, v[2 * i + 1].z, v[2 * i + 1].w};
+            const int sw = rp ^ (4 * cg);  // (c / 8) % 8 == cg for the thread's 8 columns
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = cg * 8 + 2 * j;
+                tileT[c][sw] = (a[j] & 0xFFFFu) | (b[j] << 16);
+                tileT[c + 1][sw] = (a[j] >> 16) | (b[j] & 0xFFFF0000u);
+            }
+        }
+        __syncthreads();
+        if (t + 1 < nct) load(c0 + 64);
+        for (int oc = warp; oc < 64; oc += blockDim.x >> 5) {
+            const int64_t orow = c0 + oc;
+            const uint4 raw = *reinterpret_cast<const uint4 *>(&tileT[oc][4 * (lane ^ ((oc >> 3) & 7))]);
+            if (MX) {
+                mx_quant_stretch(raw, lane, 32, static_cast<uint8_t *>(out) + orow * rows_pad, q0, out_s,
+                                 orow, C);
+            } else {
+                reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + orow * rows_pad + q0)[lane] = raw;
+            }
+        }
+        __syncthreads();
     }
 }
 
@@ -309,22 +334,23 @@ cudaError_t launch_transpose_rows(const Dims &dm, const uint16_t *in, const Sour
                                   const int32_t *pad_offsets, const int32_t *row_tok, void *out,
                                   uint32_t *out_s, cudaStream_t st)
 {
-    dim3 grid(static_cast<unsigned>(C / 64), static_cast<unsigned>(dm.rows_pad / 256));
+    constexpr int kColTiles = 4;  // 64-column tiles per block (the row segments found once)
+    dim3 grid(static_cast<unsigned>((C / 64 + kColTiles - 1) / kColTiles), static_cast<unsigned>(dm.rows_pad / 256));
     const bool mx = dm.dtype == MOK_MXFP8;
     Sources empty_src = {};
     const Sources &s = src ? *src : empty_src;
     if (mx && src)
         k_transpose_rows<true, true><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets, pad_offsets,
-                                                          row_tok, dm.rows_pad, out, out_s);
+                                                          row_tok, dm.rows_pad, out, out_s, kColTiles);
     else if (mx)
         k_transpose_rows<true, false><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets, pad_offsets,
-                                                           row_tok, dm.rows_pad, out, out_s);
+                                                           row_tok, dm.rows_pad, out, out_s, kColTiles);
     else if (src)
         k_transpose_rows<false, true><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets, pad_offsets,
-                                                           row_tok, dm.rows_pad, out, out_s);
+                                                           row_tok, dm.rows_pad, out, out_s, kColTiles);
     else
         k_transpose_rows<false, false><<<grid, 256, 0, st>>>(in, s, C, dm.E, counts, offsets,
-                                                            pad_offsets, row_tok, dm.rows_pad, out, out_s);
+                                                            pad_offsets, row_tok, dm.rows_pad, out, out_s, kColTiles);
     return cudaGetLastError();
 }
 
