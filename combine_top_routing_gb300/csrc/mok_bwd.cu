@@ -49,55 +49,78 @@ __global__ void __launch_bounds__(256) k_rev_combine(
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     const uint4 *dyrow = reinterpret_cast<const uint4 *>(dY + static_cast<int64_t>(t) * d);
-    float dg[MOK_MAX_TOPK];
-    for (int j = 0; j < k; ++j) {
-        const int64_t i = static_cast<int64_t>(t) * k + j;
-        const float g = gates[i];
-        const int64_t q = slot_row(ids, slot_pos, offsets, pad_offsets, i);
-        const uint4 *yrow = reinterpret_cast<const uint4 *>(ystage + i * d);
-        float dot = 0.0f;
-        for (int c0 = 0; c0 < d; c0 += 256) {
-            const int nvalid = d - c0 >= 256 ? 32 : 16;
+    // one pass over the columns: the token's dY chunk is read once and the k
+    // slot rows' chunks are all in flight before they are used; the dot
+    // products run per slot over the columns in order, as before
+    float dg[MOK_MAX_TOPK], g[MOK_MAX_TOPK];
+    int64_t q[MOK_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+        dg[j] = 0.0f;
+        if (j < k) {
+            const int64_t i = static_cast<int64_t>(t) * k + j;
+            g[j] = gates[i];
+            q[j] = slot_row(ids, slot_pos, offsets, pad_offsets, i);
+        }
+    }
+    for (int c0 = 0; c0 < d; c0 += 256) {
+        const int nvalid = d - c0 >= 256 ? 32 : 16;
+        uint4 a = make_uint4(0, 0, 0, 0), y[MOK_MAX_TOPK];
+        if (lane < nvalid) a = __ldg(dyrow + (c0 >> 3) + lane);
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j)
+            if (j < k && lane < nvalid)
+                y[j] = __ldg(reinterpret_cast<const uint4 *>(ystage + (static_cast<int64_t>(t) * k + j) * d) +
+                             (c0 >> 3) + lane);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j >= k) break;
             uint4 out = make_uint4(0, 0, 0, 0);
             if (lane < nvalid) {
-                const uint4 a = __ldg(dyrow + (c0 >> 3) + lane);
-                const uint4 y = __ldg(yrow + (c0 >> 3) + lane);
-                const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-                const uint32_t yv[4] = {y.x, y.y, y.z, y.w};
+                const uint32_t yv[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
                 uint32_t ov[4];
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                     const float d0 = bf16_bits_to_float(av[q2] & 0xFFFFu);
                     const float d1 = bf16_bits_to_float(av[q2] >> 16);
-                    dot = fmaf(d0, bf16_bits_to_float(yv[q2] & 0xFFFFu), dot);
-                    dot = fmaf(d1, bf16_bits_to_float(yv[q2] >> 16), dot);
-                    ov[q2] = pack_bf16x2(g * d0, g * d1);
+                    dg[j] = fmaf(d0, bf16_bits_to_float(yv[q2] & 0xFFFFu), dg[j]);
+                    dg[j] = fmaf(d1, bf16_bits_to_float(yv[q2] >> 16), dg[j]);
+                    ov[q2] = pack_bf16x2(g[j] * d0, g[j] * d1);
                 }
                 out = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-                reinterpret_cast<uint4 *>(dy_rows + q * d)[(c0 >> 3) + lane] = out;
+                reinterpret_cast<uint4 *>(dy_rows + q[j] * d)[(c0 >> 3) + lane] = out;
             }
-            if (MX) mx_quant_stretch(out, lane, nvalid, dy_q + q * d, c0, dy_s, q, rows_pad);
+            if (MX) mx_quant_stretch(out, lane, nvalid, dy_q + q[j] * d, c0, dy_s, q[j], rows_pad);
         }
+    }
 #pragma unroll
-        for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        dg[j] = dot;
+    for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+        if (j >= k) break;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) dg[j] += __shfl_xor_sync(0xffffffffu, dg[j], o);
     }
     // gradients through the renormalised top-k gates to the chosen logits
+    // (loops unrolled to the bound on k, so that the per-slot values stay in registers)
     float G = 0.0f, ssum = 0.0f;
-    for (int j = 0; j < k; ++j) {
-        G += dg[j] * gates[static_cast<int64_t>(t) * k + j];
+#pragma unroll
+    for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+        if (j >= k) break;
+        G += dg[j] * g[j];
         ssum += sel_scores[static_cast<int64_t>(t) * k + j];
     }
     float dl[MOK_MAX_TOPK];
     int sel[MOK_MAX_TOPK];
-    for (int j = 0; j < k; ++j) {
+#pragma unroll
+    for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+        if (j >= k) break;
         const int64_t i = static_cast<int64_t>(t) * k + j;
         sel[j] = ids[i];
         if (kind == MOK_ROUTER_SOFTMAX) {
-            dl[j] = gates[i] * (dg[j] - G);
+            dl[j] = g[j] * (dg[j] - G);
         } else {
-            const float s = sel_scores[i];
-            dl[j] = (dg[j] - G) / ssum * s * (1.0f - s);
+            const float sc = sel_scores[i];
+            dl[j] = (dg[j] - G) / ssum * sc * (1.0f - sc);
         }
         if (lane == 0) {
             dgates[i] = dg[j];
@@ -107,8 +130,9 @@ __global__ void __launch_bounds__(256) k_rev_combine(
     if (dlogits) {
         for (int e = lane; e < E; e += 32) {
             float v = 0.0f;
-            for (int j = 0; j < k; ++j)
-                if (sel[j] == e) v = dl[j];
+#pragma unroll
+            for (int j = 0; j < MOK_MAX_TOPK; ++j)
+                if (j < k && sel[j] == e) v = dl[j];
             dlogits[static_cast<int64_t>(t) * E + e] = v;
         }
     }
@@ -227,33 +251,51 @@ __global__ void __launch_bounds__(256) k_rev_dispatch(
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
+    // the token's slot rows and router terms (k values, registers)
+    int64_t q[MOK_MAX_TOPK];
+    float dl[MOK_MAX_TOPK];
+    int eid[MOK_MAX_TOPK];
+#pragma unroll
+    for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+        if (j < k) {
+            const int64_t i = static_cast<int64_t>(t) * k + j;
+            q[j] = slot_row(ids, slot_pos, offsets, pad_offsets, i);
+            dl[j] = dl_sel[i];
+            eid[j] = ids[i];
+        }
+    }
     for (int c0 = lane * 8; c0 < d; c0 += 256) {
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int64_t q = slot_row(ids, slot_pos, offsets, pad_offsets, static_cast<int64_t>(t) * k + j);
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(dx_rows + q * d + c0));
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        // all k slot-row loads in flight, then the sums in j order
+        uint4 v[MOK_MAX_TOPK];
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j)
+            if (j < k) v[j] = __ldg(reinterpret_cast<const uint4 *>(dx_rows + q[j] * d + c0));
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j >= k) break;
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 acc[2 * i] += bf16_bits_to_float(w[i] & 0xFFFFu);
                 acc[2 * i + 1] += bf16_bits_to_float(w[i] >> 16);
             }
         }
-        for (int j = 0; j < k; ++j) {
-            const int64_t i = static_cast<int64_t>(t) * k + j;
-            const float dl = dl_sel[i];
-            const float4 *wr = reinterpret_cast<const float4 *>(W_r + static_cast<int64_t>(ids[i]) * d + c0);
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j >= k) break;
+            const float4 *wr = reinterpret_cast<const float4 *>(W_r + static_cast<int64_t>(eid[j]) * d + c0);
             const float4 w0 = __ldg(wr), w1 = __ldg(wr + 1);
-            acc[0] = fmaf(dl, w0.x, acc[0]);
-            acc[1] = fmaf(dl, w0.y, acc[1]);
-            acc[2] = fmaf(dl, w0.z, acc[2]);
-            acc[3] = fmaf(dl, w0.w, acc[3]);
-            acc[4] = fmaf(dl, w1.x, acc[4]);
-            acc[5] = fmaf(dl, w1.y, acc[5]);
-            acc[6] = fmaf(dl, w1.z, acc[6]);
-            acc[7] = fmaf(dl, w1.w, acc[7]);
+            acc[0] = fmaf(dl[j], w0.x, acc[0]);
+            acc[1] = fmaf(dl[j], w0.y, acc[1]);
+            acc[2] = fmaf(dl[j], w0.z, acc[2]);
+            acc[3] = fmaf(dl[j], w0.w, acc[3]);
+            acc[4] = fmaf(dl[j], w1.x, acc[4]);
+            acc[5] = fmaf(dl[j], w1.y, acc[5]);
+            acc[6] = fmaf(dl[j], w1.z, acc[6]);
+            acc[7] = fmaf(dl[j], w1.w, acc[7]);
         }
         uint4 o;
         o.x = pack_bf16x2(acc[0], acc[1]);
@@ -266,23 +308,52 @@ __global__ void __launch_bounds__(256) k_rev_dispatch(
 
 // ---------------------------------------------------------------------------
 // B6: dW_r[e, c] = sum over e's dense rows p (in order) of dl(p) x[t(p), c].
-// Block (column chunk of 256, expert e); thread per column.
+// Block (512 columns, expert e); two columns per thread.  The rows' source
+// pointers and dl values are staged 256 rows at a time in shared memory, so
+// that the x loads of 8 rows are in flight at once instead of one row's
+// chain of dependent loads (row -> token -> dl -> x) at a time.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_router_wgrad(
     Sources src, int d, int k, const int32_t *__restrict__ offsets,
     const int32_t *__restrict__ row_tok, const uint8_t *__restrict__ row_j,
     const float *__restrict__ dl_sel, float *__restrict__ dW_r)
 {
+    __shared__ const uint16_t *s_x[256];
+    __shared__ float s_dl[256];
     const int e = blockIdx.y;
-    const int c = blockIdx.x * 256 + threadIdx.x;
+    const int c = (blockIdx.x * 256 + threadIdx.x) * 2;
     const int p0 = offsets[e], p1 = offsets[e + 1];
-    float acc = 0.0f;
-    for (int p = p0; p < p1; ++p) {
-        const int t = row_tok[p];
-        const float dl = dl_sel[static_cast<int64_t>(t) * k + row_j[p]];
-        if (c < d) acc = fmaf(dl, bf16_bits_to_float(source_row(src, t, d)[c]), acc);
+    float acc0 = 0.0f, acc1 = 0.0f;
+    for (int pc = p0; pc < p1; pc += 256) {
+        const int n = min(256, p1 - pc);
+        __syncthreads();  // the previous chunk's rows are consumed
+        if (threadIdx.x < n) {
+            const int p = pc + threadIdx.x;
+            const int t = row_tok[p];
+            s_dl[threadIdx.x] = dl_sel[static_cast<int64_t>(t) * k + row_j[p]];
+            s_x[threadIdx.x] = source_row(src, t, d);
+        }
+        __syncthreads();
+        if (c < d) {
+            int r = 0;
+            for (; r + 8 <= n; r += 8) {
+                uint32_t xv[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) xv[u] = __ldg(reinterpret_cast<const uint32_t *>(s_x[r + u] + c));
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    acc0 = fmaf(s_dl[r + u], bf16_bits_to_float(xv[u] & 0xFFFFu), acc0);
+                    acc1 = fmaf(s_dl[r + u], bf16_bits_to_float(xv[u] >> 16), acc1);
+                }
+            }
+            for (; r < n; ++r) {
+                const uint32_t xv = __ldg(reinterpret_cast<const uint32_t *>(s_x[r] + c));
+                acc0 = fmaf(s_dl[r], bf16_bits_to_float(xv & 0xFFFFu), acc0);
+                acc1 = fmaf(s_dl[r], bf16_bits_to_float(xv >> 16), acc1);
+            }
+        }
     }
-    if (c < d) dW_r[static_cast<int64_t>(e) * d + c] = acc;
+    if (c < d) *reinterpret_cast<float2 *>(dW_r + static_cast<int64_t>(e) * d + c) = make_float2(acc0, acc1);
 }
 
 // ---------------------------------------------------------------------------
@@ -368,7 +439,7 @@ cudaError_t launch_router_wgrad(const Dims &dm, const Sources &src, const int32_
                                 const int32_t *row_tok, const uint8_t *row_j, const float *dl_sel,
                                 float *dW_r, cudaStream_t st)
 {
-    dim3 grid(static_cast<unsigned>((dm.d + 255) / 256), static_cast<unsigned>(dm.E));
+    dim3 grid(static_cast<unsigned>((dm.d / 2 + 255) / 256), static_cast<unsigned>(dm.E));
     k_router_wgrad<<<grid, 256, 0, st>>>(src, dm.d, dm.k, offsets, row_tok, row_j, dl_sel, dW_r);
     return cudaGetLastError();
 }
