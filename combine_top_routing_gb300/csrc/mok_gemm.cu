@@ -156,8 +156,18 @@ __device__ __forceinline__ int tile_k_stages(const GemmArgs &a, int g)
     else return a.k_stages;
 }
 
+// Epilogue warps of the single-CTA GEMM per mode: the data-gradient SwiGLU
+// backward (DGRAD2) is long arithmetic per accumulator column with the MMA
+// waiting for it, so it runs on two warps per TMEM lane quarter (128 columns
+// each); the other modes on one.
+template <int MODE>
+struct GemmShape {
+    static constexpr int kEpiWarps = MODE == MODE_DGRAD2 ? 8 : 4;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+};
+
 template <int MODE, bool MX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
     k_gemm(const __grid_constant__ AMaps<MODE == MODE_ROUTER ? 64 : 2> am,
            const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
            const GemmArgs a)
@@ -188,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        mbar_init(acc_empty, GemmShape<MODE>::kEpiWarps);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -409,12 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int row_in_e = tl.m_blk * kBM + r;
                 const bool valid = row_in_e < a.counts[e];
                 const int64_t grow = a.pad_offsets[e] + row_in_e;
-                const int f0 = tl.n_blk * BN;
+                // warps 2-5 take accumulator columns [0, 128), warps 6-9 [128, 256)
+                // (nothing when BN = 128): whole 128-column MX scale groups each
+                const int c_begin = ((warp - 2) >> 2) * 128;
+                const int c_end = min(BN, c_begin + 128);
+                const int f0 = tl.n_blk * BN + c_begin;
                 uint32_t wa = 0, wb = 0;
                 // the saved a, b of the next 32 columns are loaded while this
                 // chunk is processed (software pipeline over the row's chunks)
                 uint4 na[4], nb[4];
-                if (valid) {
+                if (valid && c_begin < c_end) {
                     const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + grow * a.F + f0);
                     const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + grow * a.F + f0);
 #pragma unroll
@@ -423,9 +437,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         nb[q] = __ldg(pb + q);
                     }
                 }
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 0; c < c_end - c_begin; c += 32) {
                     uint32_t v[32];
-                    tmem_ld_32x32(trow + c, v);
+                    tmem_ld_32x32(trow + c_begin + c, v);
                     tmem_ld_wait();
                     if (valid) {
                         const int64_t off = grow * a.F + f0 + c;
@@ -442,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 bv[8 * q + 2 * i + 1] = bf16_bits_to_float(ub[i] >> 16);
                             }
                         }
-                        if (c + 32 < BN) {
+                        if (c + 32 < c_end - c_begin) {
                             const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + off + 32);
                             const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + off + 32);
 #pragma unroll
@@ -936,7 +950,7 @@ cudaError_t launch_gemm(const AMaps<MODE == MODE_ROUTER ? 64 : 2> &am, const CUt
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3(static_cast<unsigned>(grid / kCluster * kCluster));
-            cfg.blockDim = dim3(kThreads);
+            cfg.blockDim = dim3(GemmShape<MODE>::kThreads);
             cfg.dynamicSmemBytes = smem;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
@@ -956,14 +970,14 @@ cudaError_t launch_gemm(const AMaps<MODE == MODE_ROUTER ? 64 : 2> &am, const CUt
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(GemmShape<MODE>::kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         return cudaLaunchKernelEx(&cfg, k_gemm<MODE, MX>, am, b0, b1, args);
     }
-    k_gemm<MODE, MX><<<grid, kThreads, smem, st>>>(am, b0, b1, args);
+    k_gemm<MODE, MX><<<grid, GemmShape<MODE>::kThreads, smem, st>>>(am, b0, b1, args);
     return cudaGetLastError();
 }
 
