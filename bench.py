@@ -183,9 +183,9 @@ def _layer_bytes(w):
 # summarised in profiles/k_moe_fused_traffic.md, keyed by workload and CTA pairs, with a
 # hash of the kernel's sources at capture time: once the kernel changes, traffic is null.
 FUSED_TRAFFIC = {
-    ("mixtral_bf16", 1): {"bytes": 4815936000 + 789549824, "src_sha": "9e5fdee9d8b53ffe"},
-    ("dsv3_mxfp8", 0): {"bytes": 17065882368 + 3360519680, "src_sha": "9e5fdee9d8b53ffe"},
-    ("dsv3_skew_ep", 0): {"bytes": 17300825344 + 3360524032, "src_sha": "9e5fdee9d8b53ffe"},
+    ("mixtral_bf16", 1): {"bytes": 4769787392 + 789440512, "src_sha": "678044feb79b8cb5"},
+    ("dsv3_mxfp8", 0): {"bytes": 17057815040 + 3360794880, "src_sha": "678044feb79b8cb5"},
+    ("dsv3_skew_ep", 0): {"bytes": 17330199808 + 3360492288, "src_sha": "678044feb79b8cb5"},
 }
 FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h")
 
