@@ -31,6 +31,12 @@ SMALL = {
     # d and F multiples of 256: every weight-gradient GEMM runs on CTA pairs
     "mx_pairs": I.Workload("mx_pairs", T=600, d=512, E=16, k=4, F=512, dtype="mxfp8",
                            router="sigmoid", seed=45),
+    # ~1000 token rows per expert: the weight-gradient K (an expert's rows) spans
+    # more stages than the operand ring holds, so the ring wraps inside a tile
+    "bf16_bigk": I.Workload("bf16_bigk", T=2048, d=256, E=4, k=2, F=256, dtype="bf16",
+                            router="softmax", seed=46),
+    "mx_bigk": I.Workload("mx_bigk", T=2048, d=256, E=4, k=2, F=256, dtype="mxfp8",
+                          router="sigmoid", seed=47),
 }
 
 
@@ -195,7 +201,7 @@ def test_backward_bit_reproducible():
     assert len(hashes) == 1
 
 
-@pytest.mark.parametrize("name", ["mx_pairs", "bf16_many_empty", "mx_sources"])
+@pytest.mark.parametrize("name", ["mx_pairs", "bf16_many_empty", "mx_sources", "mx_bigk"])
 def test_wgrad_cta_pairs_equal_single_cta(name, monkeypatch):
     """The weight-gradient GEMMs on CTA pairs (256 dW rows per pair tile)
     give the same bits as one CTA per 128-row tile, experts without rows
