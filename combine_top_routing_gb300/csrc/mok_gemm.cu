@@ -677,8 +677,8 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
         if constexpr (MODE == MODE_WGRAD) {
             t.group = tile / wper;
             const int local = tile - t.group * wper;
-            t.n_blk = local / wmt;
-            t.m_blk = local - t.n_blk * wmt;
+            t.m_blk = local / a.n_tiles;
+            t.n_blk = local - t.m_blk * a.n_tiles;
         } else {
             t = decode_tile(tile, prefix, groups, a.n_tiles);
         }
