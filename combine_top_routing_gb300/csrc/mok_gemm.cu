@@ -563,13 +563,12 @@ struct PairMaps {
 
 // WGRAD epilogue: every epilogue warp owns 32 dW rows x (256 / (warps / 4))
 // columns per tile, stored 64 columns at a time through one shared-memory box
-// of 32 x 64 BF16 (4 KB, 128-byte swizzled) by TMA.
+// of 32 x 64 BF16 (4 KB, 128-byte swizzled) by TMA.  Box bytes per warp:
 template <int MODE>
-struct PairOut {
-    static constexpr int kCols = MODE == MODE_WGRAD ? 256 / (PairShape<MODE>::kEpiWarps / 4) : 0;
-    static constexpr int kBoxes = kCols / 64;
-    static constexpr int kWarpBytes = MODE == MODE_WGRAD ? 4096 : 0;
-};
+constexpr int pair_box_bytes()
+{
+    return MODE == MODE_WGRAD ? 4096 : 0;
+}
 
 // index of the scale tile of (k element x, row y) in a [rows, K] matrix
 __device__ __forceinline__ int sf_tile(int x, int y, int64_t rows)
@@ -589,7 +588,7 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sT = smem;  // stage s: A at s*32K, B half at s*32K + 16K
     uint8_t *sOut = sT + kPStages * kPStage;  // WGRAD output boxes (1024-byte aligned)
-    uint8_t *sSF = sOut + kEpiWarps * PairOut<MODE>::kWarpBytes;
+    uint8_t *sSF = sOut + kEpiWarps * pair_box_bytes<MODE>();
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kPStages * (kSfaBytes + kSfbBytes) : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + kPStages;
@@ -813,17 +812,18 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
                 // The accumulator is released once it is in registers; the rows go to this
                 // warp's boxes (lane = row, 16-byte chunk c of a 128-byte box row at
                 // c ^ (row & 7): the SWIZZLE_128B layout) and leave by TMA stores.
-                constexpr int kCols = PairOut<MODE>::kCols;
+                constexpr int kCols = 256 / (kEpiWarps / 4);
+                constexpr int kBoxes = kCols / 64;
                 const bool empty_k = s_pad[e + 1] == s_pad[e];
                 uint32_t pk[128];
                 drain_row_bf16(trow, kCols, empty_k, pk);
                 release();
-                uint8_t *box = sOut + (warp - 2) * PairOut<MODE>::kWarpBytes;
+                uint8_t *box = sOut + (warp - 2) * pair_box_bytes<MODE>();
                 const uint32_t rbase = smem_u32(box) + static_cast<uint32_t>(lane) * 128u;
                 const int x = tl.n_blk * 256 + ecol;
                 const int y = e * a.m_rows + (2 * tl.m_blk + static_cast<int>(rank)) * kBM + quarter * 32;
 #pragma unroll
-                for (int bx = 0; bx < PairOut<MODE>::kBoxes; ++bx) {
+                for (int bx = 0; bx < kBoxes; ++bx) {
                     if (lane == 0) bulk_wait_group_read<0>();  // the box's previous store has read it
                     __syncwarp();
 #pragma unroll
@@ -880,7 +880,7 @@ constexpr size_t pair_smem_bytes()
 {
     constexpr int st = PairShape<MODE>::kStages;
     constexpr int ew = PairShape<MODE>::kEpiWarps;
-    return 1024 + st * kPStage + ew * PairOut<MODE>::kWarpBytes + (MX ? st * (kSfaBytes + kSfbBytes) : 0) +
+    return 1024 + st * kPStage + ew * pair_box_bytes<MODE>() + (MX ? st * (kSfaBytes + kSfbBytes) : 0) +
            (2 * st + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 +
            (MODE == MODE_WGRAD ? (MOK_MAX_EXPERTS + 4) * 4 : ew * kStageWords * 4);
 }
