@@ -37,6 +37,11 @@ SMALL = {
                             router="softmax", seed=46),
     "mx_bigk": I.Workload("mx_bigk", T=2048, d=256, E=4, k=2, F=256, dtype="mxfp8",
                           router="sigmoid", seed=47),
+    # degenerate routing: one slot per token, and a single expert taking every token
+    "bf16_top1": I.Workload("bf16_top1", T=300, d=256, E=8, k=1, F=256, dtype="bf16",
+                            router="softmax", seed=48),
+    "mx_one_expert": I.Workload("mx_one_expert", T=384, d=256, E=1, k=1, F=256, dtype="mxfp8",
+                                router="sigmoid", seed=49),
 }
 
 
