@@ -1209,11 +1209,14 @@ int auto_minibatch_rows(const Dims &dm, int gather_ctas, int gemm_ctas)
 // has loaded them; with bands of B pair rows the wait is acyclic when
 // 2B <= R - U + 1 (R ring row tiles, U <= 2 row tiles per unit), which
 // B = R / 4 >= 1 satisfies for R >= 4.  Smaller rings run one CTA per tile.
-// Default: pairs for BF16 layers, one CTA per tile for MXFP8 layers, as
-// measured on GB300: MXFP8 pairs are slower on the DeepSeek-V3 shape (8.27 vs
-// 7.41 ms at 16384 tokens, 5.16 vs 4.33 ms at 8192 tokens, where no expert
-// has a ghost half), BF16 pairs gain on the Mixtral shape (4.27 vs 4.33 ms).
-// MOK_FUSED_PAIR=1 / 0 in the environment forces either.
+// Default: pairs for BF16 layers, one CTA per tile for MXFP8 layers -- on
+// GB300 the fused kernel's tensor pipe runs at the same rate either way, so
+// the ghost halves of experts whose rows round up to an odd number of row
+// tiles (about half of them on the DeepSeek-V3 shape, whose expert row counts
+// scatter around 256 or 512) make MXFP8 pairs slower (8.27 vs 7.41 ms at
+// 16384 tokens, 5.16 vs 4.33 ms at 8192) while BF16 pairs gain (4.27 vs
+// 4.33 ms on the Mixtral shape).  MOK_FUSED_PAIR=1 / 0 in the environment
+// forces either.
 bool fused_uses_pairs(const Dims &dm, const mok_config *cfg)
 {
     if (dm.d % 256 != 0) return false;
