@@ -183,9 +183,9 @@ def _layer_bytes(w):
 # summarised in profiles/k_moe_fused_traffic.md, keyed by workload and CTA pairs, with a
 # hash of the kernel's sources at capture time: once the kernel changes, traffic is null.
 FUSED_TRAFFIC = {
-    ("mixtral_bf16", 1): {"bytes": 4714239232 + 789443584, "src_sha": "48f9979643bf07bc"},
-    ("dsv3_mxfp8", 0): {"bytes": 17076248832 + 3360527104, "src_sha": "48f9979643bf07bc"},
-    ("dsv3_skew_ep", 0): {"bytes": 17309502208 + 3360569088, "src_sha": "48f9979643bf07bc"},
+    ("mixtral_bf16", 1): {"bytes": 4915918848 + 789699584, "src_sha": "27c6a11e85b154b5"},
+    ("dsv3_mxfp8", 0): {"bytes": 17070225152 + 3360603904, "src_sha": "27c6a11e85b154b5"},
+    ("dsv3_skew_ep", 0): {"bytes": 17291281152 + 3360698368, "src_sha": "27c6a11e85b154b5"},
 }
 FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h")
 
