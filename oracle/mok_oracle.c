@@ -21,7 +21,7 @@
  *
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fopenmp -shared -fPIC -lm
  * (-ffp-contract=off keeps a*b+c as two roundings; only the explicit fmaf of
- * the combine contract fuses.)
+ * the combine and reverse-dispatch contracts fuses.)
  */
 #include <math.h>
 #include <stdint.h>
@@ -389,21 +389,43 @@ void mko_router_bwd(int T, int d, int E, int k, int kind,
 
 /* ------------------------------------------------------------------ */
 /* B5 Reverse dispatch ([kucoin] §02: backward pushes in reverse-        */
-/* dispatch).  dX[t] = sum_j dx_slot[slot_pos[t,j]] + dxr[t]; BF16 out   */
-/* unless exact.                                                          */
+/* dispatch) with the router's share of dX ([kucoin] §01: the router     */
+/* decides at every step, so its logits carry gradient back to x):       */
+/*   dX[t] = sum_j dx_slot[slot_pos[t,j]] + sum_j dl_j W_r[ids[t,j]]      */
+/* where dl_j is the logit gradient of the chosen expert j (the other     */
+/* logits get none).  The pages fix no order.  Contract (exact == 0):    */
+/* one fp32 accumulator per element starting from 0, the k slot rows     */
+/* added in ascending j, then the k router terms folded in ascending j    */
+/* with fmaf(dl_j, W_r[e_j][c], acc), then BF16 round-to-nearest-even;   */
+/* dx rows hold BF16 values, dl and W_r fp32 values.  exact != 0: plain   */
+/* fp64 sum, no rounding.                                                 */
 /* ------------------------------------------------------------------ */
 
 void mko_rev_dispatch(int T, int k, int d, int exact,
                       const double *dx_rows, const int32_t *slot_pos,
-                      const double *dxr, double *dX)
+                      const int32_t *ids, const double *dl_sel, const double *Wr,
+                      double *dX)
 {
     #pragma omp parallel for schedule(static)
     for (int t = 0; t < T; ++t)
         for (int c = 0; c < d; ++c) {
-            double acc = 0.0;
-            for (int j = 0; j < k; ++j)
-                acc += dx_rows[(int64_t)slot_pos[t * k + j] * d + c];
-            if (dxr) acc += dxr[(int64_t)t * d + c];
-            dX[(int64_t)t * d + c] = exact ? acc : mko_bf16_round(acc);
+            if (exact) {
+                double acc = 0.0;
+                for (int j = 0; j < k; ++j)
+                    acc += dx_rows[(int64_t)slot_pos[t * k + j] * d + c];
+                if (dl_sel)
+                    for (int j = 0; j < k; ++j)
+                        acc += dl_sel[t * k + j] * Wr[(int64_t)ids[t * k + j] * d + c];
+                dX[(int64_t)t * d + c] = acc;
+            } else {
+                float acc = 0.0f;
+                for (int j = 0; j < k; ++j)
+                    acc = acc + (float)dx_rows[(int64_t)slot_pos[t * k + j] * d + c];
+                if (dl_sel)
+                    for (int j = 0; j < k; ++j)
+                        acc = fmaf((float)dl_sel[t * k + j],
+                                   (float)Wr[(int64_t)ids[t * k + j] * d + c], acc);
+                dX[(int64_t)t * d + c] = mko_bf16_round((double)acc);
+            }
         }
 }

@@ -87,7 +87,7 @@ def lib():
                 "mko_router_bwd": (None, [_int, _int, _int, _int, _int, _d, _d,
                                           _d, _i32, _d, _d, _d, _d, _d]),
                 "mko_rev_dispatch": (None, [_int, _int, _int, _int, _d, _i32,
-                                            _d, _d]),
+                                            _i32, _d, _d, _d]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -409,18 +409,36 @@ def router_bwd(x, Wr, scores, ids, gates, dgates, kind):
     return dict(dlogits=dl, dWr=dWr, dxr=dxr)
 
 
-def rev_dispatch(dx_rows, slot_pos, dxr, exact=False):
-    """B5 push reverse-dispatch: dX[t] = sum_j dx_rows[slot_pos[t,j]] + dxr[t]."""
+def rev_dispatch(dx_rows, slot_pos, ids=None, dl_sel=None, Wr=None, exact=False):
+    """B5 push reverse-dispatch with the router's share of dX:
+    dX[t] = sum_j dx_rows[slot_pos[t,j]] + sum_j dl_sel[t,j] W_r[ids[t,j]].
+
+    Contract mode: one fp32 accumulator from 0, the slot rows added in
+    ascending j, then the router terms folded in ascending j with fmaf, then
+    BF16; dl_sel and W_r are taken as fp32 values, dx rows as BF16 values.
+    ``dl_sel=None`` leaves the router term out."""
     dx_rows = _f64(dx_rows)
     slot_pos = np.ascontiguousarray(slot_pos, dtype=np.int32)
     T, k = slot_pos.shape
     d = dx_rows.shape[1]
-    dxr_ = None if dxr is None else _f64(dxr)
+    if dl_sel is None:
+        ids_, dl_, wr_ = None, None, None
+    else:
+        ids_ = np.ascontiguousarray(ids, dtype=np.int32)
+        dl_ = _f64(dl_sel) if exact else fp32(dl_sel)
+        wr_ = _f64(Wr) if exact else fp32(Wr)
     dX = np.empty((T, d))
-    lib().mko_rev_dispatch(T, k, d, int(bool(exact)), _p(dx_rows, _d),
-                           _p(slot_pos, _i32), None if dxr_ is None else _p(dxr_, _d),
-                           _p(dX, _d))
+    lib().mko_rev_dispatch(T, k, d, int(bool(exact)), _p(dx_rows, _d), _p(slot_pos, _i32),
+                           None if ids_ is None else _p(ids_, _i32),
+                           None if dl_ is None else _p(dl_, _d),
+                           None if wr_ is None else _p(wr_, _d), _p(dX, _d))
     return dX
+
+
+def chosen_logit_grads(dlogits, ids):
+    """The logit gradients of the chosen experts, [T, k] in slot order (the
+    other logits get none)."""
+    return np.take_along_axis(_f64(dlogits), np.asarray(ids, dtype=np.int64), axis=1)
 
 
 def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode):
@@ -456,6 +474,7 @@ def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode):
         grads[e] = expert_wgrad(dy_rows[lo:hi], h_s, g["da"], g["db"], xe_rows, mode)
     xs = _f64(x)[fwd["tokens"]]
     rb = router_bwd(xs, Wr, r["scores"], r["ids"], r["gates"], dgates, kind)
-    dX = rev_dispatch(dx_rows, lay["slot_pos"], rb["dxr"], exact=exact)
+    dl_sel = chosen_logit_grads(rb["dlogits"], r["ids"])
+    dX = rev_dispatch(dx_rows, lay["slot_pos"], r["ids"], dl_sel, Wr, exact=exact)
     return dict(dX=dX, dgates=dgates, dlogits=rb["dlogits"], dWr=rb["dWr"],
                 dxr=rb["dxr"], dy_rows=dy_rows, dx_rows=dx_rows, experts=grads)
