@@ -34,6 +34,8 @@ int check_config(const mok_config *cfg, Dims *dm)
         cfg->minibatch_rows != 256)
         return MOK_ERR_INVALID_ARG;
     if (cfg->gather_sm_fraction < 0.0f || cfg->gather_sm_fraction >= 1.0f) return MOK_ERR_INVALID_ARG;
+    for (const int v : {cfg->fused_cta_pairs, cfg->gemm_cta_pairs})
+        if (v != MOK_PAIRS_AUTO && v != MOK_PAIRS_ON && v != MOK_PAIRS_OFF) return MOK_ERR_INVALID_ARG;
     if (E > MOK_MAX_EXPERTS || k > MOK_MAX_TOPK || k > E) return MOK_ERR_UNSUPPORTED;
     if (d % 128 != 0 || F % 128 != 0) return MOK_ERR_UNSUPPORTED;
     const int64_t S = static_cast<int64_t>(T) * k;
@@ -59,6 +61,7 @@ int check_config(const mok_config *cfg, Dims *dm)
         dm->rows_pad = round_up(S + static_cast<int64_t>(E) * (MOK_ROW_ALIGN - 1), 256);
         dm->E_pad = static_cast<int>(round_up(E, 128));
         dm->nchunks = static_cast<int>((S + kLayoutChunk - 1) / kLayoutChunk);
+        dm->gemm_pairs = cfg->gemm_cta_pairs != MOK_PAIRS_OFF;
     }
     return MOK_OK;
 }
@@ -636,6 +639,32 @@ int mok_quantize_mx(const void *src, int64_t batch, int64_t rows, int64_t K, int
     if (transpose != 0 && transpose != 1) return MOK_ERR_INVALID_ARG;
     return cuda_status(launch_quant_mx(static_cast<const uint16_t *>(src), batch, rows, K, transpose,
                                        codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int mok_swiglu_quantize_mx(const float *a, const float *b, int64_t rows, int64_t F, float *h,
+                           uint8_t *codes, uint32_t *scales, void *stream)
+{
+    if (!a || !b || !codes || !scales || rows < 1 || F < 1) return MOK_ERR_INVALID_ARG;
+    if (rows % 128 != 0 || F % 128 != 0) return MOK_ERR_UNSUPPORTED;
+    return cuda_status(launch_swiglu_quant(a, b, rows, F, h, codes, scales, static_cast<cudaStream_t>(stream)));
+}
+
+int mok_bwd_ws_layout(const mok_config *cfg, mok_bwd_layout *out)
+{
+    Dims dm;
+    const int rc = check_config(cfg, &dm);
+    if (rc != MOK_OK) return rc;
+    if (!out) return MOK_ERR_INVALID_ARG;
+    BwdWs w;
+    bwd_ws_layout(dm, &w);
+    out->status = w.status;
+    out->dy = w.dy;
+    out->da = w.da;
+    out->db = w.db;
+    out->dx = w.dx;
+    out->dl_sel = w.dl_sel;
+    out->total = w.total;
+    return MOK_OK;
 }
 
 int mok_reset_device_status(void *ws, void *stream)

@@ -41,8 +41,6 @@
 // schedule order (cooperative launch: all CTAs are resident).
 #include <cuda_bf16.h>
 
-#include <stdlib.h>
-
 #include <mutex>
 
 #include "mok_internal.h"
@@ -1215,14 +1213,12 @@ int auto_minibatch_rows(const Dims &dm, int gather_ctas, int gemm_ctas)
 // tiles (about half of them on the DeepSeek-V3 shape, whose expert row counts
 // scatter around 256 or 512) make MXFP8 pairs slower (8.27 vs 7.41 ms at
 // 16384 tokens, 5.16 vs 4.33 ms at 8192) while BF16 pairs gain (4.27 vs
-// 4.33 ms on the Mixtral shape).  MOK_FUSED_PAIR=1 / 0 in the environment
+// 4.33 ms on the Mixtral shape).  cfg->fused_cta_pairs = MOK_PAIRS_ON / OFF
 // forces either.
 bool fused_uses_pairs(const Dims &dm, const mok_config *cfg)
 {
-    if (dm.d % 256 != 0) return false;
-    const char *v = getenv("MOK_FUSED_PAIR");
-    if (v && v[0] == '0') return false;
-    if (!(v && v[0] == '1') && dm.dtype == MOK_MXFP8) return false;
+    if (dm.d % 256 != 0 || cfg->fused_cta_pairs == MOK_PAIRS_OFF) return false;
+    if (cfg->fused_cta_pairs == MOK_PAIRS_AUTO && dm.dtype == MOK_MXFP8) return false;
     const int64_t ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
     return ring_rows >= dm.rows_pad || ring_rows / 128 >= 4;
 }

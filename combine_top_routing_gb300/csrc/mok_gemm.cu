@@ -35,8 +35,6 @@
 // CTAs share B tiles and the group's rows through L2.
 #include <cuda_bf16.h>
 
-#include <stdlib.h>
-
 #include <mutex>
 
 #include "mok_internal.h"
@@ -51,22 +49,6 @@ namespace {
 #define MOK_GEMM_CLUSTER 1
 #endif
 constexpr int kCluster = MOK_GEMM_CLUSTER;  // CTAs per cluster of the GEMM launch
-#ifndef MOK_GEMM_PAIR
-#define MOK_GEMM_PAIR 1
-#endif
-// Forward expert GEMMs of the separate-kernel path on CTA pairs (cta_group::2):
-// the compiled default (on: 7.5 vs 8.0 ms for the MXFP8 expert FFN of the
-// DeepSeek-V3 shape, 4.2 vs 4.3 ms for the BF16 Mixtral shape on GB300),
-// overridden by the environment variable MOK_GEMM_PAIR ("0" or "1") read at
-// each launch.
-constexpr bool kPairGemm = MOK_GEMM_PAIR != 0;
-bool use_pair_gemm()
-{
-    const char *v = getenv("MOK_GEMM_PAIR");
-    if (v && (v[0] == '0' || v[0] == '1')) return v[0] == '1';
-    return kPairGemm;
-}
-
 enum { MODE_ROUTER = 0, MODE_FFN1, MODE_FFN2, MODE_DGRAD2, MODE_DGRAD1, MODE_WGRAD };
 
 template <int NA>
@@ -1076,7 +1058,9 @@ cudaError_t launch_ffn(const Dims &dm, const void *xe, const uint32_t *xe_scales
     g1.saved_a = saved_a;
     g1.saved_b = saved_b;
     g1.saved_h = saved_h;
-    const bool pair = use_pair_gemm();
+    // CTA pairs unless the config turns them off (MXFP8 expert FFN of the
+    // DeepSeek-V3 shape 7.5 vs 8.0 ms, BF16 Mixtral shape 4.2 vs 4.3 ms on GB300)
+    const bool pair = dm.gemm_pairs;
     PairMaps p1 = {}, p2 = {};
     if (pair) {
         p1.a = a1.m[0];
@@ -1202,7 +1186,7 @@ cudaError_t launch_wgrad(const Dims &dm, const void *A_T, const uint32_t *A_s, i
     am.n = 1;
     GemmArgs g = base_args(dm, status, wait_ns);
     g.pad_offsets = pad_offsets;
-    if (use_pair_gemm() && a_rows % 256 == 0 && b_rows % 256 == 0) {
+    if (dm.gemm_pairs && a_rows % 256 == 0 && b_rows % 256 == 0) {
         // CTA pairs: 256 dW rows x 256 columns per pair tile
         PairMaps pm = {};
         pm.a = am.m[0];
@@ -1235,6 +1219,50 @@ cudaError_t launch_wgrad(const Dims &dm, const void *A_T, const uint32_t *A_s, i
     g.out_ld = b_rows;
     return mx ? launch_gemm<MODE_WGRAD, true>(am, bm, bm, g, st)
               : launch_gemm<MODE_WGRAD, false>(am, bm, bm, g, st);
+}
+
+// ---------------------------------------------------------------------------
+// The FFN1 epilogue's SwiGLU and MXFP8 quantisation of h, run on fp32 a, b
+// read from memory (mok_swiglu_quantize_mx): one thread per row and block of
+// 32 columns along F, through the same swiglu_f32 and mx_block32 as the
+// epilogues, so the codes and scales it writes are the ones the expert GEMM
+// writes for the same fp32 accumulator values.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_swiglu_quant(const float *__restrict__ a,
+                                                      const float *__restrict__ b, int64_t rows, int F,
+                                                      float *__restrict__ h, uint8_t *__restrict__ codes,
+                                                      uint32_t *__restrict__ scales)
+{
+    const int64_t nblk = F / 32;
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= rows * nblk) return;
+    const int64_t r = i / nblk;
+    const int c = static_cast<int>(i % nblk) * 32;
+    const int64_t off = r * F + c;
+    float hv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) hv[j] = swiglu_f32(a[off + j], b[off + j]);
+    if (h) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) h[off + j] = hv[j];
+    }
+    uint32_t q[8];
+    const uint32_t sb = mx_block32(hv, q);
+    uint4 *o = reinterpret_cast<uint4 *>(codes + off);
+    o[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    o[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    // byte (c / 32) % 4 of the word of k-group c / 128 holds this block's scale
+    reinterpret_cast<uint8_t *>(scales + scale_word_row(c >> 7, r, rows))[(c >> 5) & 3] =
+        static_cast<uint8_t>(sb);
+}
+
+cudaError_t launch_swiglu_quant(const float *a, const float *b, int64_t rows, int64_t F, float *h,
+                                uint8_t *codes, uint32_t *scales, cudaStream_t st)
+{
+    const int64_t threads = rows * (F / 32);
+    k_swiglu_quant<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(
+        a, b, rows, static_cast<int>(F), h, codes, scales);
+    return cudaGetLastError();
 }
 
 }  // namespace mok

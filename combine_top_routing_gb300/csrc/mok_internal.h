@@ -46,6 +46,7 @@ struct Dims {
     int64_t rows_pad;       // padded expert-ordered rows bound
     int E_pad;              // E rounded up to 128 (router GEMM N)
     int nchunks;            // layout chunks of kLayoutChunk slots
+    bool gemm_pairs;        // separate expert FFN / weight-gradient GEMMs may use CTA pairs
 };
 
 constexpr int kLayoutChunk = 256;
@@ -145,6 +146,8 @@ cudaError_t launch_rev_dispatch(const Dims &dm, const int32_t *ids, const int32_
 cudaError_t launch_router_wgrad(const Dims &dm, const Sources &src, const int32_t *offsets,
                                 const int32_t *row_tok, const uint8_t *row_j, const float *dl_sel,
                                 float *dW_r, cudaStream_t st);
+cudaError_t launch_swiglu_quant(const float *a, const float *b, int64_t rows, int64_t F, float *h,
+                                uint8_t *codes, uint32_t *scales, cudaStream_t st);
 cudaError_t launch_transpose_bf16(const uint16_t *src, int64_t batch, int64_t rows, int64_t K,
                                   uint16_t *dst, cudaStream_t st);
 
@@ -165,8 +168,8 @@ int64_t fused_ring_rows(const Dims &dm, size_t ring_bytes);
 int auto_gather_ctas(const Dims &dm, int sms);
 int auto_minibatch_rows(const Dims &dm, int gather_ctas, int gemm_ctas);
 // Whether the fused forward runs its GEMM role on CTA pairs (d a multiple of
-// 256 and an uncapped ring or one of at least 4 row tiles; the environment
-// variable MOK_FUSED_PAIR=0 turns it off), and its CTAs.
+// 256 and an uncapped ring or one of at least 4 row tiles, as
+// cfg->fused_cta_pairs allows), and its CTAs.
 bool fused_uses_pairs(const Dims &dm, const mok_config *cfg);
 int fused_ctas(const Dims &dm, const mok_config *cfg, int sms);
 // The knobs one fused launch of `ctas` CTAs uses: gather CTAs and minibatch rows.

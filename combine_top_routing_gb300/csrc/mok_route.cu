@@ -167,7 +167,10 @@ cudaError_t launch_topk(const Dims &dm, const float *logits, int32_t *ids, float
 //                  lanes with equal expert get consecutive ranks (match +
 //                  popc), so a slot's row is offsets[e] + (slots of e before
 //                  it) -- stable by t*k+j.
-// Everything is integer, so the result is the same on every run.
+// Everything is integer, so the result is the same on every run.  An id
+// outside [0, E) (possible only when the caller supplies the ids) is counted
+// nowhere and placed nowhere: its slot_pos is -1, and offsets[E] becomes -1
+// instead of T*k, so the error is visible and no table is indexed with it.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_layout_count(const int32_t *__restrict__ ids, int64_t S,
                                                       int E, int nchunks,
@@ -178,7 +181,10 @@ __global__ void __launch_bounds__(256) k_layout_count(const int32_t *__restrict_
     __syncthreads();
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * kLayoutChunk;
     const int64_t hi = lo + kLayoutChunk < S ? lo + kLayoutChunk : S;
-    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) atomicAdd(&hist[ids[i]], 1);
+    for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+        const int e = ids[i];
+        if (static_cast<unsigned>(e) < static_cast<unsigned>(E)) atomicAdd(&hist[e], 1);
+    }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += blockDim.x)
         chunk_counts[static_cast<int64_t>(e) * nchunks + blockIdx.x] = hist[e];
@@ -228,7 +234,8 @@ __global__ void __launch_bounds__(256) k_layout_scan_chunks(const int32_t *__res
 }
 
 __global__ void __launch_bounds__(1024) k_layout_scan_experts(const int32_t *__restrict__ counts,
-                                                              int E, int32_t *__restrict__ offsets,
+                                                              int E, int64_t S,
+                                                              int32_t *__restrict__ offsets,
                                                               int32_t *__restrict__ pad_offsets)
 {
     __shared__ int32_t s_warp[2][32];
@@ -273,7 +280,8 @@ __global__ void __launch_bounds__(1024) k_layout_scan_experts(const int32_t *__r
         offsets[e] = excl_c;
         pad_offsets[e] = excl_p;
         if (e == E - 1) {
-            offsets[E] = excl_c + cnt;
+            // fewer counted slots than T*k: some id was outside [0, E)
+            offsets[E] = excl_c + cnt == S ? excl_c + cnt : -1;
             pad_offsets[E] = excl_p + pad;
         }
     }
@@ -300,14 +308,19 @@ __global__ void __launch_bounds__(32) k_layout_place(const int32_t *__restrict__
         const uint32_t active = __ballot_sync(0xffffffffu, act);
         if (act) {
             const int e = ids[i];
-            const uint32_t peers = __match_any_sync(active, e);
+            const bool ok = static_cast<unsigned>(e) < static_cast<unsigned>(E);
+            const uint32_t peers = __match_any_sync(active, ok ? e : -1);
             const int rank = __popc(peers & ((1u << lane) - 1u));
-            const int pos = run[e] + rank;
-            slot_pos[i] = pos;
-            row_tok[pos] = static_cast<int32_t>(i / k);
-            row_j[pos] = static_cast<uint8_t>(i % k);
+            if (ok) {
+                const int pos = run[e] + rank;
+                slot_pos[i] = pos;
+                row_tok[pos] = static_cast<int32_t>(i / k);
+                row_j[pos] = static_cast<uint8_t>(i % k);
+            } else {
+                slot_pos[i] = -1;
+            }
             __syncwarp(active);
-            if (rank == 0) run[e] += __popc(peers);
+            if (ok && rank == 0) run[e] += __popc(peers);
         }
         __syncwarp();
     }
@@ -325,7 +338,7 @@ cudaError_t launch_layout(const Dims &dm, const int32_t *ids, int32_t *counts, i
     k_layout_scan_chunks<<<dm.E, 256, 0, st>>>(chunk_counts, dm.nchunks, chunk_base, counts);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
-    k_layout_scan_experts<<<1, 1024, 0, st>>>(counts, dm.E, offsets, pad_offsets);
+    k_layout_scan_experts<<<1, 1024, 0, st>>>(counts, dm.E, dm.S, offsets, pad_offsets);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     k_layout_place<<<dm.nchunks, 32, hist_bytes, st>>>(ids, dm.S, dm.k, dm.E, dm.nchunks, chunk_base,

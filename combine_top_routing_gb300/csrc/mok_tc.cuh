@@ -92,27 +92,36 @@ __device__ __forceinline__ void load_bf16x32(const uint16_t *src, float *v)
     }
 }
 
-// 32 fp32 values -> one MX block: 32 E4M3 codes at dst (16-byte aligned);
-// returns the E8M0 scale byte.
-__device__ __forceinline__ uint32_t quant_mx32(const float *v, uint8_t *dst)
+// SwiGLU of one accumulator element pair: h = silu(a) b, silu(a) = a / (1 + e^-a).
+__device__ __forceinline__ float swiglu_f32(float a, float b) { return a / (1.0f + __expf(-a)) * b; }
+
+// 32 fp32 values -> one MX block: 32 E4M3 codes packed four per word into q;
+// returns the E8M0 scale byte.  Every MXFP8 quantisation of h (the FFN1
+// epilogues and mok_swiglu_quantize_mx) runs this function.
+__device__ __forceinline__ uint32_t mx_block32(const float (&v)[32], uint32_t (&q)[8])
 {
     float amax = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
     const int x = mx_scale_exp(amax);
     const float inv = mx_inv_scale(x);
-    uint4 *o = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-        const float *s = v + 16 * q;
-        uint4 w;
-        w.x = pack_e4m3x2(s[0] * inv, s[1] * inv) | (pack_e4m3x2(s[2] * inv, s[3] * inv) << 16);
-        w.y = pack_e4m3x2(s[4] * inv, s[5] * inv) | (pack_e4m3x2(s[6] * inv, s[7] * inv) << 16);
-        w.z = pack_e4m3x2(s[8] * inv, s[9] * inv) | (pack_e4m3x2(s[10] * inv, s[11] * inv) << 16);
-        w.w = pack_e4m3x2(s[12] * inv, s[13] * inv) | (pack_e4m3x2(s[14] * inv, s[15] * inv) << 16);
-        o[q] = w;
-    }
+    for (int i = 0; i < 8; ++i)
+        q[i] = pack_e4m3x2(v[4 * i] * inv, v[4 * i + 1] * inv) |
+               (pack_e4m3x2(v[4 * i + 2] * inv, v[4 * i + 3] * inv) << 16);
     return static_cast<uint32_t>(x + 127);
+}
+
+// 32 fp32 values -> one MX block: 32 E4M3 codes at dst (16-byte aligned);
+// returns the E8M0 scale byte.
+__device__ __forceinline__ uint32_t quant_mx32(const float (&v)[32], uint8_t *dst)
+{
+    uint32_t q[8];
+    const uint32_t s = mx_block32(v, q);
+    uint4 *o = reinterpret_cast<uint4 *>(dst);
+    o[0] = make_uint4(q[0], q[1], q[2], q[3]);
+    o[1] = make_uint4(q[4], q[5], q[6], q[7]);
+    return s;
 }
 
 __device__ __forceinline__ int64_t scale_word(int64_t x_elem, int64_t row, int64_t rows)
@@ -217,24 +226,15 @@ __device__ __forceinline__ void epi_ffn1(uint32_t trow, bool valid, int64_t grow
             tmem_ld_wait();
             float hv[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float av = __uint_as_float(gv[i]);
-                hv[i] = av / (1.0f + __expf(-av)) * __uint_as_float(uv[i]);
-            }
+            for (int i = 0; i < 32; ++i) hv[i] = swiglu_f32(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
             if (!MX) {
 #pragma unroll
                 for (int i = 0; i < 16; ++i) hq[c / 2 + i] = pack_bf16x2(hv[2 * i], hv[2 * i + 1]);
             } else {
-                float amax = 0.0f;
+                uint32_t q[8];
+                sword |= mx_block32(hv, q) << (8 * (c >> 5));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(hv[i]));
-                const int x = mx_scale_exp(amax);
-                const float inv = mx_inv_scale(x);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    hq[c / 4 + i] = pack_e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
-                                    (pack_e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
-                sword |= static_cast<uint32_t>(x + 127) << (8 * (c >> 5));
+                for (int i = 0; i < 8; ++i) hq[c / 4 + i] = q[i];
             }
         }
         release();
@@ -254,10 +254,7 @@ __device__ __forceinline__ void epi_ffn1(uint32_t trow, bool valid, int64_t grow
         tmem_ld_wait();
         float hv[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float av = __uint_as_float(gv[i]);
-            hv[i] = av / (1.0f + __expf(-av)) * __uint_as_float(uv[i]);
-        }
+        for (int i = 0; i < 32; ++i) hv[i] = swiglu_f32(__uint_as_float(gv[i]), __uint_as_float(uv[i]));
         if (valid) {
             const int64_t off = grow * F + f0 + c;
             if (saved_a) {

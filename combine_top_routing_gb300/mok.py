@@ -20,6 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 MOK_OK, MOK_ERR_INVALID_ARG, MOK_ERR_UNSUPPORTED, MOK_ERR_CUDA, MOK_ERR_TIMEOUT = range(5)
 MOK_ROUTER_SOFTMAX, MOK_ROUTER_SIGMOID = 0, 1
 MOK_BF16, MOK_MXFP8 = 0, 1
+MOK_PAIRS_AUTO, MOK_PAIRS_ON, MOK_PAIRS_OFF = 0, 1, 2
 MOK_ROW_ALIGN = 128
 MOK_MAX_SOURCES = 64
 
@@ -29,6 +30,7 @@ EXPORTS = [
     "mok_moe_backward",
     "mok_quantize_mx", "mok_transpose_bf16", "mok_reset_device_status", "mok_get_device_status",
     "mok_status_string", "mok_layout_static", "mok_fused_plan", "mok_dispatch_by_token",
+    "mok_bwd_ws_layout", "mok_swiglu_quantize_mx",
 ]
 
 
@@ -39,7 +41,8 @@ class MokConfig(ctypes.Structure):
         ("dtype", ctypes.c_int), ("n_sources", ctypes.c_int),
         ("source_rows", ctypes.POINTER(ctypes.c_int)), ("minibatch_rows", ctypes.c_int),
         ("gather_sm_fraction", ctypes.c_float), ("ring_bytes", ctypes.c_size_t),
-        ("wait_limit_ns", ctypes.c_ulonglong),
+        ("wait_limit_ns", ctypes.c_ulonglong), ("fused_cta_pairs", ctypes.c_int),
+        ("gemm_cta_pairs", ctypes.c_int),
     ]
 
 
@@ -52,6 +55,10 @@ class MokWeights(ctypes.Structure):
 
 class MokWeightGrads(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("d_gate", "d_up", "d_down")]
+
+
+class MokBwdLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("status", "dy", "da", "db", "dx", "dl_sel", "total")]
 
 
 class MokCtxLayout(ctypes.Structure):
@@ -91,6 +98,8 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp]
         L.mok_transpose_bf16.argtypes = [vp, i64, i64, i64, vp, vp]
         L.mok_layout_static.argtypes = [cfgp] + [vp] * 8
+        L.mok_bwd_ws_layout.argtypes = [cfgp, ctypes.POINTER(MokBwdLayout)]
+        L.mok_swiglu_quantize_mx.argtypes = [vp, vp, i64, i64, vp, vp, vp, vp]
         L.mok_fused_plan.argtypes = [cfgp] + [ctypes.POINTER(ctypes.c_int)] * 4 + [ctypes.POINTER(i64)]
         L.mok_reset_device_status.argtypes = [vp, vp]
         L.mok_get_device_status.argtypes = [vp, vp]
@@ -128,14 +137,15 @@ class Config:
 
     def __init__(self, T, d_model, n_experts, top_k, d_ff, router, dtype, n_sources=1,
                  source_rows=None, minibatch_rows=0, gather_sm_fraction=0.0, ring_bytes=0,
-                 wait_limit_ns=0):
+                 wait_limit_ns=0, fused_cta_pairs=MOK_PAIRS_AUTO, gemm_cta_pairs=MOK_PAIRS_AUTO):
         self._rows = None
         if n_sources > 1:
             rows = source_rows or [T // n_sources] * n_sources
             self._rows = (ctypes.c_int * n_sources)(*rows)
         self.c = MokConfig(T, d_model, n_experts, top_k, d_ff, router, dtype, n_sources,
                            self._rows if self._rows is not None else None, minibatch_rows,
-                           gather_sm_fraction, ring_bytes, wait_limit_ns)
+                           gather_sm_fraction, ring_bytes, wait_limit_ns, fused_cta_pairs,
+                           gemm_cta_pairs)
 
     @classmethod
     def from_workload(cls, w, **kw):
@@ -165,6 +175,12 @@ def workspace_size(cfg: Config) -> tuple[int, int, int]:
 def saved_ctx_layout(cfg: Config) -> MokCtxLayout:
     out = MokCtxLayout()
     _check("mok_saved_ctx_layout", lib().mok_saved_ctx_layout(cfg.ref, ctypes.byref(out)))
+    return out
+
+
+def bwd_ws_layout(cfg: Config) -> MokBwdLayout:
+    out = MokBwdLayout()
+    _check("mok_bwd_ws_layout", lib().mok_bwd_ws_layout(cfg.ref, ctypes.byref(out)))
     return out
 
 
@@ -243,6 +259,12 @@ def moe_backward(cfg, x_src, W_r, saved_ctx, dY, weights: MokWeights, dX, grads:
 def quantize_mx(src, batch, rows, K, transpose, codes, scales, stream=None):
     _check("mok_quantize_mx", lib().mok_quantize_mx(
         _ptr(src), batch, rows, K, int(transpose), _ptr(codes), _ptr(scales), _stream(stream)))
+
+
+def swiglu_quantize_mx(a, b, rows, F, h, codes, scales, stream=None):
+    """The expert GEMM epilogue's SwiGLU + MXFP8 quantisation of h on fp32 a, b."""
+    _check("mok_swiglu_quantize_mx", lib().mok_swiglu_quantize_mx(
+        _ptr(a), _ptr(b), rows, F, _ptr(h), _ptr(codes), _ptr(scales), _stream(stream)))
 
 
 def transpose_bf16(src, batch, rows, K, dst, stream=None):

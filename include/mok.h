@@ -59,6 +59,10 @@ enum {
 
 enum { MOK_ROUTER_SOFTMAX = 0, MOK_ROUTER_SIGMOID = 1 };
 enum { MOK_BF16 = 0, MOK_MXFP8 = 1 };
+/* Tile choice of the tensor-core GEMMs: one CTA per 128-row tile, or CTA
+ * pairs (cta_group::2, 256-row tiles shared by two SMs).  Results are
+ * bit-identical either way; only the speed differs. */
+enum { MOK_PAIRS_AUTO = 0, MOK_PAIRS_ON = 1, MOK_PAIRS_OFF = 2 };
 
 #define MOK_ROW_ALIGN 128      /* expert segment alignment of row buffers */
 #define MOK_MAX_SOURCES 64     /* simulated expert-parallel source buffers */
@@ -85,6 +89,15 @@ typedef struct {
                                       fused forward (0 = automatic) */
     size_t ring_bytes;             /* token ring of the fused forward (0 = no cap) */
     unsigned long long wait_limit_ns; /* device spin give-up (0 = 2 s) */
+    int fused_cta_pairs;           /* GEMM role of the fused forward on CTA pairs:
+                                      MOK_PAIRS_AUTO (from the shape, see
+                                      mok_fused_plan), MOK_PAIRS_ON (wherever the
+                                      shape allows), MOK_PAIRS_OFF */
+    int gemm_cta_pairs;            /* the separate expert FFN (mok_expert_ffn) and
+                                      the weight-gradient GEMMs on CTA pairs:
+                                      MOK_PAIRS_AUTO (= on) / ON / OFF; pairs
+                                      need the tile's dimensions to be
+                                      multiples of 256, else one CTA per tile */
 } mok_config;
 
 /* Expert weights.  Masters are BF16; the MXFP8 copies are made by
@@ -129,6 +142,16 @@ int mok_workspace_size(const mok_config *cfg, size_t *fwd_ws, size_t *saved_ctx,
 
 /* Offsets of the saved-context fields for this config. */
 int mok_saved_ctx_layout(const mok_config *cfg, mok_ctx_layout *out);
+
+/* Byte offsets of the backward workspace's intermediate rows, for
+ * inspection after mok_moe_backward: the status word, dy rows (BF16
+ * [rows_pad, d], B1's output in the padded expert order), da and db (BF16
+ * [rows_pad, F], B2's output), dx rows (BF16 [rows_pad, d], B3's output) and
+ * the chosen experts' logit gradients (fp32 [T, k]).  256-byte aligned. */
+typedef struct {
+    size_t status, dy, da, db, dx, dl_sel, total;
+} mok_bwd_layout;
+int mok_bwd_ws_layout(const mok_config *cfg, mok_bwd_layout *out);
 
 /*
  * A1 + A2: router top-k and layout ([kucoin] §01: the router decides each
@@ -235,9 +258,10 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
  * host only (no device work): its CTAs (at most one per SM), whether its
  * GEMM role runs on CTA pairs (1) or one CTA per tile (0), the CTAs that
  * start in the gather role, the minibatch (rows per hand-off) and the token
- * ring's rows.  CTA pairs are used for BF16 layers with d a multiple of 256
- * and an uncapped ring or one of at least 512 rows (the environment variable
- * MOK_FUSED_PAIR = 0 / 1 forces either where the shape allows).  A knob the config
+ * ring's rows.  CTA pairs need d a multiple of 256 and an uncapped ring or
+ * one of at least 512 rows; cfg->fused_cta_pairs = MOK_PAIRS_ON / OFF forces
+ * either where the shape allows, MOK_PAIRS_AUTO takes them for BF16 layers.
+ * A knob the config
  * leaves 0 is chosen from the shape ([kucoin] §03: the right minibatch and
  * number of communication SMs change with the hidden size, top-k and expert
  * size; §02: one minibatch should give the expert GEMM two full waves of
@@ -295,6 +319,20 @@ int mok_moe_backward(const mok_config *cfg, const void *const *x_src, const floa
 int mok_quantize_mx(const void *src, int64_t batch, int64_t rows, int64_t K,
                     int transpose, uint8_t *codes, uint32_t *scales, void *stream);
 
+/*
+ * The expert GEMM's SwiGLU and MXFP8 quantisation of h, on fp32 inputs
+ * ([kucoin] §02: MXFP8 quantisation fused into SwiGLU).  h = silu(a) * b in
+ * fp32, quantised in blocks of 32 along F, by the same device code the FFN1
+ * epilogue runs on its fp32 accumulators -- so for given fp32 a, b the codes
+ * and scales are the ones the fused forward writes.  For checking the
+ * epilogue's quantiser against a reference on known inputs.
+ * a, b   device fp32 [rows, F];  h device fp32 [rows, F] (the fp32 SwiGLU
+ *        output) or NULL;  codes device E4M3 [rows, F];  scales device, tile
+ *        layout for a [rows, F] matrix.  rows and F multiples of 128.
+ */
+int mok_swiglu_quantize_mx(const float *a, const float *b, int64_t rows, int64_t F, float *h,
+                           uint8_t *codes, uint32_t *scales, void *stream);
+
 /* BF16 transpose of `batch` matrices [rows, K] into [K, rows] each (the
  * transposed weights of the BF16 backward).  rows, K >= 1. */
 int mok_transpose_bf16(const void *src, int64_t batch, int64_t rows, int64_t K, void *dst,
@@ -316,13 +354,24 @@ int mok_transpose_bf16(const void *src, int64_t batch, int64_t rows, int64_t K, 
  * the routing ids [T, k] (device int32): counts, offsets, pad_offsets,
  * slot_pos, row_tok, row_j, with the same layouts and the same bits.
  *
+ * Precondition: every id lies in [0, E).  The kernels check it: an id
+ * outside that range is counted for no expert and placed in no row, its
+ * slot_pos is set to -1, and offsets[E] is set to -1 instead of T*k (the
+ * other outputs then describe the valid slots only).  Check offsets[E]
+ * before using the layout when the ids come from outside mok_route_layout.
+ *
  * Limit: 2 * ceil(T*k / 256) * E <= 262144 (for example T*k = 131072 slots
  * with E = 256 experts); larger layers return MOK_ERR_UNSUPPORTED and enqueue
- * nothing.  It allocates nothing and calls no allocating routine.
- * The first call on a device looks up the array's device address with that
- * device current (once per device); make that first call before any stream
- * capture.  Every GPU that loads the library holds the 1 MiB until the
- * process exits.  All calls on a device share the one array, and each call
+ * nothing.  The call itself allocates nothing and calls no allocating
+ * routine, with one exception on its first call on each device: it looks up
+ * the array's device address with that device current, and under CUDA's lazy
+ * module loading (the default) that lookup also loads this part of the
+ * library's device code onto the device, which allocates device memory (the
+ * 1 MiB array among it) and may synchronise the device.  So make the first
+ * call on each device during set-up, before any stream capture and before
+ * the point where allocation is not allowed; every later call on that device
+ * is allocation-free.  Every GPU that loads the library holds the 1 MiB until
+ * the process exits.  All calls on a device share the one array, and each call
  * overwrites what the previous one left there (nothing in it needs to start
  * at zero), so two calls that can run at the same time on the GPU -- on
  * different streams without ordering between them -- race and give wrong

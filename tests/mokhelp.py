@@ -4,6 +4,8 @@ the tolerance check.  Nothing here computes any step of the layer."""
 from __future__ import annotations
 
 import hashlib
+import json
+import os
 
 import numpy as np
 import torch
@@ -53,6 +55,17 @@ def check_close(got: np.ndarray, ref: np.ndarray, rel=REL_L2, mabs=MAX_ABS, what
         mx = (np.abs(got - ref) / np.maximum(max(1.0, rms), np.abs(ref))).max()
     else:
         mx = 0.0
+    diag = os.environ.get("MOK_TEST_DIAG")
+    if diag and got.size:
+        d = np.abs(got - ref)
+        i = int(np.argmax(d))
+        with open(diag, "a") as f:
+            f.write(json.dumps({
+                "test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], "what": what,
+                "n": int(got.size), "rel_l2": float(err), "max_abs": float(d.max()),
+                "ref_at_max": float(ref.reshape(-1)[i]), "ref_rms": float(np.sqrt(np.mean(ref * ref))),
+                "max_units_1_ref": float((d / np.maximum(1.0, np.abs(ref))).max()),
+                "max_units_1_ref_rms": float(mx)}) + "\n")
     assert err <= rel and mx <= mabs, f"{what}: rel_l2={err:.3e} max_abs={mx:.3e}"
     return err, mx
 

@@ -57,6 +57,8 @@ def test_workspace_size_valid_and_monotone():
     (dict(dtype=7), mok.MOK_ERR_INVALID_ARG),
     (dict(minibatch_rows=100), mok.MOK_ERR_INVALID_ARG),
     (dict(gather_sm_fraction=1.5), mok.MOK_ERR_INVALID_ARG),
+    (dict(fused_cta_pairs=3), mok.MOK_ERR_INVALID_ARG),
+    (dict(gemm_cta_pairs=-1), mok.MOK_ERR_INVALID_ARG),
 ])
 def test_bad_configs_rejected_on_host(kw, code):
     with pytest.raises(mok.MokError) as ei:
@@ -83,6 +85,11 @@ def test_null_pointers_rejected_before_any_launch():
     assert rc == mok.MOK_ERR_INVALID_ARG
     rc = L.mok_get_device_status(None, None)
     assert rc == mok.MOK_ERR_INVALID_ARG
+    rc = L.mok_swiglu_quantize_mx(None, None, 128, 128, None, None, None, None)
+    assert rc == mok.MOK_ERR_INVALID_ARG
+    dummy = ctypes.c_void_p(16)  # never dereferenced: the shape check fails first
+    rc = L.mok_swiglu_quantize_mx(dummy, dummy, 100, 128, None, dummy, dummy, None)
+    assert rc == mok.MOK_ERR_UNSUPPORTED
 
 
 def test_status_strings():
@@ -97,6 +104,18 @@ def test_saved_ctx_layout_is_aligned_and_ordered():
     offs = [getattr(lay, f) for f in fields]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs)
+
+
+def test_bwd_ws_layout_inside_the_backward_workspace():
+    for dtype in (0, 1):
+        cfg = _cfg(dtype=dtype, T=300)
+        lay = mok.bwd_ws_layout(cfg)
+        offs = [getattr(lay, f) for f, _ in mok.MokBwdLayout._fields_]
+        assert all(o % 256 == 0 for o in offs) and offs == sorted(offs)
+        assert lay.total == mok.workspace_size(cfg)[2]
+        R = mok.max_padded_rows(cfg)
+        assert lay.da - lay.dy >= R * 256 * 2 and lay.dx - lay.db >= R * 256 * 2
+        assert lay.total - lay.dl_sel >= 300 * 2 * 4
 
 
 def _plan(**kw):
@@ -118,9 +137,13 @@ def test_fused_plan_honours_explicit_knobs():
     # 1 MiB of BF16 rows of 256 elements = 2048 rows; an uncapped ring holds every padded row
     assert q["ring_rows"] == 2048
     assert _plan()["ring_rows"] == mok.max_padded_rows(_cfg())
-    # MXFP8 layers and rings below 512 rows run one CTA per tile
+    # MXFP8 layers and rings below 512 rows run one CTA per tile by default;
+    # the config forces either where the shape allows
     assert _plan(dtype=1)["cta_pairs"] == 0
     assert _plan(ring_bytes=256 * 256 * 2, T=4096)["cta_pairs"] == 0
+    assert _plan(dtype=1, fused_cta_pairs=mok.MOK_PAIRS_ON)["cta_pairs"] == 1
+    assert _plan(fused_cta_pairs=mok.MOK_PAIRS_OFF)["cta_pairs"] == 0
+    assert _plan(d_model=384, fused_cta_pairs=mok.MOK_PAIRS_ON)["cta_pairs"] == 0
 
 
 def test_fused_plan_shape_rules():

@@ -13,6 +13,7 @@ import pytest
 import torch
 
 from combine_top_routing_gb300 import inputs as I
+from combine_top_routing_gb300 import mok
 from oracle import oracle as O
 from mokhelp import bf16_np, check_close, expert_weights_np, f32_np, make_layer, sha
 
@@ -86,8 +87,15 @@ def test_backward_small_full_parity(name):
     pad = layer.ctx_view("pad_offsets", torch.int32, (w.E + 1,)).cpu().numpy()
     q = pad[ids] + slot_pos - off[ids]
     R = layer.rows_pad
-    dy_rows = bf16_np(layer.bws[256:256 + R * w.d * 2].view(torch.bfloat16).view(R, w.d))
+    dy_rows = bf16_np(_bwd_view(layer, "dy", torch.bfloat16, (R, w.d)))
     assert np.array_equal(dy_rows[q.reshape(-1)], dy_ref.reshape(-1, w.d))
+    # B5 at its step boundary: the GPU's dx rows and chosen-logit gradients
+    # through the oracle's reverse dispatch (contract: fp32, slot rows then
+    # router terms in ascending j, fused multiply-adds) -- dX bit for bit
+    dx_rows = bf16_np(_bwd_view(layer, "dx", torch.bfloat16, (R, w.d)))
+    dl_sel = f32_np(_bwd_view(layer, "dl_sel", torch.float32, (w.T, w.k)))
+    dX_step = O.rev_dispatch(dx_rows, q.astype(np.int32), ids, dl_sel, Wr)
+    assert np.array_equal(bf16_np(layer.dX), dX_step)
     dg = f32_np(layer.dgates)
     assert np.all(np.abs(dg - dg_ref) <= 1e-5 * (1 + np.abs(dg_ref)) + 1e-6 * w.d)
     check_close(f32_np(layer.dlogits), g["dlogits"], what="dlogits")
@@ -116,16 +124,22 @@ def test_backward_small_full_parity(name):
         assert not layer.grads["d_gate"][e].any() and not layer.grads["d_down"][e].any()
 
 
-def test_backward_full_size_sampled():
-    w = I.WORKLOADS["dsv3_fwdbwd"]
+@pytest.mark.parametrize("name,ntok", [("dsv3_fwdbwd", 16), ("mixtral_bf16", 16)])
+def test_backward_full_size_sampled(name, ntok):
+    """Full-size layers: the DeepSeek-V3-shaped MXFP8 forward+backward and the
+    Mixtral-shaped BF16 one (its dgrad GEMM has K = 2F = 28672).  dX, dgates
+    and dlogits on sampled tokens end to end; the weight gradients of the
+    hottest and the coldest expert at their step boundary (all their rows)."""
+    w = I.WORKLOADS[name]
     layer, inp = _run(w)
     ids, gates = _routing(layer, w)
     rng = np.random.default_rng(7)
-    tokens = np.sort(rng.choice(w.T, 4, replace=False))
+    tokens = np.sort(rng.choice(w.T, ntok, replace=False))
     x = bf16_np(inp["x"])
     Wr = f32_np(inp["Wr"])
+    bias = None if inp["bias"] is None else f32_np(inp["bias"])
     ge = lambda e: expert_weights_np(inp, e)
-    f = O.forward(x, Wr, None, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype, tokens=tokens,
+    f = O.forward(x, Wr, bias, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype, tokens=tokens,
                   ids=ids[tokens], gates=gates[tokens])
     dY = bf16_np(inp["dY"][torch.from_numpy(tokens).cuda()])
     g = O.backward(f, dY, x, Wr, ge, E=w.E, k=w.k, kind=_kind(w), mode=w.dtype)
@@ -152,7 +166,6 @@ def _check_wgrad_step(layer, inp, w, ids, experts):
     """B4 at its step boundary: the GPU's saved h and its dy, da, db rows and
     the tokens' x rows through the oracle's weight-gradient step, for the
     given experts, against the GPU's dW."""
-    bw = layer.bws
     R = layer.rows_pad
     x = bf16_np(inp["x"])
     counts = layer.ctx_view("counts", torch.int32, (w.E,)).cpu().numpy()
@@ -160,10 +173,9 @@ def _check_wgrad_step(layer, inp, w, ids, experts):
     off = layer.ctx_view("offsets", torch.int32, (w.E + 1,)).cpu().numpy()
     row_tok = layer.ctx_view("row_tok", torch.int32, (w.S,)).cpu().numpy()
     h = layer.ctx_view("h", torch.bfloat16, (R, w.F))
-    fields = _bwd_offsets(layer)
-    dy_rows = bw[fields["dy"]:fields["dy"] + R * w.d * 2].view(torch.bfloat16).view(R, w.d)
-    da = bw[fields["da"]:fields["da"] + R * w.F * 2].view(torch.bfloat16).view(R, w.F)
-    db = bw[fields["db"]:fields["db"] + R * w.F * 2].view(torch.bfloat16).view(R, w.F)
+    dy_rows = _bwd_view(layer, "dy", torch.bfloat16, (R, w.d))
+    da = _bwd_view(layer, "da", torch.bfloat16, (R, w.F))
+    db = _bwd_view(layer, "db", torch.bfloat16, (R, w.F))
     for e in experts:
         if counts[e] == 0:
             continue
@@ -176,20 +188,11 @@ def _check_wgrad_step(layer, inp, w, ids, experts):
         check_close(bf16_np(layer.grads["d_up"][e]), ref["dWu"], what=f"dW_u[{e}]")
 
 
-def _bwd_offsets(layer):
-    """Byte offsets of the backward workspace fields (mirrors the library's
-    carving order: 256-byte aligned, in declaration order)."""
-    w = layer.w
-    R, d, F = layer.rows_pad, w.d, w.F
-    mx = w.dtype == "mxfp8"
-    sizes = [("status", 256), ("dy", R * d * 2), ("dy_q", R * d if mx else 0),
-             ("dy_s", R * d // 32 if mx else 0), ("da", R * F * 2), ("db", R * F * 2)]
-    out, cur = {}, 0
-    for name, n in sizes:
-        cur = (cur + 255) // 256 * 256
-        out[name] = cur
-        cur += n
-    return out
+def _bwd_view(layer, field, dtype, shape):
+    """A view of one intermediate of the backward workspace (mok_bwd_ws_layout)."""
+    off = getattr(mok.bwd_ws_layout(layer.cfg), field)
+    n = int(np.prod(shape)) * torch.tensor([], dtype=dtype).element_size()
+    return layer.bws[off:off + n].view(dtype).view(shape)
 
 
 def test_backward_bit_reproducible():
@@ -207,7 +210,7 @@ def test_backward_bit_reproducible():
 
 
 @pytest.mark.parametrize("name", ["mx_pairs", "bf16_many_empty", "mx_sources", "mx_bigk"])
-def test_wgrad_cta_pairs_equal_single_cta(name, monkeypatch):
+def test_wgrad_cta_pairs_equal_single_cta(name):
     """The weight-gradient GEMMs on CTA pairs (256 dW rows per pair tile)
     give the same bits as one CTA per 128-row tile, experts without rows
     included (their dW blocks are zero)."""
@@ -217,7 +220,7 @@ def test_wgrad_cta_pairs_equal_single_cta(name, monkeypatch):
     layer.forward()
     grads = {}
     for pair in ("0", "1"):
-        monkeypatch.setenv("MOK_GEMM_PAIR", pair)
+        layer.cfg.c.gemm_cta_pairs = mok.MOK_PAIRS_ON if pair == "1" else mok.MOK_PAIRS_OFF
         layer.backward(inp["dY"])
         torch.cuda.synchronize()
         grads[pair] = {k: v.clone() for k, v in layer.grads.items()}

@@ -79,9 +79,17 @@ def test_forward_full_size_sampled(name):
     assert layer.status() == 0
     R = Routed(layer)
     torch.cuda.synchronize()
+    # 64 tokens: one routed to the hottest expert, one to the coldest expert
+    # that has rows, the rest drawn at random
+    ids = R.ids.cpu().numpy()
+    counts = np.bincount(ids.reshape(-1), minlength=w.E)
+    hot = int(np.argmax(counts))
+    cold = int(np.argmin(np.where(counts > 0, counts, 1 << 30)))
     rng = np.random.default_rng(w.seed + 100)
-    ntok = 6 if w.E > 64 else 24
-    tokens = np.sort(rng.choice(w.T, ntok, replace=False))
+    picked = {int(np.nonzero((ids == hot).any(1))[0][0]), int(np.nonzero((ids == cold).any(1))[0][0])}
+    rest = rng.permutation(w.T)
+    tokens = np.sort(np.array(list(picked) + [int(t) for t in rest if t not in picked][:64 - len(picked)]))
+    assert len(tokens) == 64 and (ids[tokens] == hot).any() and (ids[tokens] == cold).any()
     ref = _oracle_out(w, inp, R, tokens)
     check_close(bf16_np(out[torch.from_numpy(tokens).cuda()]), ref["out"], what="out")
     ystage = layer.ctx_view("ystage", torch.bfloat16, (w.T, w.k, w.d))

@@ -68,18 +68,20 @@ def test_fused_equals_stepwise_bit_exact(name):
 
 
 @pytest.mark.parametrize("name", ["mx_skew_sources", "bf16"])
-def test_fused_cta_pairs_equal_single_cta_bit_exact(name, monkeypatch):
+def test_fused_cta_pairs_equal_single_cta_bit_exact(name):
     """d a multiple of 256: the GEMM role on CTA pairs (256-row tiles, ghost
     odd halves for experts with an odd number of row tiles) gives the same
     bits as one CTA per 128-row tile."""
     w = CASES[name]
     layer, _ = make_layer(w)
-    monkeypatch.setenv("MOK_FUSED_PAIR", "1")
+    layer.cfg.c.fused_cta_pairs = mok.MOK_PAIRS_ON
     paired = layer.forward().clone()
     torch.cuda.synchronize()
     assert layer.status() == 0
-    assert mok.fused_plan(layer.cfg)["gather_ctas"] % 2 == 0
-    monkeypatch.setenv("MOK_FUSED_PAIR", "0")
+    plan = mok.fused_plan(layer.cfg)
+    assert plan["cta_pairs"] == 1 and plan["gather_ctas"] % 2 == 0
+    layer.cfg.c.fused_cta_pairs = mok.MOK_PAIRS_OFF
+    assert mok.fused_plan(layer.cfg)["cta_pairs"] == 0
     single = layer.forward().clone()
     torch.cuda.synchronize()
     assert layer.status() == 0
@@ -98,6 +100,29 @@ def test_fused_bit_identical_across_splits_minibatches_rings():
         torch.cuda.synchronize()
         assert layer.status() == 0, (frac, mb, ring_rows)
         hashes[(frac, mb, ring_rows)] = sha(out)
+    assert len(set(hashes.values())) == 1, hashes
+
+
+def test_full_size_skewed_layer_bit_identical_across_repeats_splits_minibatches():
+    """[miku]: results are bit-identical whatever the schedule.  The
+    DeepSeek-V3-shaped layer with Zipf-skewed routing (hottest expert about
+    20x the mean), 64 source buffers and a 256 MB token ring that wraps:
+    three repeats at the shape-chosen knobs, then every gather share in
+    {1/8, 1/4, 1/3} x minibatch in {64, 128, 256}, all with the same output
+    bytes."""
+    w = I.WORKLOADS["dsv3_skew_ep"]
+    layer, _ = make_layer(w)
+    plan = mok.fused_plan(layer.cfg)
+    assert plan["ring_rows"] < layer.rows_pad   # the ring wraps
+    hashes = {}
+    for rep in range(3):
+        hashes[("auto", rep)] = sha(layer.forward())
+    for frac, mb in itertools.product((0.125, 0.25, 1 / 3), (64, 128, 256)):
+        layer.cfg.c.gather_sm_fraction = frac
+        layer.cfg.c.minibatch_rows = mb
+        hashes[(frac, mb)] = sha(layer.forward())
+    torch.cuda.synchronize()
+    assert layer.status() == 0
     assert len(set(hashes.values())) == 1, hashes
 
 

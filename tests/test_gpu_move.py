@@ -142,3 +142,40 @@ def test_combine_bit_exact(T, k, d):
     torch.cuda.synchronize()
     ref = O.combine(bf16_np(y), f32_np(gates))
     assert np.array_equal(bf16_np(out), ref)
+
+
+def test_swiglu_h_quantisation_bit_exact_given_the_same_fp32_input():
+    """MXFP8 quantisation of h ([kucoin] §02: fused into SwiGLU), checked the
+    way the contract states it: given the GPU's own fp32 SwiGLU output, its
+    E4M3 codes and E8M0 scales (blocks of 32 along F) equal the oracle's
+    quantisation of those fp32 values bit for bit.  mok_swiglu_quantize_mx
+    runs the FFN1 epilogue's own SwiGLU and block quantiser on fp32 a, b
+    from memory.  Rows cover the edge cases: an all-zero block (scale byte 0),
+    rows scaled by 2^-20 .. 2^6 (h from about 2^-80 to 2^12; elements far
+    below their block maximum get subnormal codes), a block whose maximum has
+    mantissa 1.111b (saturates at 448), and random N(0,1) accumulators."""
+    rows, F = 256, 512
+    g = torch.Generator(device="cpu").manual_seed(61)
+    a = torch.randn((rows, F), generator=g, dtype=torch.float64)
+    b = torch.randn((rows, F), generator=g, dtype=torch.float64)
+    row_scale = 2.0 ** torch.randint(-20, 7, (rows, 1), generator=g).double()
+    a, b = a * row_scale, b * row_scale
+    a[3, 32:64] = 0.0                                  # h = 0 over one block: scale byte 0
+    b[5] *= 2.0 ** -20                                 # tiny h: scale exponents near -60
+    a[7, :32], b[7, :32] = 20.0, 192.0                 # silu(20) = 20 in fp32: h = 3840 = 1.111b x 2^11,
+    #                                                    which the OCP scale rule saturates to 448 x 2^3
+    a, b = a.float().cuda(), b.float().cuda()
+    h = torch.empty((rows, F), dtype=torch.float32, device="cuda")
+    codes = torch.empty((rows, F), dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(scale_words(rows, F), dtype=torch.int32, device="cuda")
+    mok.swiglu_quantize_mx(a, b, rows, F, h, codes, scales)
+    torch.cuda.synchronize()
+    hv = h.double().cpu().numpy()
+    ref_codes, ref_scales = O.mx_quantize(hv)
+    assert np.array_equal(codes.cpu().numpy(), ref_codes)
+    assert np.array_equal(scales_to_canonical(scales, rows, F), ref_scales)
+    assert ref_scales[3, 1] == 0 and (ref_codes[3, 32:64] == 0).all()
+    assert ref_scales[7, 0] == 127 + 3 and ref_codes[7, 0] == 0x7E
+    # the fp32 SwiGLU itself: within a few fp32 ulps of the fp64 formula
+    ref_h = O.swiglu(a.double().cpu().numpy(), b.double().cpu().numpy())
+    assert np.all(np.abs(hv - ref_h) <= 1e-5 * np.abs(ref_h) + 1e-30)
