@@ -1,8 +1,13 @@
 """MoE-layer throughput on GB300: tokens/s of one forward layer (router top-k,
-layout, pull dispatch, grouped SwiGLU FFN, weighted combine) through the C ABI.
+layout, pull dispatch, grouped SwiGLU FFN, weighted combine) through the C ABI,
+and of the forward + backward layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
     python bench.py --impl reference ...   # the CPU oracle on the host cores
+
+Default: the DeepSeek-V3-shaped MXFP8 forward (T 16384, d 7168, E 256, k 8,
+F 2048); the same line carries the MXFP8 forward + backward at T 8192, the
+Zipf-skewed layer's achieved expert load, and the Mixtral-shaped BF16 layer.
 
 One JSON line on rank 0.  N > 1 runs under torch.distributed.run: every rank
 runs its own independent layer on its own batch of T tokens (the layer is
@@ -26,7 +31,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd on 1 GB300; % of FP8 TC / HBM roofline"
-DEFAULT_WORKLOAD = "mixtral_bf16"
+DEFAULT_WORKLOAD = "dsv3_mxfp8"
+# forward + backward workload of each forward workload (the MXFP8 backward is
+# quoted at T 8192), and the secondary BF16 layer reported beside the primary
+FWD_BWD_OF = {"dsv3_mxfp8": "dsv3_fwdbwd", "dsv3_skew_ep": "dsv3_fwdbwd"}
+SECONDARY = "mixtral_bf16"
+# Tensor-pipe rate of tcgen05 MXFP8 (kind::mxf8f6f4, block-scaled, M 128 N 256)
+# on shared-memory-resident tiles, one issuing thread per SM on all 152 SMs of
+# this GB300, measured by a timing-only program; and the nameplate peaks.
+MXFP8_PIPE_TFLOPS = 4850.0
+NOMINAL = {"mxfp8_tflops": 4500.0, "bf16_tflops": 2250.0, "hbm_gbs": 8000.0}
+L2_FLUSH_BYTES = 256 << 20
 
 
 def _args():
@@ -38,6 +53,8 @@ def _args():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-backward", action="store_true")
+    p.add_argument("--no-secondary", action="store_true",
+                   help="skip the secondary (Mixtral-shaped BF16) layer and the skew report")
     p.add_argument("--sweep", action="store_true",
                    help="also time the fused forward over gather SM fraction x minibatch")
     p.add_argument("--cpu-sample-tokens", type=int, default=0)
@@ -178,15 +195,12 @@ def _layer_bytes(w):
 
 
 # DRAM bytes (read + write) per launch of the fused kernel, from one ncu capture
-# (`--metrics dram__bytes_read.sum,dram__bytes_write.sum`, one pass) of
-# `python bench.py --steps 2 --warmup 3 --no-cpu-baseline --no-backward [--workload W]`,
-# summarised in profiles/k_moe_fused_traffic.md, keyed by workload and CTA pairs, with a
-# hash of the kernel's sources at capture time: once the kernel changes, traffic is null.
-FUSED_TRAFFIC = {
-    ("mixtral_bf16", 1): {"bytes": 4915918848 + 789699584, "src_sha": "27c6a11e85b154b5"},
-    ("dsv3_mxfp8", 0): {"bytes": 17070225152 + 3360603904, "src_sha": "27c6a11e85b154b5"},
-    ("dsv3_skew_ep", 0): {"bytes": 17291281152 + 3360698368, "src_sha": "27c6a11e85b154b5"},
-}
+# (`--metrics dram__bytes_read.sum,dram__bytes_write.sum`) of a case small enough
+# to capture -- the same per-expert shape with the tokens and experts cut by
+# `scale` -- multiplied by `scale` (the weights, activations and staging all
+# grow in proportion), keyed by workload and CTA pairs, with a hash of the
+# kernel's sources at capture time: once the kernel changes, traffic is null.
+FUSED_TRAFFIC = {}
 FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h")
 
 
@@ -203,7 +217,7 @@ def _fused_traffic(workload: str, pairs: int):
     e = FUSED_TRAFFIC.get((workload, pairs))
     if e is None or e["src_sha"] != _fused_src_sha():
         return None
-    return e["bytes"]
+    return {"bytes": e["bytes_small"] * e["scale"], "captured": e["case"], "scale": e["scale"]}
 
 
 def _dispatch_bytes(w):
@@ -231,19 +245,24 @@ def run_reference(args):
     from combine_top_routing_gb300 import inputs as I
     from oracle import oracle as O
     w = _workload(args)
-    inp = I.make_inputs(w, device="cpu")
+    # inputs are drawn where the GPU arm draws them (same values); the oracle
+    # converts each expert's weights to fp64 on the host when it uses them
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = I.make_inputs(w, device=dev)
     kind = O.SOFTMAX if w.router == "softmax" else O.SIGMOID
 
     def bf(t):
-        return O.bf16_values(t.contiguous().view(torch.int16).numpy().view(np.uint16))
+        return O.bf16_values(t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
 
-    # 256 tokens a step: the oracle's per-call set-up (every expert's weights
-    # converted to fp64) stays a minor part of a step (~1.5 s on 16 Arm cores)
-    ntok = args.cpu_sample_tokens or 256
+    # tokens per step: every step pays the fp64 conversion and MXFP8
+    # quantisation of each expert its tokens touch (~0.3 s per expert at the
+    # DeepSeek-V3 shape), so steps stay a few seconds: 256 tokens over 8
+    # experts, 2 tokens (16 experts) over 256
+    ntok = min(w.T, args.cpu_sample_tokens or (256 if w.E <= 16 else 2))
     rng = np.random.default_rng(0)
     x = bf(inp["x"])
-    Wr = inp["Wr"].double().numpy()
-    bias = None if inp["bias"] is None else inp["bias"].double().numpy()
+    Wr = inp["Wr"].double().cpu().numpy()
+    bias = None if inp["bias"] is None else inp["bias"].double().cpu().numpy()
     ge = lambda e: (bf(inp["Wg"][e]), bf(inp["Wu"][e]), bf(inp["Wd"][e]))
 
     def step():
@@ -266,7 +285,8 @@ def run_reference(args):
         "config": {"workload": w.name, "T": w.T, "d_model": w.d, "experts": w.E, "top_k": w.k,
                    "d_ff": w.F, "gemm_dtype": w.dtype, "sample_tokens_per_step": ntok},
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{ntok} random tokens of {w.name} per step (full layer "
+                         "cpu_model": _cpu_model(), "rate": "measured on a token sample, not extrapolated",
+                         "sample": f"{ntok} random tokens of {w.name} (T {w.T}) per step (full layer "
                                    f"forward of those tokens, fp64 oracle)"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -274,8 +294,21 @@ def run_reference(args):
     return 0
 
 
+def _cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(w, inp_gpu, budget_s=20.0):
-    """Oracle forward on a bounded token sample, on this host's cores."""
+    """Oracle forward on a bounded token sample, on this host's cores: the rate
+    measured on the sample (per-token work is uniform once routing is fixed)."""
     import numpy as np
     import torch
 
@@ -301,8 +334,111 @@ def cpu_baseline(w, inp_gpu, budget_s=20.0):
             ntok *= 2
     cores = len(os.sched_getaffinity(0))
     return {"value": total_tok / t_total, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{total_tok} random tokens of {w.name} through the fp64 oracle forward "
-                      f"({t_total:.1f} s of CPU work)"}
+            "cpu_model": _cpu_model(), "rate": "measured on a token sample, not extrapolated",
+            "sample": f"{total_tok} random tokens of {w.name} (T {w.T}) through the fp64 oracle "
+                      f"forward, {t_total:.1f} s of CPU work; value = sampled tokens / that time"}
+
+
+class L2Flush:
+    """Writes a buffer twice the size of L2 between timed iterations, so that no
+    iteration finds the previous one's data in L2."""
+
+    def __init__(self):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.buf.fill_(0)
+
+
+def time_flushed(fn, steps, stream, flush):
+    """Mean CUDA-event time of `steps` calls of fn on `stream`, L2 flushed
+    before each call (outside the timed events)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for e0, e1 in evs:
+        flush()
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+
+
+def _expert_load(w, dev="cuda"):
+    """Achieved per-expert slot counts of workload w's routing (the router and
+    layout through the C ABI; no expert weights needed)."""
+    import torch
+
+    from combine_top_routing_gb300 import inputs as I
+    from combine_top_routing_gb300 import mok
+    inp = I.make_inputs(w, device=dev, with_weights=False)
+    cfg = mok.Config.from_workload(w)
+    ws = torch.empty(mok.workspace_size(cfg)[0], dtype=torch.uint8, device=dev)
+    x_src = I.split_sources(inp["x"], w.n_sources) if w.n_sources > 1 else [inp["x"]]
+    ids = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    gates = torch.empty((w.T, w.k), dtype=torch.float32, device=dev)
+    counts = torch.empty(w.E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    pad = torch.empty(w.E + 1, dtype=torch.int32, device=dev)
+    slot_pos = torch.empty((w.T, w.k), dtype=torch.int32, device=dev)
+    row_tok = torch.empty(w.S, dtype=torch.int32, device=dev)
+    row_j = torch.empty(w.S, dtype=torch.uint8, device=dev)
+    mok.route_layout(cfg, x_src, inp["Wr"], inp["bias"], ids, gates, None, None, counts, offsets,
+                     pad, slot_pos, row_tok, row_j, ws)
+    c = counts.cpu().double()
+    return {"workload": w.name, "hottest_over_mean": float(c.max() / c.mean()),
+            "hottest_rows": int(c.max()), "coldest_rows": int(c.min()),
+            "mean_rows": float(c.mean())}
+
+
+def _layer_line(w, layer, stream, steps, flush, peaks):
+    """Device-resident forward timing (L2 flushed between steps) of one layer."""
+    import torch
+    for _ in range(3):
+        layer.forward()
+    torch.cuda.synchronize()
+    ms = time_flushed(layer.forward, steps, stream, flush)
+    flops = _layer_flops(w)
+    peak_tc = _tc_peak(w, peaks)
+    return ms, {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
+                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6800.0)}
+
+
+def _tc_peak(w, peaks):
+    """Measured dense tensor peak for the layer's GEMM dtype: the BF16 burst
+    figure, x2 (the nominal FP8:BF16 ratio) for MXFP8."""
+    return peaks.get("bf16_tflops", 1900.0) * (2.0 if w.dtype == "mxfp8" else 1.0)
+
+
+def _fwd_bwd(w, stream, steps, flush, barrier, world):
+    """Forward + backward of the training layer of workload w (saved context,
+    weight gradients, router gradients), L2 flushed between steps."""
+    import torch
+
+    from combine_top_routing_gb300 import inputs as I
+    from combine_top_routing_gb300 import mok
+    from combine_top_routing_gb300.layer import MoELayer
+    rank = int(os.environ.get("RANK", "0"))
+    inp = I.make_inputs(I.scaled(w, seed=w.seed + 1000 * rank), device="cuda")
+    tl = MoELayer(w, inp, training=True)
+    tl.prepare_backward()
+
+    def step():
+        tl.forward()
+        tl.backward(inp["dY"])
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    ms = reduce_max(time_flushed(step, steps, stream, flush), "cuda")
+    if tl.status() != 0:
+        raise RuntimeError("device status after backward: " + mok.status_string(tl.status()))
+    del tl, inp
+    torch.cuda.empty_cache()
+    return ms
 
 
 def main():
@@ -324,12 +460,13 @@ def main():
     inp = I.make_inputs(I.scaled(w, seed=w.seed + 1000 * rank), device="cuda")
     layer = MoELayer(w, inp)
     stream = torch.cuda.current_stream()
+    flush = L2Flush()
 
     def barrier():
         if world > 1:
             dist.barrier()
 
-    # ---------------- device-resident timed region
+    # ---------------- device-resident timed region (L2 flushed between steps)
     peaks, peak_src = _peaks()
     with ClockSampler(local) as clk:
         for _ in range(max(3, args.warmup)):
@@ -337,60 +474,26 @@ def main():
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         wall0 = time.time()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            layer.forward()
-        ev1.record(stream)
-        torch.cuda.synchronize()
+        ms = time_flushed(layer.forward, args.steps, stream, flush)
         clk.mark(wall0, time.time())
     barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
     status = layer.status()
     if status != 0:
         raise RuntimeError(f"device status {mok.status_string(status)}")
     ms = reduce_max(ms, "cuda")
     value = job_throughput(w.T, world, ms)
+    flops = _layer_flops(w)
+    peak_tc = _tc_peak(w, peaks)
 
-    # ---------------- forward + backward (training layer: saved context)
-    fb_ms = None
-    if not args.no_backward:
-        tl = MoELayer(w, inp, training=True)
-        tl.prepare_backward()
-        for _ in range(max(3, args.warmup)):
-            tl.forward()
-            tl.backward(inp["dY"])
-        torch.cuda.synchronize()
-        barrier()
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        fb_steps = max(3, min(args.steps, 20))
-        f0.record(stream)
-        for _ in range(fb_steps):
-            tl.forward()
-            tl.backward(inp["dY"])
-        f1.record(stream)
-        torch.cuda.synchronize()
-        if tl.status() != 0:
-            raise RuntimeError("device status after backward: " + mok.status_string(tl.status()))
-        fb_ms = reduce_max(f0.elapsed_time(f1) / fb_steps, "cuda")
-        del tl
-        torch.cuda.empty_cache()
-
-    # ---------------- the dominant kernel (k_moe_fused) timed alone, same stream
+    # ---------------- the dominant kernel (the fused forward) timed alone, same stream
     R = _route_for_ffn(layer)
     iters = max(5, min(50, args.steps))
 
     def timed(fn):
         for _ in range(2):
             fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(iters):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / iters
+        return time_flushed(fn, iters, stream, flush)
 
     # the HBM-bound steps on their own (separate kernels, same stream)
     disp_ms = timed(lambda: mok.dispatch(layer.cfg, layer.x_src, R.ids, R.offsets, R.pad_offsets,
@@ -405,37 +508,30 @@ def main():
                               ("combine", comb_ms, _combine_bytes(w))):
         gbs = nbytes / (ms_ / 1e3) / 1e9
         hbm_steps[name] = {"ms": ms_, "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
-                           "peak_gbs": hbm_peak, "frac": gbs / hbm_peak}
+                           "peak_gbs": hbm_peak, "frac": gbs / hbm_peak,
+                           "frac_of_nominal_8tbs": gbs / NOMINAL["hbm_gbs"]}
     plan = mok.fused_plan(layer.cfg)
     fused_ms = timed(lambda: mok.moe_fused(layer.cfg, layer.x_src, layer.wstruct, R.ids, R.gates,
                                            R.counts, R.offsets, R.pad_offsets, R.row_tok, R.row_j,
                                            R.ystage, layer.out, layer.ws))
     ffn_ms = timed(lambda: _ffn(layer, R))
-    flops = _layer_flops(w)
     fused_tflops = flops / (fused_ms / 1e3) / 1e12
-    bf16_peak = peaks.get("bf16_tflops", 1900.0)
-    peak_tc = bf16_peak * (2.0 if w.dtype == "mxfp8" else 1.0)
+    launches_per_step = 8  # router split, router GEMM, top-k, 4 layout passes, fused kernel
 
     sweep = None
     if args.sweep:
         sweep = []
         for frac in (0.0625, 0.125, 0.25, 1 / 3):
             for mb in (64, 128, 256):
-                lw = MoELayer(w, inp, gather_sm_fraction=frac, minibatch_rows=mb)
-                for _ in range(2):
-                    lw.forward()
-                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s0.record(stream)
-                for _ in range(iters):
-                    lw.forward()
-                s1.record(stream)
-                torch.cuda.synchronize()
-                if lw.status() != 0:
-                    raise RuntimeError("device status in sweep: " + mok.status_string(lw.status()))
+                layer.cfg.c.gather_sm_fraction = frac
+                layer.cfg.c.minibatch_rows = mb
+                sms = timed(layer.forward)
+                if layer.status() != 0:
+                    raise RuntimeError("device status in sweep: " + mok.status_string(layer.status()))
                 sweep.append({"gather_sm_fraction": round(frac, 4), "minibatch_rows": mb,
-                              "ms_per_step": s0.elapsed_time(s1) / iters})
-                del lw
-                torch.cuda.empty_cache()
+                              "ms_per_step": sms})
+        layer.cfg.c.gather_sm_fraction = 0.0
+        layer.cfg.c.minibatch_rows = 0
 
     # ---------------- end to end through the C ABI with host buffers
     x_host = torch.empty_like(inp["x"], device="cpu").pin_memory()
@@ -460,31 +556,70 @@ def main():
     base = None
     if rank == 0 and not args.no_cpu_baseline:
         base = cpu_baseline(w, inp)
+    del pipe, R, layer, inp
+    torch.cuda.empty_cache()
+
+    # ---------------- forward + backward (training layer: saved context)
+    fb = None
+    if not args.no_backward:
+        wf = I.WORKLOADS[FWD_BWD_OF[w.name]] if w.name in FWD_BWD_OF else w
+        fb_steps = max(3, min(args.steps, 20))
+        fb_ms = _fwd_bwd(wf, stream, fb_steps, flush, barrier, world)
+        fb = {"workload": wf.name, "T": wf.T, "gemm_dtype": wf.dtype,
+              "value": job_throughput(wf.T, world, fb_ms), "unit": "tokens/s", "ms_per_step": fb_ms,
+              "tensor_frac": 3 * _layer_flops(wf) / (fb_ms / 1e3) / 1e12 / _tc_peak(wf, peaks),
+              "tensor_frac_of_nominal": 3 * _layer_flops(wf) / (fb_ms / 1e3) / 1e12 /
+                                        NOMINAL["mxfp8_tflops" if wf.dtype == "mxfp8" else "bf16_tflops"],
+              "steps": fb_steps, "l2": "flushed between timed steps"}
+
+    # ---------------- skewed layer's achieved load, secondary BF16 layer
+    skew = secondary = None
+    if not args.no_secondary:
+        skew = _expert_load(I.WORKLOADS["dsv3_skew_ep"])
+        torch.cuda.empty_cache()
+        if w.name != SECONDARY:
+            w2 = I.WORKLOADS[SECONDARY]
+            inp2 = I.make_inputs(I.scaled(w2, seed=w2.seed + 1000 * rank), device="cuda")
+            l2 = MoELayer(w2, inp2)
+            ms2, lr2 = _layer_line(w2, l2, stream, max(3, min(args.steps, 20)), flush, peaks)
+            ms2 = reduce_max(ms2, "cuda")
+            secondary = {"workload": w2.name, "T": w2.T, "gemm_dtype": w2.dtype, "pass": "forward",
+                         "value": job_throughput(w2.T, world, ms2), "unit": "tokens/s",
+                         "ms_per_step": ms2, "layer_roofline": lr2}
+            if not args.no_backward:
+                ms2b = _fwd_bwd(w2, stream, max(3, min(args.steps, 10)), flush, barrier, world)
+                secondary["fwd_bwd"] = {"value": job_throughput(w2.T, world, ms2b), "unit": "tokens/s",
+                                        "ms_per_step": ms2b,
+                                        "tensor_frac": 3 * _layer_flops(w2) / (ms2b / 1e3) / 1e12 /
+                                                       _tc_peak(w2, peaks)}
+            del l2, inp2
+            torch.cuda.empty_cache()
 
     if rank == 0:
         clocks = clk.summary(peaks.get("sm_max_mhz"))
-        launches_per_step = 8  # split, router GEMM, top-k, 4 layout passes, fused kernel
+        mx = w.dtype == "mxfp8"
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "mxfp8(e4m3+e8m0)/fp32-acc" if w.dtype == "mxfp8" else "bf16/fp32-acc",
+            "dtype": "mxfp8(e4m3+e8m0)/fp32-acc" if mx else "bf16/fp32-acc",
             "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "d_model": w.d, "experts": w.E,
                        "top_k": w.k, "d_ff": w.F, "gemm_dtype": w.dtype,
                        "router": w.router, "pass": "forward",
-                       "l2": "inputs larger than L2 (expert weights %.1f GB)" %
-                             (w.E * 3 * w.F * w.d * (1 if w.dtype == 'mxfp8' else 2) / 1e9),
+                       "l2": f"flushed between timed iterations ({L2_FLUSH_BYTES >> 20} MB written "
+                             "outside the timed events)",
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "tensor", "achieved": fused_tflops, "peak": peak_tc,
                          "unit": "TFLOP/s", "frac": fused_tflops / peak_tc,
-                         "traffic": _fused_traffic(w.name, plan["cta_pairs"]),
-                         "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + write.sum)",
+                         "traffic": None, "traffic_unit": "DRAM bytes per launch",
                          "kernel": ("k_moe_fused_pair" if plan["cta_pairs"] else "k_moe_fused")
                                    + " (pull dispatch + FFN1 + FFN2 + combine)",
                          "algorithmic": "6*S*d*F flops per launch",
                          "peak_source": f"{peak_src} bf16 burst"
-                                        + (" x2 for fp8" if w.dtype == "mxfp8" else ""),
+                                        + (" x2 (nominal fp8:bf16 ratio)" if mx else ""),
+                         "frac_of_tensor_pipe_measured": (fused_tflops / MXFP8_PIPE_TFLOPS) if mx else None,
+                         "frac_of_nominal": fused_tflops / NOMINAL["mxfp8_tflops" if mx else "bf16_tflops"],
                          "ms_per_launch": fused_ms},
             "expert_ffn_separate_kernels": {"ms": ffn_ms,
                                             "tflops": flops / (ffn_ms / 1e3) / 1e12},
@@ -492,11 +627,14 @@ def main():
             "fused_plan": plan,
             "sweep": sweep,
             "layer_roofline": {"tensor_frac": flops / (ms / 1e3) / 1e12 / peak_tc,
+                               "tensor_frac_of_nominal": flops / (ms / 1e3) / 1e12 /
+                                   NOMINAL["mxfp8_tflops" if mx else "bf16_tflops"],
                                "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 /
-                                           peaks.get("hbm_gbs", 6800.0)},
-            "fwd_bwd": None if fb_ms is None else {
-                "value": job_throughput(w.T, world, fb_ms), "unit": "tokens/s", "ms_per_step": fb_ms,
-                "tensor_frac": 3 * flops / (fb_ms / 1e3) / 1e12 / peak_tc},
+                                           peaks.get("hbm_gbs", 6800.0),
+                               "hbm_frac_of_nominal": _layer_bytes(w) / (ms / 1e3) / 1e9 / NOMINAL["hbm_gbs"]},
+            "fwd_bwd": fb,
+            "expert_load_skewed": skew,
+            "secondary": secondary,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2,
                     "how": "mok_moe_forward per step from pinned host x to pinned host out; copy-in, "
@@ -506,6 +644,11 @@ def main():
             "clocks": clocks,
             "cpu_baseline": base,
         }
+        tr = _fused_traffic(w.name, plan["cta_pairs"])
+        if tr is not None:
+            line["roofline"]["traffic"] = tr["bytes"]
+            line["roofline"]["traffic_how"] = (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
+                                               f"launch at {tr['captured']}, x{tr['scale']}")
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
