@@ -327,6 +327,50 @@ def forward(x, Wr, bias, get_expert, *, E, k, kind, mode, tokens=None,
 
 
 # ---------------------------------------------------------------------------
+# Error scales of the reductions
+# ---------------------------------------------------------------------------
+# A sum of K terms whose factors each carry an independent relative rounding
+# error of size u (BF16 storage, an MXFP8 code) is off by about u times the
+# root-sum-square of its terms -- whatever the sum itself is, since the terms
+# can cancel to near zero.  These give that scale for every reduction of the
+# backward, propagated through the linear maps that follow it, so a
+# comparison can measure an element's error against it.
+
+def terms_rss(A, B):
+    """sqrt(sum_r (A[r, i] B[r, j])^2) for every element (i, j) of A^T B."""
+    A, B = _f64(A), _f64(B)
+    return np.sqrt((A * A).T @ (B * B))
+
+
+def gate_grad_rss(dY, ystage):
+    """Terms' root-sum-square of dgates[t, j] = <dY[t], y_tj>: [T, k]."""
+    dY, ystage = _f64(dY), _f64(ystage)
+    return np.sqrt(np.einsum("tc,tjc->tj", dY * dY, ystage * ystage))
+
+
+def router_bwd_rss(scores, ids, gates, dg_rss, kind):
+    """Error scale of dlogits [T, E] from the dgates scale: the router backward
+    is linear in dgates, dl_j = sum_j' J_jj' dg_j' with
+    J = diag(g) (I - 1 g^T) (softmax) or diag(s (1 - s) / sum_sel s) (I - 1 g^T)
+    (sigmoid), so independent errors of scale dg_rss map to
+    sqrt(sum_j' J_jj'^2 dg_rss_j'^2).  Zero off the chosen experts."""
+    scores, gates, dg_rss = _f64(scores), _f64(gates), _f64(dg_rss)
+    ids = np.asarray(ids, dtype=np.int64)
+    T, k = ids.shape
+    sel = np.take_along_axis(scores, ids, axis=1)
+    M = np.eye(k)[None, :, :] - gates[:, None, :]            # I - 1 g^T, [T, k, k]
+    if kind == SOFTMAX:
+        row = gates
+    else:
+        row = sel * (1.0 - sel) / sel.sum(axis=1, keepdims=True)
+    J = row[:, :, None] * M
+    rss_sel = np.sqrt(np.einsum("tjl,tl->tj", J * J, dg_rss * dg_rss))
+    out = np.zeros((T, scores.shape[1]))
+    np.put_along_axis(out, ids, rss_sel, axis=1)
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Backward
 # ---------------------------------------------------------------------------
 
@@ -376,10 +420,11 @@ def expert_dgrad(dy, a_saved, b_saved, Wg, Wu, Wd, mode):
     return dict(dh=dh, da=da, db=db, dx=dx)
 
 
-def expert_wgrad(dy, h_saved, da, db, xe, mode):
+def expert_wgrad(dy, h_saved, da, db, xe, mode, rss=False):
     """B4 for one expert: dW_d = dy^T h, dW_g = da^T xe, dW_u = db^T xe,
     K = the expert's rows.  mxfp8: every operand quantised along the rows
-    (zero-padded to a multiple of 32).  Stored as BF16 unless exact."""
+    (zero-padded to a multiple of 32).  Stored as BF16 unless exact.
+    rss: also the root-sum-square of each element's terms (terms_rss)."""
     ops = [_f64(v) for v in (dy, h_saved, da, db, xe)]
     if mode == "mxfp8":
         ops = [mx_qdq_rows_padded(v) for v in ops]
@@ -389,7 +434,11 @@ def expert_wgrad(dy, h_saved, da, db, xe, mode):
     dWu = db_.T @ xe_
     if mode != "exact":
         dWd, dWg, dWu = bf16_round(dWd), bf16_round(dWg), bf16_round(dWu)
-    return dict(dWd=dWd, dWg=dWg, dWu=dWu)
+    out = dict(dWd=dWd, dWg=dWg, dWu=dWu)
+    if rss:
+        out.update(dWd_rss=terms_rss(dy_, h_), dWg_rss=terms_rss(da_, xe_),
+                   dWu_rss=terms_rss(db_, xe_))
+    return out
 
 
 def router_bwd(x, Wr, scores, ids, gates, dgates, kind):
@@ -441,11 +490,13 @@ def chosen_logit_grads(dlogits, ids):
     return np.take_along_axis(_f64(dlogits), np.asarray(ids, dtype=np.int64), axis=1)
 
 
-def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode):
+def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode, rss=False):
     """Full backward of ``forward`` (all tokens of that call).
 
     Quantisers are straight-through (treated as identity); routing is
-    piecewise constant so only the chosen logits get gradient."""
+    piecewise constant so only the chosen logits get gradient.  rss: also
+    the error scales of the reductions (dgates_rss, dlogits_rss, dWr_rss,
+    and dW*_rss per expert; see terms_rss)."""
     r, lay = fwd["router"], fwd["layout"]
     exact = mode == "exact"
     dY = _f64(dY)
@@ -463,6 +514,9 @@ def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode):
         lo, hi = int(off[e]), int(off[e + 1])
         if hi == lo:
             grads[e] = dict(dWd=np.zeros((d, F)), dWg=np.zeros((F, d)), dWu=np.zeros((F, d)))
+            if rss:
+                grads[e].update(dWd_rss=np.zeros((d, F)), dWg_rss=np.zeros((F, d)),
+                                dWu_rss=np.zeros((F, d)))
             continue
         Wg, Wu, Wd = get_expert(e)
         f = fwd["experts"][e]
@@ -471,10 +525,15 @@ def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode):
         g = expert_dgrad(dy_rows[lo:hi], a_s, b_s, Wg, Wu, Wd, mode)
         dx_rows[lo:hi] = g["dx"]
         xe_rows = fwd["dispatch"]["xe"][lo:hi]
-        grads[e] = expert_wgrad(dy_rows[lo:hi], h_s, g["da"], g["db"], xe_rows, mode)
+        grads[e] = expert_wgrad(dy_rows[lo:hi], h_s, g["da"], g["db"], xe_rows, mode, rss=rss)
     xs = _f64(x)[fwd["tokens"]]
     rb = router_bwd(xs, Wr, r["scores"], r["ids"], r["gates"], dgates, kind)
     dl_sel = chosen_logit_grads(rb["dlogits"], r["ids"])
     dX = rev_dispatch(dx_rows, lay["slot_pos"], r["ids"], dl_sel, Wr, exact=exact)
-    return dict(dX=dX, dgates=dgates, dlogits=rb["dlogits"], dWr=rb["dWr"],
-                dxr=rb["dxr"], dy_rows=dy_rows, dx_rows=dx_rows, experts=grads)
+    out = dict(dX=dX, dgates=dgates, dlogits=rb["dlogits"], dWr=rb["dWr"],
+               dxr=rb["dxr"], dy_rows=dy_rows, dx_rows=dx_rows, experts=grads)
+    if rss:
+        dg_rss = gate_grad_rss(dY, fwd["ystage"])
+        dl_rss = router_bwd_rss(r["scores"], r["ids"], r["gates"], dg_rss, kind)
+        out.update(dgates_rss=dg_rss, dlogits_rss=dl_rss, dWr_rss=terms_rss(dl_rss, xs))
+    return out

@@ -16,9 +16,22 @@ from combine_top_routing_gb300.layer import MoELayer
 from oracle import oracle as O
 
 # Tolerances for BF16 / fp32-accumulated outputs and gradients (GPU vs oracle):
-# relative L2 error, and max-abs error |got - ref| / max(1, |ref|, RMS(ref)).
+# relative L2 error, and max-abs error measured per element in units of
+# max(1, |ref_i|, scale_i): absolute for O(1) values, relative for values
+# above 1 (one BF16 ulp at |v| in [4, 8) is 0.031 > 2e-2), and, for the
+# elements of a reduction, relative to the root-sum-square of its terms
+# (scale_i, from the oracle's terms_rss family): a sum whose terms carry
+# independent roundings is off by a multiple of that, however far the sum
+# itself cancels.
 REL_L2 = 5e-3
 MAX_ABS = 2e-2
+# MXFP8 weight gradients compared end to end (the oracle's own forward and
+# backward): the GPU's h, dy, da, db and the oracle's can differ by one BF16
+# ulp, and the weight-gradient GEMMs re-quantise them to MXFP8 along the token
+# rows, so a fraction phi of the E4M3 codes can land one step (at most 2^-3 of
+# the element) apart.  Independent flips add in quadrature: against the terms'
+# root-sum-square the error is at most 2^-3 sqrt(phi); 2^-4 admits phi <= 1/4.
+MAX_ABS_MX_CHAIN = 2.0 ** -4
 
 
 def bf16_np(t: torch.Tensor) -> np.ndarray:
@@ -40,32 +53,27 @@ def scales_to_canonical(words: torch.Tensor | np.ndarray, rows: int, K: int) -> 
     return out
 
 
-def check_close(got: np.ndarray, ref: np.ndarray, rel=REL_L2, mabs=MAX_ABS, what=""):
+def check_close(got: np.ndarray, ref: np.ndarray, rel=REL_L2, mabs=MAX_ABS, what="", scale=None):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     err = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-    # max-abs in units of max(1, |ref_i|, RMS(ref)): absolute for O(1) tensors,
-    # relative for large elements (one BF16 ulp at |v| in [4, 8) is 0.031 >
-    # 2e-2), and relative to the tensor's scale for sums whose elements can
-    # cancel to near zero (gate gradients are dot products over d)
-    if got.size:
-        rms = float(np.sqrt(np.mean(ref * ref)))
-        mx = (np.abs(got - ref) / np.maximum(max(1.0, rms), np.abs(ref))).max()
-    else:
-        mx = 0.0
+    unit = np.maximum(1.0, np.abs(ref))
+    if scale is not None:
+        unit = np.maximum(unit, np.asarray(scale, dtype=np.float64))
+    d = np.abs(got - ref)
+    mx = float((d / unit).max()) if got.size else 0.0
     diag = os.environ.get("MOK_TEST_DIAG")
     if diag and got.size:
-        d = np.abs(got - ref)
-        i = int(np.argmax(d))
+        i = int(np.argmax(d / unit))
         with open(diag, "a") as f:
             f.write(json.dumps({
                 "test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0], "what": what,
                 "n": int(got.size), "rel_l2": float(err), "max_abs": float(d.max()),
-                "ref_at_max": float(ref.reshape(-1)[i]), "ref_rms": float(np.sqrt(np.mean(ref * ref))),
-                "max_units_1_ref": float((d / np.maximum(1.0, np.abs(ref))).max()),
-                "max_units_1_ref_rms": float(mx)}) + "\n")
+                "max_units": mx, "ref_at_max": float(ref.reshape(-1)[i]),
+                "unit_at_max": float(unit.reshape(-1)[i]),
+                "max_units_1_ref": float((d / np.maximum(1.0, np.abs(ref))).max())}) + "\n")
     assert err <= rel and mx <= mabs, f"{what}: rel_l2={err:.3e} max_abs={mx:.3e}"
     return err, mx
 

@@ -232,3 +232,47 @@ def test_mxfp8_backward_close_to_exact():
         for key in ("dWd", "dWg", "dWu"):
             assert rel(res["bf16"]["experts"][e][key], res["exact"]["experts"][e][key]) < 1e-2
             assert rel(res["mxfp8"]["experts"][e][key], res["exact"]["experts"][e][key]) < 1.5e-1
+
+
+# ---------------------------------------------------------------------------
+# Error scales of the reductions (used as comparison units by the GPU tests)
+# ---------------------------------------------------------------------------
+
+def test_terms_rss_brute_force():
+    rng = np.random.default_rng(50)
+    A, B = rng.standard_normal((7, 3)), rng.standard_normal((7, 4))
+    got = O.terms_rss(A, B)
+    for i in range(3):
+        for j in range(4):
+            assert np.isclose(got[i, j], np.sqrt(sum((A[r, i] * B[r, j]) ** 2 for r in range(7))))
+    # one term: the scale is the magnitude of the sum itself
+    assert np.allclose(O.terms_rss(A[:1], B[:1]), np.abs(A[:1].T @ B[:1]))
+
+
+def test_gate_grad_rss_brute_force():
+    rng = np.random.default_rng(51)
+    dY, y = rng.standard_normal((3, 5)), rng.standard_normal((3, 2, 5))
+    got = O.gate_grad_rss(dY, y)
+    for t in range(3):
+        for j in range(2):
+            assert np.isclose(got[t, j], np.sqrt(np.sum((dY[t] * y[t, j]) ** 2)))
+
+
+@pytest.mark.parametrize("kind", [O.SOFTMAX, O.SIGMOID])
+def test_router_bwd_rss_uses_the_jacobian_of_the_router_backward(kind):
+    """router_bwd is linear in dgates: its Jacobian, taken column by column
+    from router_bwd itself, propagates per-gate scales in quadrature."""
+    rng = np.random.default_rng(52 + kind)
+    T, d, E, k = 5, 8, 6, 3
+    x, Wr = rng.standard_normal((T, d)), rng.standard_normal((E, d))
+    r = O.router(x, Wr, None, k, kind)
+    dg_rss = rng.uniform(0.5, 2.0, (T, k))
+    got = O.router_bwd_rss(r["scores"], r["ids"], r["gates"], dg_rss, kind)
+    base = O.router_bwd(x, Wr, r["scores"], r["ids"], r["gates"], np.zeros((T, k)), kind)["dlogits"]
+    want = np.zeros((T, E))
+    for jp in range(k):
+        unit = np.zeros((T, k))
+        unit[:, jp] = 1.0
+        col = O.router_bwd(x, Wr, r["scores"], r["ids"], r["gates"], unit, kind)["dlogits"] - base
+        want += (col * dg_rss[:, jp:jp + 1]) ** 2
+    assert np.allclose(got, np.sqrt(want), rtol=1e-12, atol=1e-15)
