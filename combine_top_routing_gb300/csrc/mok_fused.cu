@@ -701,8 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ids to both CTAs through a cluster-wide queue; the even CTA issues the MMAs
 // and scale copies; both CTAs run the epilogue of their own rows.  When an
 // expert has an odd number of row tiles its last pair tile has a ghost odd
-// half: the odd CTA loads the even half's rows again (already waited for and
-// resident, so the loads hit L2), stores nothing and signals no counter.  Gather CTAs come in pairs and a pair
+// half: the odd CTA loads its A operand from rows past the end of the tensor
+// (TMA fills zeros without reading memory), stores nothing and signals no
+// counter.  Gather CTAs come in pairs and a pair
 // enters the GEMM role only once both of its CTAs have finished gathering, so
 // a pair never holds a tile while one of its CTAs waits in the gather role.
 // Tiles keep the single-CTA kernel's per-row arithmetic, so results are
@@ -885,20 +886,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     report_timeout(a.status, abort_flag);  // a schedule bug: stop, touch nothing
                     break;
                 }
-                // a ghost half loads the even half's rows (resident, results discarded)
+                // a ghost half waits for the even half's rows and loads its A
+                // operand from rows past the end of the tensor (TMA fills zeros and
+                // reads no memory); its results are discarded
                 const int ma = jb.ghost ? jb.m0 : m;
                 if (jb.f1 ? !spin_ge(&ready[ma], 2, a, abort_flag) : !spin_ge(&h_done[ma], 4 * a.NT1, a, abort_flag))
                     break;
                 fence_proxy_async_global();
                 const int kst = jb.f1 ? a.k1 : a.k2;
-                const int ya = jb.f1 ? static_cast<int>((static_cast<int64_t>(ma) * kBM) % a.ring_rows) : ma * kBM;
+                const int64_t arows = jb.f1 ? a.ring_rows : a.h_rows;
+                const int ya = jb.ghost ? static_cast<int>(arows)
+                               : jb.f1 ? static_cast<int>((static_cast<int64_t>(ma) * kBM) % a.ring_rows) : ma * kBM;
+                // scale tiles of A: (K / 128) x (rows / 128) of them; the ghost's lie past the last
+                const int sfa_end = static_cast<int>(((jb.f1 ? a.d : a.F) >> 7) * (arows >> 7));
                 // B rows of this CTA's half, and the first B row of the tile (scales)
                 const int yb_tile = jb.f1 ? jb.e * a.F + jb.n * 128 : jb.e * a.d + jb.n * 256;
                 const int yb = jb.f1 ? yb_tile : yb_tile + static_cast<int>(rank) * 128;
                 const CUtensorMap *amap = jb.f1 ? &pm.ring : &pm.h;
                 const CUtensorMap *bmap = jb.f1 ? (rank ? &pm.u : &pm.g) : &pm.dn;
                 const CUtensorMap *samap = jb.f1 ? &pm.s_ring : &pm.s_h;
-                const int64_t arows = jb.f1 ? a.ring_rows : a.h_rows;
                 for (int ks = 0; ks < kst; ++ks) {
                     if (!wait_bar(&empty[stage], phase ^ 1u, a.status, a.wait_ns, abort_flag)) goto producer_done;
                     uint8_t *dA = sT + stage * kFPStage;
@@ -909,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d_pair(dA + kAStage, bmap, fb, x, yb);
                     if constexpr (MX) {
                         uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
-                        tma_load_2d_pair(dS, samap, fb, 0, sf_tile(x, ya, arows));
+                        tma_load_2d_pair(dS, samap, fb, 0, jb.ghost ? sfa_end : sf_tile(x, ya, arows));
                         if (jb.f1) {
                             tma_load_2d_pair(dS + kSfaBytes, &pm.s_g, fb, 0, sf_tile(x, yb_tile, a.EF));
                             tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_u, fb, 0, sf_tile(x, yb_tile, a.EF));
