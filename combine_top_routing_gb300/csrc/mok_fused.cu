@@ -559,6 +559,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, acc_phase = 0, qs = 0, qphase = 0;
+            const uint64_t adesc0 = sdesc_k_sw128(smem_u32(sA));
+            const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
+            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
                 const int tile = tq[qs];
@@ -572,7 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int m = f1 ? decode_phase_tile(tile, s_pad, a.E, a.NT1, a.band1).m : 0;
                 const int BN = f1 ? 256 : a.BN2;
                 const int kst = f1 ? a.k1 : a.k2;
-                const uint32_t idesc = idesc_bf16(kBM, BN);
+                // MXFP8: the scale-factor byte selectors (bits 4-5 and 29-30) are or-ed in per MMA
+                const uint32_t idesc = MX ? idesc_mxf8(kBM, BN, 0, 0) : idesc_bf16(kBM, BN);
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kst; ++ks) {
@@ -583,23 +587,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __threadfence();
                         red_release_gpu_add(&consumed[m], 1);
                     }
-                    const uint32_t aaddr = smem_u32(sA + stage * kAStage);
-                    const uint32_t baddr = smem_u32(sB + stage * kBStage);
+                    // descriptors: the stage's base plus 32 bytes of K per MMA (address >> 4
+                    // in the low bits; every shared address here is below 256 KB, so no carry)
+                    const uint64_t ad0 = adesc0 + static_cast<uint64_t>((stage * kAStage) >> 4);
+                    const uint64_t bd0 = bdesc0 + static_cast<uint64_t>((stage * kBStage) >> 4);
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
                     if (MX) {
-                        const uint32_t sbase = smem_u32(sSF + stage * (kSfaBytes + kSfbBytes));
-                        tmem_cp_32x128b_warpx4(sfa_col, sdesc_sf(sbase));
-                        tmem_cp_32x128b_warpx4(sfb_col, sdesc_sf(sbase + kSfaBytes));
-                        if (BN == 256) tmem_cp_32x128b_warpx4(sfb_col + 4, sdesc_sf(sbase + kSfaBytes + 512));
+                        const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
+                        tmem_cp_32x128b_warpx4(sfa_col, sd);
+                        tmem_cp_32x128b_warpx4(sfb_col, sd + (kSfaBytes >> 4));
+                        if (BN == 256) tmem_cp_32x128b_warpx4(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_k_sw128(aaddr + kk * 32);
-                        const uint64_t bd = sdesc_k_sw128(baddr + kk * 32);
                         const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-                        if (MX) mma_mxf8(tmem, ad, bd, idesc_mxf8(kBM, BN, kk, kk), sfa_col, sfb_col, accum);
-                        else mma_bf16(tmem, ad, bd, idesc, accum);
+                        if (MX)
+                            mma_mxf8(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc | (kk << 4) | (kk << 29), sfa_col,
+                                     sfb_col, accum);
+                        else mma_bf16(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, accum);
                     }
                     tc_commit(&empty[stage]);
                     if (++stage == kStages) {
@@ -936,6 +942,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && rank == 0) {
             // ---------------------------------------- even CTA: MMA issue for the pair
             uint32_t stage = 0, phase = 0, acc_phase = 0, qs = 0, qphase = 0;
+            const uint64_t tdesc0 = sdesc_k_sw128(smem_u32(sT));
+            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
                 const int tile = tq[qs];
@@ -947,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (tile < 0) break;
                 const Job jb = job_of(tile);
                 const int kst = jb.f1 ? a.k1 : a.k2;
-                const uint32_t idesc = idesc_bf16(2 * kBM, 256);
+                const uint32_t idesc = MX ? idesc_mxf8(2 * kBM, 256, 0, 0) : idesc_bf16(2 * kBM, 256);
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kst; ++ks) {
@@ -959,23 +967,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         red_release_gpu_add(&consumed[jb.m0], 1);
                         if (!jb.ghost_odd) red_release_gpu_add(&consumed[jb.m0 + 1], 1);
                     }
-                    const uint32_t aaddr = smem_u32(sT + stage * kFPStage);
-                    const uint32_t baddr = aaddr + kAStage;
+                    // descriptors: the stage's base plus 32 bytes of K per MMA (see k_moe_fused)
+                    const uint64_t ad0 = tdesc0 + static_cast<uint64_t>((stage * kFPStage) >> 4);
+                    const uint64_t bd0 = ad0 + (kAStage >> 4);
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
                     if (MX) {
-                        const uint32_t sbase = smem_u32(sSF + stage * (kSfaBytes + kSfbBytes));
-                        tmem_cp_32x128b_warpx4_pair(sfa_col, sdesc_sf(sbase));
-                        tmem_cp_32x128b_warpx4_pair(sfb_col, sdesc_sf(sbase + kSfaBytes));
-                        tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sdesc_sf(sbase + kSfaBytes + 512));
+                        const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
+                        tmem_cp_32x128b_warpx4_pair(sfa_col, sd);
+                        tmem_cp_32x128b_warpx4_pair(sfb_col, sd + (kSfaBytes >> 4));
+                        tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_k_sw128(aaddr + kk * 32);
-                        const uint64_t bd = sdesc_k_sw128(baddr + kk * 32);
                         const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-                        if (MX) mma_mxf8_pair(tmem, ad, bd, idesc_mxf8(2 * kBM, 256, kk, kk), sfa_col, sfb_col, accum);
-                        else mma_bf16_pair(tmem, ad, bd, idesc, accum);
+                        if (MX)
+                            mma_mxf8_pair(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc | (kk << 4) | (kk << 29), sfa_col,
+                                          sfb_col, accum);
+                        else mma_bf16_pair(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, accum);
                     }
                     tc_commit_pair(&empty[stage], 0x3);
                     if (++stage == kFPStages) {

@@ -92,8 +92,11 @@ __device__ __forceinline__ void load_bf16x32(const uint16_t *src, float *v)
     }
 }
 
-// SwiGLU of one accumulator element pair: h = silu(a) b, silu(a) = a / (1 + e^-a).
-__device__ __forceinline__ float swiglu_f32(float a, float b) { return a / (1.0f + __expf(-a)) * b; }
+// SwiGLU of one accumulator element pair: h = silu(a) b, silu(a) = a / (1 + e^-a),
+// the quotient by the fast reciprocal (a few ulp in fp32, far below the BF16 or
+// MXFP8 rounding of h that follows; for a < -88, 1 + e^-a is infinite and
+// silu(a) is -0).
+__device__ __forceinline__ float swiglu_f32(float a, float b) { return __fdividef(a, 1.0f + __expf(-a)) * b; }
 
 // 32 fp32 values -> one MX block: 32 E4M3 codes packed four per word into q;
 // returns the E8M0 scale byte.  Every MXFP8 quantisation of h (the FFN1
