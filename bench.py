@@ -512,7 +512,7 @@ def main():
                            "frac_of_nominal_8tbs": gbs / NOMINAL["hbm_gbs"]}
     plan = mok.fused_plan(layer.cfg)
     fused_ms = timed(lambda: mok.moe_fused(layer.cfg, layer.x_src, layer.wstruct, R.ids, R.gates,
-                                           R.counts, R.offsets, R.pad_offsets, R.row_tok, R.row_j,
+                                           R.counts, R.offsets, R.pad_offsets, R.slot_pos, R.row_tok, R.row_j,
                                            R.ystage, layer.out, layer.ws))
     ffn_ms = timed(lambda: _ffn(layer, R))
     fused_tflops = flops / (fused_ms / 1e3) / 1e12

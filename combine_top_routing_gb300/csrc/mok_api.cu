@@ -33,7 +33,7 @@ int check_config(const mok_config *cfg, Dims *dm)
     if (cfg->minibatch_rows != 0 && cfg->minibatch_rows != 64 && cfg->minibatch_rows != 128 &&
         cfg->minibatch_rows != 256)
         return MOK_ERR_INVALID_ARG;
-    if (cfg->gather_sm_fraction < 0.0f || cfg->gather_sm_fraction >= 1.0f) return MOK_ERR_INVALID_ARG;
+    if (!(cfg->gather_sm_fraction >= 0.0f && cfg->gather_sm_fraction <= 1.0f)) return MOK_ERR_INVALID_ARG;
     for (const int v : {cfg->fused_cta_pairs, cfg->gemm_cta_pairs})
         if (v != MOK_PAIRS_AUTO && v != MOK_PAIRS_ON && v != MOK_PAIRS_OFF) return MOK_ERR_INVALID_ARG;
     if (E > MOK_MAX_EXPERTS || k > MOK_MAX_TOPK || k > E) return MOK_ERR_UNSUPPORTED;
@@ -433,6 +433,8 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
         // the token ring must hold at least one minibatch of every size (256 rows)
         const int64_t ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
         if (ring_rows < 256) return MOK_ERR_INVALID_ARG;
+        // every CTA gathering first needs a ring that holds every row
+        if (cfg->gather_sm_fraction >= 1.0f && ring_rows < dm.rows_pad) return MOK_ERR_INVALID_ARG;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     FwdWs fw;
@@ -454,6 +456,7 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     io.counts = o.counts;
     io.offsets = o.offsets;
     io.pad_offsets = o.pad_offsets;
+    io.slot_pos = o.slot_pos;
     io.row_tok = o.row_tok;
     io.row_j = o.row_j;
     io.gates = o.gates;
@@ -490,20 +493,23 @@ int mok_fused_plan(const mok_config *cfg, int *ctas, int *cta_pairs, int *gather
 
 int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_weights *w,
                   const int32_t *ids, const float *gates, const int32_t *counts,
-                  const int32_t *offsets, const int32_t *pad_offsets, const int32_t *row_tok,
-                  const uint8_t *row_j, void *ystage, void *out, void *ws, void *stream)
+                  const int32_t *offsets, const int32_t *pad_offsets, const int32_t *slot_pos,
+                  const int32_t *row_tok, const uint8_t *row_j, void *ystage, void *out, void *ws,
+                  void *stream)
 {
     Dims dm;
     int rc = check_config(cfg, &dm);
     if (rc != MOK_OK) return rc;
-    if (!w || !ids || !gates || !counts || !offsets || !pad_offsets || !row_tok || !row_j ||
-        !ystage || !out || !ws)
+    if (!w || !ids || !gates || !counts || !offsets || !pad_offsets || !slot_pos || !row_tok ||
+        !row_j || !ystage || !out || !ws)
         return MOK_ERR_INVALID_ARG;
     const bool mx = dm.dtype == MOK_MXFP8;
     if (mx && (!w->q_gate || !w->q_up || !w->q_down || !w->s_gate || !w->s_up || !w->s_down))
         return MOK_ERR_INVALID_ARG;
     if (!mx && (!w->w_gate || !w->w_up || !w->w_down)) return MOK_ERR_INVALID_ARG;
     if (fused_ring_rows(dm, cfg->ring_bytes) < 256) return MOK_ERR_INVALID_ARG;
+    if (cfg->gather_sm_fraction >= 1.0f && fused_ring_rows(dm, cfg->ring_bytes) < dm.rows_pad)
+        return MOK_ERR_INVALID_ARG;
     Sources src;
     if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
     FwdWs fw;
@@ -516,6 +522,7 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
     io.counts = counts;
     io.offsets = offsets;
     io.pad_offsets = pad_offsets;
+    io.slot_pos = slot_pos;
     io.row_tok = row_tok;
     io.row_j = row_j;
     io.gates = gates;

@@ -43,6 +43,7 @@
 
 #include <mutex>
 
+#include "mok_gather.cuh"
 #include "mok_internal.h"
 #include "mok_ptx.cuh"
 #include "mok_tc.cuh"
@@ -55,7 +56,7 @@ constexpr int kTQ = 2;  // depth of the tile-id queue from the scheduler thread 
 
 struct FusedArgs {
     int E, T, k, d, F;
-    const int32_t *ids, *counts, *offsets, *pad_offsets, *row_tok;
+    const int32_t *ids, *counts, *offsets, *pad_offsets, *slot_pos, *row_tok;
     const uint8_t *row_j;
     const float *gates;
     Sources src;
@@ -71,6 +72,7 @@ struct FusedArgs {
     uint16_t *saved_a, *saved_b, *saved_h;
     int mb;                   // minibatch rows per hand-off (64, 128, 256)
     int n_gather;             // CTAs that start in the gather role
+    int prologue;             // 1: every CTA gathers tokens first (gather_all_tokens)
     int NT1, NT2, BN2, k1, k2;
     int band1;                // row tiles per band of the FFN1 order (ring-bounded)
     int *counters;            // zeroed: [0] next tile, [1] next minibatch, [2] FFN2 tiles done,
@@ -370,43 +372,76 @@ __device__ __forceinline__ void gather_rows(const FusedArgs &a, const int *s_pad
     }
 }
 
+// Gather prologue (a gather share of 1, uncapped ring): every warp of every
+// CTA pulls whole tokens -- each token's row read once, quantised once
+// (MXFP8), written into its k slot rows of the ring -- then the grid waits
+// until every CTA has arrived (bounded; all CTAs are resident), so every FFN1
+// tile finds its rows in place.  Every thread of the CTA calls it.
+template <bool MX>
+__device__ __forceinline__ void gather_all_tokens(const FusedArgs &a, int *arrived, volatile int *abort_flag,
+                                                  int warp, int lane)
+{
+    const int nw = kThreads / 32;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * nw + warp; t < a.T;
+         t += static_cast<int64_t>(gridDim.x) * nw)
+        dispatch_token<MX>(a.src, t, a.d, a.k, a.ids, a.slot_pos, a.offsets, a.pad_offsets, a.ring,
+                           a.ring_scales, a.ring_rows, lane);
+    // the rows are read by TMA (async proxy) after the barrier
+    fence_proxy_async_global();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_release_gpu_add(arrived, 1);
+        spin_ge(arrived, static_cast<int>(gridDim.x), a, abort_flag);
+    }
+    __syncthreads();
+}
+
 // Weighted combine of the fused forward: once every FFN2 tile has pushed its
-// rows (ffn2_done), each CTA combines a share of the tokens in the fixed j
-// order.  Every thread of the CTA calls it.
+// rows (ffn2_done), all threads of all CTAs walk the (token, 16-column) pieces
+// of the output, each with its 2k slot loads in flight before the (ordered)
+// accumulation -- the access pattern of the separate combine kernel.  Every
+// thread of the CTA calls it.
 __device__ __forceinline__ void combine_tokens(const FusedArgs &a, int *ffn2_done, int total_mt,
                                                volatile int *abort_flag)
 {
     if (threadIdx.x == 0 && !*abort_flag) spin_ge(ffn2_done, 4 * total_mt * a.NT2, a, abort_flag);
     __syncthreads();
     if (*abort_flag) return;
-    const int vec = a.d / 8;
-    for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-        for (int c = threadIdx.x; c < vec; c += blockDim.x) {
-            // all k slot loads in flight before the (ordered) accumulation
-            uint4 yv[MOK_MAX_TOPK];
-            float g[MOK_MAX_TOPK];
+    const int64_t vec_per_tok = a.d / 16;
+    const int64_t n = static_cast<int64_t>(a.T) * vec_per_tok;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / vec_per_tok;
+        const int64_t c = (i % vec_per_tok) * 2;
+        uint4 y[MOK_MAX_TOPK][2];
+        float g[MOK_MAX_TOPK];
 #pragma unroll
-            for (int j = 0; j < MOK_MAX_TOPK; ++j) {
-                if (j < a.k) {
-                    g[j] = a.gates[t * a.k + j];
-                    yv[j] = *(reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c);
-                }
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j < a.k) {
+                g[j] = a.gates[t * a.k + j];
+                const uint4 *row = reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c;
+                y[j][0] = row[0];
+                y[j][1] = row[1];
             }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
             float acc[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
 #pragma unroll
             for (int j = 0; j < MOK_MAX_TOPK; ++j) {
                 if (j < a.k) {
-                    const uint32_t w[4] = {yv[j].x, yv[j].y, yv[j].z, yv[j].w};
+                    const uint32_t w[4] = {y[j][hh].x, y[j][hh].y, y[j][hh].z, y[j][hh].w};
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc[2 * i] = fmaf(g[j], bf16_bits_to_float(w[i] & 0xFFFFu), acc[2 * i]);
-                        acc[2 * i + 1] = fmaf(g[j], bf16_bits_to_float(w[i] >> 16), acc[2 * i + 1]);
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = fmaf(g[j], bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
+                        acc[2 * q + 1] = fmaf(g[j], bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
                     }
                 }
             }
-            reinterpret_cast<uint4 *>(a.out + t * a.d)[c] =
+            reinterpret_cast<uint4 *>(a.out + t * a.d)[c + hh] =
                 make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
                            pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
         }
@@ -485,7 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kE = MX ? 128 : 64;
 
     // ---------------------------------------------------------- gather role
-    if (static_cast<int>(blockIdx.x) < a.n_gather)
+    if (a.prologue)
+        gather_all_tokens<MX>(a, next_unit, abort_flag, warp, lane);
+    else if (static_cast<int>(blockIdx.x) < a.n_gather)
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
                         kThreads / 32, smem, kStages * (kAStage + kBStage));
 
@@ -513,7 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const int e = expert_of_row(s_pad, a.E, static_cast<int64_t>(m) * kBM);
-                if (f1 ? !spin_ge(&ready[m], 2, a, abort_flag) : !spin_ge(&h_done[m], 4 * a.NT1, a, abort_flag))
+                if (f1 ? !(a.prologue || spin_ge(&ready[m], 2, a, abort_flag))
+                       : !spin_ge(&h_done[m], 4 * a.NT1, a, abort_flag))
                     break;
                 fence_proxy_async_global();
                 const int BN = f1 ? 256 : a.BN2;
@@ -832,7 +870,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bandp = a.band1 >= (1 << 29) ? (1 << 30) : (a.band1 / 2 > 0 ? a.band1 / 2 : 1);
 
     // ---------------------------------------------------------- gather role
-    if (static_cast<int>(blockIdx.x) < a.n_gather) {
+    if (a.prologue) {
+        gather_all_tokens<MX>(a, next_unit, abort_flag, warp, lane);
+    } else if (static_cast<int>(blockIdx.x) < a.n_gather) {
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
                         kThreads / 32, smem, kFPStages * kFPStage);
         cluster_sync_all();  // the pair joins the GEMM role together
@@ -896,7 +936,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // operand from rows past the end of the tensor (TMA fills zeros and
                 // reads no memory); its results are discarded
                 const int ma = jb.ghost ? jb.m0 : m;
-                if (jb.f1 ? !spin_ge(&ready[ma], 2, a, abort_flag) : !spin_ge(&h_done[ma], 4 * a.NT1, a, abort_flag))
+                if (jb.f1 ? !(a.prologue || spin_ge(&ready[ma], 2, a, abort_flag))
+                          : !spin_ge(&h_done[ma], 4 * a.NT1, a, abort_flag))
                     break;
                 fence_proxy_async_global();
                 const int kst = jb.f1 ? a.k1 : a.k2;
@@ -1250,8 +1291,29 @@ int fused_ctas(const Dims &dm, const mok_config *cfg, int sms)
 }
 
 // ctas: the CTAs of the launch (for the pair kernel, its grid)
+// A gather share of 1 (every CTA pulls whole tokens first, then every CTA runs
+// the GEMM role) when the config asks for it, or automatically when the ring
+// is uncapped and the split rule would give the gather role at least 1/8 of
+// the CTAs: the split keeps that share away from the GEMM role for as long as
+// it takes a fraction of the SMs to pull the rows (one read per slot), the
+// prologue takes every SM for the time the whole GPU needs to pull them (one
+// read per token).  Measured on GB300 (DeepSeek-V3 MXFP8 shape, 38 of 152 CTAs
+// by the split rule): 6.43 -> 6.09 ms; Mixtral shape (10 of 152): 3.66 vs
+// 3.68 ms, so the split stays there.
+bool fused_gathers_first(const Dims &dm, const mok_config *cfg, int ctas)
+{
+    if (fused_ring_rows(dm, cfg->ring_bytes) < dm.rows_pad) return false;
+    if (cfg->gather_sm_fraction >= 1.0f) return true;
+    return cfg->gather_sm_fraction == 0.0f && 8 * auto_gather_ctas(dm, ctas) >= ctas;
+}
+
 void fused_knobs(const Dims &dm, const mok_config *cfg, int ctas, int *gather, int *mb)
 {
+    if (fused_gathers_first(dm, cfg, ctas)) {
+        *gather = ctas;
+        *mb = 0;
+        return;
+    }
     *gather = cfg->gather_sm_fraction > 0.0f ? gather_ctas(ctas, cfg->gather_sm_fraction)
                                              : auto_gather_ctas(dm, ctas);
     if (fused_uses_pairs(dm, cfg)) {
@@ -1299,6 +1361,7 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     a.counts = io.counts;
     a.offsets = io.offsets;
     a.pad_offsets = io.pad_offsets;
+    a.slot_pos = io.slot_pos;
     a.row_tok = io.row_tok;
     a.row_j = io.row_j;
     a.gates = io.gates;
@@ -1326,6 +1389,8 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
         if (ge != cudaSuccess) return ge;
     }
     fused_knobs(dm, cfg, grid, &a.n_gather, &a.mb);
+    a.prologue = a.n_gather >= grid ? 1 : 0;
+    if (a.prologue && ring_rows < dm.rows_pad) return cudaErrorInvalidValue;
     a.NT1 = dm.F / 128;
     a.BN2 = dm.d % 256 == 0 ? 256 : 128;
     a.NT2 = dm.d / a.BN2;

@@ -299,7 +299,11 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
             uint32_t stage = 0, phase = 0, acc_phase = 0;
-            const uint32_t idesc = idesc_bf16(kBM, BN);
+            // MXFP8: the scale-factor byte selectors (bits 4-5 and 29-30) are or-ed in per MMA
+            const uint32_t idesc = MX ? idesc_mxf8(kBM, BN, 0, 0) : idesc_bf16(kBM, BN);
+            const uint64_t adesc0 = sdesc_k_sw128(smem_u32(sA));
+            const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
+            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
                 const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
                 const int kst = tile_k_stages<MODE, MX>(a, tl.group);
@@ -308,23 +312,25 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
                 for (int ks = 0; ks < kst; ++ks) {
                     if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
                     tc_fence_after();
-                    const uint32_t aaddr = smem_u32(sA + stage * kAStage);
-                    const uint32_t baddr = smem_u32(sB + stage * kBStage);
+                    // descriptors: the stage's base plus 32 bytes of K per MMA (address >> 4
+                    // in the low bits; every shared address here is below 256 KB, so no carry)
+                    const uint64_t ad0 = adesc0 + static_cast<uint64_t>((stage * kAStage) >> 4);
+                    const uint64_t bd0 = bdesc0 + static_cast<uint64_t>((stage * kBStage) >> 4);
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
                     if (MX) {
-                        const uint32_t sbase = smem_u32(sSF + stage * (kSfaBytes + kSfbBytes));
-                        tmem_cp_32x128b_warpx4(sfa_col, sdesc_sf(sbase));
-                        tmem_cp_32x128b_warpx4(sfb_col, sdesc_sf(sbase + kSfaBytes));
-                        if (BN == 256) tmem_cp_32x128b_warpx4(sfb_col + 4, sdesc_sf(sbase + kSfaBytes + 512));
+                        const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
+                        tmem_cp_32x128b_warpx4(sfa_col, sd);
+                        tmem_cp_32x128b_warpx4(sfb_col, sd + (kSfaBytes >> 4));
+                        if (BN == 256) tmem_cp_32x128b_warpx4(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_k_sw128(aaddr + kk * 32);
-                        const uint64_t bd = sdesc_k_sw128(baddr + kk * 32);
                         const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-                        if (MX) mma_mxf8(tmem, ad, bd, idesc_mxf8(kBM, BN, kk, kk), sfa_col, sfb_col, accum);
-                        else mma_bf16(tmem, ad, bd, idesc, accum);
+                        if (MX)
+                            mma_mxf8(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc | (kk << 4) | (kk << 29), sfa_col,
+                                     sfb_col, accum);
+                        else mma_bf16(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, accum);
                     }
                     tc_commit(&empty[stage]);
                     if (++stage == kStages) {
@@ -730,7 +736,9 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
         if (lane == 0 && rank == 0) {
             // ---------------------------------------- even CTA: MMA issue for the pair
             uint32_t stage = 0, phase = 0, acc_phase = 0;
-            const uint32_t idesc = idesc_bf16(2 * kBM, 256);
+            const uint32_t idesc = MX ? idesc_mxf8(2 * kBM, 256, 0, 0) : idesc_bf16(2 * kBM, 256);
+            const uint64_t tdesc0 = sdesc_k_sw128(smem_u32(sT));
+            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (int tile = pair; tile < total; tile += npairs) {
                 const int kst = k_stages_of(locate(tile).group);
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
@@ -738,23 +746,24 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
                 for (int ks = 0; ks < kst; ++ks) {
                     if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
                     tc_fence_after();
-                    const uint32_t aaddr = smem_u32(sT + stage * kPStage);
-                    const uint32_t baddr = aaddr + kAStage;
+                    // descriptors: the stage's base plus 32 bytes of K per MMA (see k_gemm)
+                    const uint64_t ad0 = tdesc0 + static_cast<uint64_t>((stage * kPStage) >> 4);
+                    const uint64_t bd0 = ad0 + (kAStage >> 4);
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
                     if (MX) {
-                        const uint32_t sbase = smem_u32(sSF + stage * (kSfaBytes + kSfbBytes));
-                        tmem_cp_32x128b_warpx4_pair(sfa_col, sdesc_sf(sbase));
-                        tmem_cp_32x128b_warpx4_pair(sfb_col, sdesc_sf(sbase + kSfaBytes));
-                        tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sdesc_sf(sbase + kSfaBytes + 512));
+                        const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
+                        tmem_cp_32x128b_warpx4_pair(sfa_col, sd);
+                        tmem_cp_32x128b_warpx4_pair(sfb_col, sd + (kSfaBytes >> 4));
+                        tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sdesc_k_sw128(aaddr + kk * 32);
-                        const uint64_t bd = sdesc_k_sw128(baddr + kk * 32);
                         const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
-                        if (MX) mma_mxf8_pair(tmem, ad, bd, idesc_mxf8(2 * kBM, 256, kk, kk), sfa_col, sfb_col, accum);
-                        else mma_bf16_pair(tmem, ad, bd, idesc, accum);
+                        if (MX)
+                            mma_mxf8_pair(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc | (kk << 4) | (kk << 29), sfa_col,
+                                          sfb_col, accum);
+                        else mma_bf16_pair(tmem, ad0 + 2 * kk, bd0 + 2 * kk, idesc, accum);
                     }
                     tc_commit_pair(&empty[stage], 0x3);
                     if (++stage == kPStages) {

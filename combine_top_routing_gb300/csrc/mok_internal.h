@@ -153,7 +153,7 @@ cudaError_t launch_transpose_bf16(const uint16_t *src, int64_t batch, int64_t ro
 
 // Buffers of the fused persistent forward.
 struct FusedIo {
-    const int32_t *ids, *counts, *offsets, *pad_offsets, *row_tok;
+    const int32_t *ids, *counts, *offsets, *pad_offsets, *slot_pos, *row_tok;
     const uint8_t *row_j;
     const float *gates;
     void *ring;               // token ring (a prefix of the xe buffer)
@@ -167,12 +167,16 @@ int64_t fused_ring_rows(const Dims &dm, size_t ring_bytes);
 // Defaults of the fused forward's knobs when the config leaves them 0.
 int auto_gather_ctas(const Dims &dm, int sms);
 int auto_minibatch_rows(const Dims &dm, int gather_ctas, int gemm_ctas);
+// Whether every CTA gathers the tokens first (a gather share of 1; see fused_knobs).
+bool fused_gathers_first(const Dims &dm, const mok_config *cfg, int ctas);
 // Whether the fused forward runs its GEMM role on CTA pairs (d a multiple of
 // 256 and an uncapped ring or one of at least 4 row tiles, as
 // cfg->fused_cta_pairs allows), and its CTAs.
 bool fused_uses_pairs(const Dims &dm, const mok_config *cfg);
 int fused_ctas(const Dims &dm, const mok_config *cfg, int sms);
-// The knobs one fused launch of `ctas` CTAs uses: gather CTAs and minibatch rows.
+// The knobs one fused launch of `ctas` CTAs uses: gather CTAs and minibatch rows
+// (gather CTAs == ctas: every CTA gathers the tokens first, then every CTA
+// runs the GEMM role; minibatch rows then 0).
 void fused_knobs(const Dims &dm, const mok_config *cfg, int ctas, int *gather_ctas, int *minibatch_rows);
 int fused_counter_ints(const Dims &dm);
 cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &src, const FusedIo &io,

@@ -12,6 +12,7 @@
 // warp owns whole rows so reads and writes are fully coalesced.
 #include <cuda_bf16.h>
 
+#include "mok_gather.cuh"
 #include "mok_internal.h"
 #include "mok_ptx.cuh"
 
@@ -105,66 +106,8 @@ __global__ void __launch_bounds__(256) k_dispatch_by_token(const Sources src, in
     const int lane = threadIdx.x & 31;
     const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); t < T;
-         t += warps) {
-        int64_t q[MOK_MAX_TOPK];
-#pragma unroll
-        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
-            if (j < k) {
-                const int e = ids[t * k + j];
-                q[j] = pad_offsets[e] + (slot_pos[t * k + j] - offsets[e]);
-            }
-        }
-        const uint4 *in = reinterpret_cast<const uint4 *>(source_row(src, static_cast<int>(t), d));
-        if (!MX) {
-            for (int c0 = 0; c0 < d / 8; c0 += 128) {
-                uint4 v[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c = c0 + 32 * u + lane;
-                    v[u] = c < d / 8 ? __ldg(in + c) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int j = 0; j < MOK_MAX_TOPK; ++j) {
-                    if (j < k) {
-                        uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xe) + q[j] * d);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int c = c0 + 32 * u + lane;
-                            if (c < d / 8) out[c] = v[u];
-                        }
-                    }
-                }
-            }
-        } else {
-            for (int c0 = 0; c0 < d; c0 += 1024) {
-                uint4 raw[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int cu = c0 + 256 * u;
-                    const int nvalid = cu >= d ? 0 : (d - cu >= 256 ? 32 : 16);
-                    raw[u] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int cu = c0 + 256 * u;
-                    if (cu >= d) continue;
-                    const int nvalid = d - cu >= 256 ? 32 : 16;
-                    uint2 codes;
-                    uint32_t word;
-                    mx_quant8(raw[u], lane, codes, word);
-#pragma unroll
-                    for (int j = 0; j < MOK_MAX_TOPK; ++j) {
-                        if (j < k) {
-                            uint8_t *row = static_cast<uint8_t *>(xe) + q[j] * d;
-                            if (lane < nvalid) *reinterpret_cast<uint2 *>(row + cu + 8 * lane) = codes;
-                            if ((lane & 15) == 0 && lane < nvalid)
-                                xe_scales[mx_word_index((cu + 8 * lane) >> 7, q[j], rows_pad)] = word;
-                        }
-                    }
-                }
-            }
-        }
-    }
+         t += warps)
+        dispatch_token<MX>(src, t, d, k, ids, slot_pos, offsets, pad_offsets, xe, xe_scales, rows_pad, lane);
 }
 
 cudaError_t launch_dispatch_by_token(const Dims &dm, const Sources &src, const int32_t *ids,

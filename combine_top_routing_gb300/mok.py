@@ -91,7 +91,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_dispatch_by_token.argtypes = [cfgp, vp] + [vp] * 7
         L.mok_expert_ffn.argtypes = [cfgp, vp, vp, ctypes.POINTER(MokWeights)] + [vp] * 10
         L.mok_combine.argtypes = [cfgp, vp, vp, vp, vp]
-        L.mok_moe_fused.argtypes = [cfgp, vp, ctypes.POINTER(MokWeights)] + [vp] * 11
+        L.mok_moe_fused.argtypes = [cfgp, vp, ctypes.POINTER(MokWeights)] + [vp] * 12
         L.mok_moe_forward.argtypes = [cfgp, vp, vp, vp, ctypes.POINTER(MokWeights), vp, vp, vp, vp]
         L.mok_moe_backward.argtypes = [cfgp, vp, vp, vp, vp, ctypes.POINTER(MokWeights), vp,
                                        ctypes.POINTER(MokWeightGrads), vp, vp, vp, vp, vp]
@@ -232,13 +232,13 @@ def combine(cfg, ystage, gates, out, stream=None):
     _check("mok_combine", lib().mok_combine(cfg.ref, _ptr(ystage), _ptr(gates), _ptr(out), _stream(stream)))
 
 
-def moe_fused(cfg, x_src, weights: MokWeights, ids, gates, counts, offsets, pad_offsets, row_tok,
-              row_j, ystage, out, ws, stream=None):
+def moe_fused(cfg, x_src, weights: MokWeights, ids, gates, counts, offsets, pad_offsets, slot_pos,
+              row_tok, row_j, ystage, out, ws, stream=None):
     arr = _src_array(x_src)
     _check("mok_moe_fused", lib().mok_moe_fused(
         cfg.ref, arr, ctypes.byref(weights), _ptr(ids), _ptr(gates), _ptr(counts), _ptr(offsets),
-        _ptr(pad_offsets), _ptr(row_tok), _ptr(row_j), _ptr(ystage), _ptr(out), _ptr(ws),
-        _stream(stream)))
+        _ptr(pad_offsets), _ptr(slot_pos), _ptr(row_tok), _ptr(row_j), _ptr(ystage), _ptr(out),
+        _ptr(ws), _stream(stream)))
 
 
 def moe_forward(cfg, x_src, W_r, bias, weights: MokWeights, out, saved_ctx, ws, stream=None):

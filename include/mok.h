@@ -86,7 +86,9 @@ typedef struct {
     int minibatch_rows;            /* rows per hand-off chunk of the fused forward:
                                       64 | 128 | 256 (0 = from the shape) */
     float gather_sm_fraction;      /* SMs given to the gather/combine role in the
-                                      fused forward (0 = automatic) */
+                                      fused forward (0 = automatic; 1 = every CTA
+                                      gathers the tokens first, then every CTA runs
+                                      the GEMM role -- needs an uncapped ring) */
     size_t ring_bytes;             /* token ring of the fused forward (0 = no cap) */
     unsigned long long wait_limit_ns; /* device spin give-up (0 = 2 s) */
     int fused_cta_pairs;           /* GEMM role of the fused forward on CTA pairs:
@@ -243,15 +245,21 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates,
  * minibatches of cfg->minibatch_rows (0: chosen from the shape);
  * the other SMs run the FFN1 and FFN2 tiles as rows arrive; finally every SM
  * combines.  The result is bit-identical to mok_dispatch + mok_expert_ffn +
- * mok_combine for every split, minibatch and ring size.  ystage: device BF16
- * [T,k,d]; out: device BF16 [T,d]; ws: fwd_ws bytes.  A ring below 256 rows
- * returns MOK_ERR_INVALID_ARG; a bounded device wait that runs out sets
- * MOK_ERR_TIMEOUT in the status word.
+ * mok_combine for every split, minibatch and ring size.  With a gather share
+ * of 1 (uncapped ring only) every CTA first pulls whole tokens -- each row
+ * read once and quantised once, written into its k slot rows, as
+ * mok_dispatch_by_token -- and the GEMM role starts on every CTA once all of
+ * them have arrived.  ids/gates/counts/offsets/pad_offsets/slot_pos/row_tok/
+ * row_j as produced by mok_route_layout; ystage: device BF16 [T,k,d]; out:
+ * device BF16 [T,d]; ws: fwd_ws bytes.  A ring below 256 rows, or a gather
+ * share of 1 with a capped ring, returns MOK_ERR_INVALID_ARG; a bounded device
+ * wait that runs out sets MOK_ERR_TIMEOUT in the status word.
  */
 int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_weights *w,
                   const int32_t *ids, const float *gates, const int32_t *counts,
-                  const int32_t *offsets, const int32_t *pad_offsets, const int32_t *row_tok,
-                  const uint8_t *row_j, void *ystage, void *out, void *ws, void *stream);
+                  const int32_t *offsets, const int32_t *pad_offsets, const int32_t *slot_pos,
+                  const int32_t *row_tok, const uint8_t *row_j, void *ystage, void *out, void *ws,
+                  void *stream);
 
 /*
  * The launch plan of the fused forward for this config on the current device,
@@ -271,7 +279,9 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
  * of 64, 128, 256 rows for which one round of the gather role (one
  * minibatch per gather CTA, every 128-row tile released as soon as it has
  * landed) hands over two waves of FFN1 tiles to the GEMM CTAs, else 256.
- * Any output may be NULL.
+ * With an uncapped ring and a share of 1/8 of the CTAs or more by that rule,
+ * or a config share of 1, every CTA gathers first instead (gather CTAs =
+ * CTAs, minibatch 0; see mok_moe_fused).  Any output may be NULL.
  */
 int mok_fused_plan(const mok_config *cfg, int *ctas, int *cta_pairs, int *gather_ctas,
                    int *minibatch_rows, int64_t *ring_rows);

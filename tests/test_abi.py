@@ -57,6 +57,7 @@ def test_workspace_size_valid_and_monotone():
     (dict(dtype=7), mok.MOK_ERR_INVALID_ARG),
     (dict(minibatch_rows=100), mok.MOK_ERR_INVALID_ARG),
     (dict(gather_sm_fraction=1.5), mok.MOK_ERR_INVALID_ARG),
+    (dict(gather_sm_fraction=-0.5), mok.MOK_ERR_INVALID_ARG),
     (dict(fused_cta_pairs=3), mok.MOK_ERR_INVALID_ARG),
     (dict(gemm_cta_pairs=-1), mok.MOK_ERR_INVALID_ARG),
 ])
@@ -148,16 +149,28 @@ def test_fused_plan_honours_explicit_knobs():
 
 def test_fused_plan_shape_rules():
     # gather share: per-row gather time over per-row FFN1 time grows as F shrinks
-    wide = _plan(d_model=4096, d_ff=14336, n_experts=8, top_k=2, T=8192)
-    narrow = _plan(d_model=7168, d_ff=2048, n_experts=256, top_k=8, T=16384, dtype=1)
+    # (a capped ring keeps the split gather)
+    cap = dict(ring_bytes=64 << 20)
+    wide = _plan(d_model=4096, d_ff=14336, n_experts=8, top_k=2, T=8192, **cap)
+    narrow = _plan(d_model=7168, d_ff=2048, n_experts=256, top_k=8, T=16384, dtype=1, **cap)
     for p in (wide, narrow):
         assert p["ctas"] / 16 - 1 <= p["gather_ctas"] <= p["ctas"] / 3 + 1
     assert narrow["gather_ctas"] > wide["gather_ctas"]
+    # uncapped ring: every CTA gathers first where the split would give the
+    # gather role 1/8 of the CTAs or more (the DeepSeek-V3 shape), not otherwise
+    narrow_u = _plan(d_model=7168, d_ff=2048, n_experts=256, top_k=8, T=16384, dtype=1)
+    wide_u = _plan(d_model=4096, d_ff=14336, n_experts=8, top_k=2, T=8192)
+    assert narrow_u["gather_ctas"] == narrow_u["ctas"] and narrow_u["minibatch_rows"] == 0
+    assert 8 * narrow["gather_ctas"] >= narrow["ctas"]
+    assert wide_u["gather_ctas"] == wide["gather_ctas"] < wide_u["ctas"] / 8
+    # an explicit share of 1 with an uncapped ring
+    full = _plan(gather_sm_fraction=1.0)
+    assert full["gather_ctas"] == full["ctas"]
     # minibatch: the smallest of 64/128/256 rows for which one gather round
     # (a minibatch per gather CTA) hands over two waves of FFN1 tiles
     for F in (128, 512, 2048, 14336):
         for frac in (0.0625, 0.25):
-            p = _plan(d_ff=F, d_model=1024, gather_sm_fraction=frac)
+            p = _plan(d_ff=F, d_model=1024, gather_sm_fraction=frac, ring_bytes=64 << 20)
             g, gemm = p["gather_ctas"], p["ctas"] - p["gather_ctas"]
             want = next((mb for mb in (64, 128) if g * mb * (F // 128) >= 2 * 128 * gemm), 256)
             assert p["minibatch_rows"] == want, (F, frac, p)

@@ -126,6 +126,34 @@ def test_full_size_skewed_layer_bit_identical_across_repeats_splits_minibatches(
     assert len(set(hashes.values())) == 1, hashes
 
 
+@pytest.mark.parametrize("name", ["mx_skew_sources", "bf16"])
+def test_gather_prologue_equals_split_gather_bit_exact(name):
+    """A gather share of 1: every CTA pulls whole tokens first (one read per
+    token), then every CTA runs the GEMM role -- the same bits as the split
+    gather, on one CTA per tile and on CTA pairs."""
+    w = CASES[name]
+    layer, _ = make_layer(w)
+    ref = layer.forward().clone()
+    for pairs in (mok.MOK_PAIRS_OFF, mok.MOK_PAIRS_ON):
+        layer.cfg.c.fused_cta_pairs = pairs
+        layer.cfg.c.gather_sm_fraction = 1.0
+        plan = mok.fused_plan(layer.cfg)
+        assert plan["gather_ctas"] == plan["ctas"]
+        out = layer.forward().clone()
+        torch.cuda.synchronize()
+        assert layer.status() == 0
+        assert torch.equal(out, ref), pairs
+
+
+def test_gather_prologue_needs_an_uncapped_ring():
+    w = CASES["bf16"]
+    layer, _ = make_layer(w, gather_sm_fraction=1.0)
+    layer.cfg.c.ring_bytes = 512 * w.d * 2
+    with pytest.raises(mok.MokError) as ei:
+        layer.forward()
+    assert ei.value.code == mok.MOK_ERR_INVALID_ARG
+
+
 def test_ring_smaller_than_a_minibatch_is_refused():
     w = CASES["bf16"]
     layer, _ = make_layer(w)
@@ -162,7 +190,7 @@ def test_moe_fused_entry_equals_forward():
     out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device="cuda")
     for _ in range(2):
         mok.moe_fused(layer.cfg, layer.x_src, layer.wstruct, R.ids, R.gates, R.counts, R.offsets,
-                      R.pad_offsets, R.row_tok, R.row_j, ystage, out, layer.ws)
+                      R.pad_offsets, R.slot_pos, R.row_tok, R.row_j, ystage, out, layer.ws)
         torch.cuda.synchronize()
         assert layer.status() == 0
         assert torch.equal(out, ref)
