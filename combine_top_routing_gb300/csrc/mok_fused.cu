@@ -53,6 +53,10 @@ namespace mok {
 namespace {
 
 constexpr int kTQ = 2;  // depth of the tile-id queue from the scheduler thread to MMA / epilogue
+// 7 warps: 0 TMA producer (and tile scheduler), 1 MMA issue, 2-5 epilogue (one
+// TMEM lane quarter each), 6 MXFP8 scale copies into TMEM (idle for BF16)
+constexpr int kFThreads = 224;
+constexpr int kScaleWarp = 6;
 
 struct FusedArgs {
     int E, T, k, d, F;
@@ -381,7 +385,7 @@ template <bool MX>
 __device__ __forceinline__ void gather_all_tokens(const FusedArgs &a, int *arrived, volatile int *abort_flag,
                                                   int warp, int lane)
 {
-    const int nw = kThreads / 32;
+    const int nw = kFThreads / 32;
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * nw + warp; t < a.T;
          t += static_cast<int64_t>(gridDim.x) * nw)
         dispatch_token<MX>(a.src, t, a.d, a.k, a.ids, a.slot_pos, a.offsets, a.pad_offsets, a.ring,
@@ -449,7 +453,7 @@ __device__ __forceinline__ void combine_tokens(const FusedArgs &a, int *ffn2_don
 }
 
 template <bool MX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFThreads, 1)
     k_moe_fused(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ CUtensorMap tmG,
                 const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
                 const __grid_constant__ CUtensorMap tmD, const __grid_constant__ FusedArgs a)
@@ -463,7 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + kStages;
-    uint64_t *acc_full = bars + 2 * kStages;
+    uint64_t *sf_ready = bars + 2 * kStages;  // MXFP8: the stage's scales are in TMEM
+    uint64_t *acc_full = bars + 3 * kStages;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *tq_full = acc_empty + 1;
     uint64_t *tq_empty = tq_full + kTQ;
@@ -487,12 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
         for (int i = 0; i < kTQ; ++i) {
             mbar_init(&tq_full[i], 1);
-            mbar_init(&tq_empty[i], 5);
+            mbar_init(&tq_empty[i], MX ? 6 : 5);  // MMA, 4 epilogue warps (+ scale copier)
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -524,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         gather_all_tokens<MX>(a, next_unit, abort_flag, warp, lane);
     else if (static_cast<int>(blockIdx.x) < a.n_gather)
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
-                        kThreads / 32, smem, kStages * (kAStage + kBStage));
+                        kFThreads / 32, smem, kStages * (kAStage + kBStage));
 
     // ------------------------------------------------------------ GEMM role
     if (warp == 0) {
@@ -599,7 +605,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, acc_phase = 0, qs = 0, qphase = 0;
             const uint64_t adesc0 = sdesc_k_sw128(smem_u32(sA));
             const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
-            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
                 const int tile = tq[qs];
@@ -618,7 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kst; ++ks) {
-                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    // MXFP8: sf_ready (the scale copier waited for the loads, then
+                    // copied the stage's scales into TMEM); BF16: the loads
+                    if (!wait_bar(MX ? &sf_ready[stage] : &full[stage], phase, a.status, a.wait_ns, abort_flag))
+                        goto mma_done;
                     tc_fence_after();
                     if (f1 && ks == kst - 1) {
                         // every ring row of row tile m this tile needs is now in shared memory
@@ -631,12 +639,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd0 = bdesc0 + static_cast<uint64_t>((stage * kBStage) >> 4);
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
-                    if (MX) {
-                        const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
-                        tmem_cp_32x128b_warpx4(sfa_col, sd);
-                        tmem_cp_32x128b_warpx4(sfb_col, sd + (kSfaBytes >> 4));
-                        if (BN == 256) tmem_cp_32x128b_warpx4(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
-                    }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
@@ -655,6 +657,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         mma_done:;
+        }
+    } else if (warp == kScaleWarp) {
+        if (MX && lane == 0) {
+            // ------------------------------------------------ scale copier
+            // the same tile and stage sequence as the MMA issuer: once a stage's
+            // loads have landed, copy its A and B scales into the stage's TMEM
+            // columns and commit to sf_ready (a scale slot is refilled only after
+            // empty[stage], i.e. after the MMAs that read it have completed)
+            uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
+            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
+            for (;;) {
+                if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
+                const int tile = tq[qs];
+                mbar_arrive(&tq_empty[qs]);
+                if (++qs == kTQ) {
+                    qs = 0;
+                    qphase ^= 1u;
+                }
+                if (tile < 0) break;
+                const bool f1 = tile < T1;
+                const int BN = f1 ? 256 : a.BN2;
+                const int kst = f1 ? a.k1 : a.k2;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto copier_done;
+                    tc_fence_after();
+                    const uint32_t sfa_col = tmem + kSfCol + stage * 16;
+                    const uint32_t sfb_col = sfa_col + 4;
+                    const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
+                    tmem_cp_32x128b_warpx4(sfa_col, sd);
+                    tmem_cp_32x128b_warpx4(sfb_col, sd + (kSfaBytes >> 4));
+                    if (BN == 256) tmem_cp_32x128b_warpx4(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
+                    tc_commit(&sf_ready[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        copier_done:;
         }
     } else {
         const int quarter = warp & 3;
@@ -789,7 +830,7 @@ __device__ __forceinline__ PPTile decode_pair_tile(int t, const int *s_pp, int E
 }
 
 template <bool MX>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kFThreads, 1)
     k_moe_fused_pair(const __grid_constant__ FusedPairMaps pm, const __grid_constant__ FusedArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -800,7 +841,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sSF + (MX ? kFPStages * (kSfaBytes + kSfbBytes) : 0));
     uint64_t *full = bars;
     uint64_t *empty = bars + kFPStages;
-    uint64_t *acc_full = bars + 2 * kFPStages;
+    uint64_t *sf_ready = bars + 2 * kFPStages;  // MXFP8, even CTA: the stage's scales are in TMEM
+    uint64_t *acc_full = bars + 3 * kFPStages;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *tq_full = acc_empty + 1;
     uint64_t *tq_empty = tq_full + kTQ;
@@ -826,12 +868,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kFPStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_ready[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);  // four epilogue warps of each CTA
         for (int i = 0; i < kTQ; ++i) {
             mbar_init(&tq_full[i], 1);
-            mbar_init(&tq_empty[i], 10);  // even: MMA + 4 epilogue warps; odd: producer + 4 epilogue warps
+            // even: MMA + 4 epilogue warps (+ scale copier); odd: producer + 4 epilogue warps
+            mbar_init(&tq_empty[i], MX ? 11 : 10);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -874,7 +918,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         gather_all_tokens<MX>(a, next_unit, abort_flag, warp, lane);
     } else if (static_cast<int>(blockIdx.x) < a.n_gather) {
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
-                        kThreads / 32, smem, kFPStages * kFPStage);
+                        kFThreads / 32, smem, kFPStages * kFPStage);
         cluster_sync_all();  // the pair joins the GEMM role together
     }
 
@@ -984,7 +1028,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---------------------------------------- even CTA: MMA issue for the pair
             uint32_t stage = 0, phase = 0, acc_phase = 0, qs = 0, qphase = 0;
             const uint64_t tdesc0 = sdesc_k_sw128(smem_u32(sT));
-            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
                 const int tile = tq[qs];
@@ -1000,7 +1043,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kst; ++ks) {
-                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    // MXFP8: sf_ready (loads landed, scales copied); BF16: the loads
+                    if (!wait_bar(MX ? &sf_ready[stage] : &full[stage], phase, a.status, a.wait_ns, abort_flag))
+                        goto mma_done;
                     tc_fence_after();
                     if (jb.f1 && ks == kst - 1) {
                         // every ring row of the pair's row tiles is now in shared memory
@@ -1013,12 +1058,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bd0 = ad0 + (kAStage >> 4);
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
-                    if (MX) {
-                        const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
-                        tmem_cp_32x128b_warpx4_pair(sfa_col, sd);
-                        tmem_cp_32x128b_warpx4_pair(sfb_col, sd + (kSfaBytes >> 4));
-                        tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
-                    }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (ks > 0 || kk > 0) ? 1u : 0u;
@@ -1037,6 +1076,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc_phase ^= 1u;
             }
         mma_done:;
+        }
+    } else if (warp == kScaleWarp) {
+        if (MX && lane == 0 && rank == 0) {
+            // ---------------------------------- even CTA: scale copier for the pair
+            // once a stage's loads (both CTAs') have landed, copy the stage's
+            // scales into both CTAs' TMEM and commit to sf_ready (see k_moe_fused)
+            uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
+            const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
+            for (;;) {
+                if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
+                const int tile = tq[qs];
+                mbar_arrive(&tq_empty[qs]);
+                if (++qs == kTQ) {
+                    qs = 0;
+                    qphase ^= 1u;
+                }
+                if (tile < 0) break;
+                const int kst = tile < T1 ? a.k1 : a.k2;
+                for (int ks = 0; ks < kst; ++ks) {
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto copier_done;
+                    tc_fence_after();
+                    const uint32_t sfa_col = tmem + kSfCol + stage * 16;
+                    const uint32_t sfb_col = sfa_col + 4;
+                    const uint64_t sd = sfdesc0 + static_cast<uint64_t>((stage * (kSfaBytes + kSfbBytes)) >> 4);
+                    tmem_cp_32x128b_warpx4_pair(sfa_col, sd);
+                    tmem_cp_32x128b_warpx4_pair(sfb_col, sd + (kSfaBytes >> 4));
+                    tmem_cp_32x128b_warpx4_pair(sfb_col + 4, sd + ((kSfaBytes + 512) >> 4));
+                    tc_commit_pair(&sf_ready[stage], 0x1);
+                    if (++stage == kFPStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        copier_done:;
         }
     } else {
         // ---------------------------------------------------- epilogue (both CTAs)
@@ -1115,7 +1189,7 @@ template <bool MX>
 constexpr size_t fused_pair_smem_bytes()
 {
     return 1024 + kFPStages * kFPStage + (MX ? kFPStages * (kSfaBytes + kSfbBytes) : 0) +
-           (2 * kFPStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + 2 * (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+           (3 * kFPStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + 2 * (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
 }
 
 // Launch configuration of the pair kernel: its attributes are set once and its
@@ -1137,7 +1211,7 @@ cudaError_t fused_pair_setup(int *grid_out)
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(kFThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
@@ -1161,7 +1235,7 @@ cudaError_t launch_fused_pair_t(const FusedPairMaps &pm, const FusedArgs &args, 
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kFThreads);
     cfg.dynamicSmemBytes = fused_pair_smem_bytes<MX>();
     cfg.stream = st;
     cfg.attrs = attr;
@@ -1173,7 +1247,7 @@ template <bool MX>
 constexpr size_t fused_smem_bytes()
 {
     return 1024 + kStages * (kAStage + kBStage) + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0) +
-           (2 * kStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+           (3 * kStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
 }
 
 template <bool MX>
@@ -1189,7 +1263,7 @@ cudaError_t launch_fused_t(const CUtensorMap &ring, const CUtensorMap &g, const 
                                         static_cast<int>(smem));
         int per_sm = 0;
         if (attr_err == cudaSuccess)
-            attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe_fused<MX>, kThreads, smem);
+            attr_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_moe_fused<MX>, kFThreads, smem);
         if (attr_err == cudaSuccess && per_sm < 1) attr_err = cudaErrorInvalidConfiguration;
     });
     if (attr_err != cudaSuccess) return attr_err;
@@ -1198,7 +1272,7 @@ cudaError_t launch_fused_t(const CUtensorMap &ring, const CUtensorMap &g, const 
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms()));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kFThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
@@ -1263,18 +1337,20 @@ int auto_minibatch_rows(const Dims &dm, int gather_ctas, int gemm_ctas)
 // has loaded them; with bands of B pair rows the wait is acyclic when
 // 2B <= R - U + 1 (R ring row tiles, U <= 2 row tiles per unit), which
 // B = R / 4 >= 1 satisfies for R >= 4.  Smaller rings run one CTA per tile.
-// Default: pairs for BF16 layers, one CTA per tile for MXFP8 layers -- on
-// GB300 the fused kernel's tensor pipe runs at the same rate either way, so
-// the ghost halves of experts whose rows round up to an odd number of row
-// tiles (about half of them on the DeepSeek-V3 shape, whose expert row counts
-// scatter around 256 or 512) make MXFP8 pairs slower (8.27 vs 7.41 ms at
-// 16384 tokens, 5.16 vs 4.33 ms at 8192) while BF16 pairs gain (4.27 vs
-// 4.33 ms on the Mixtral shape).  cfg->fused_cta_pairs = MOK_PAIRS_ON / OFF
-// forces either.
+// Default: pairs for BF16 layers; for MXFP8 layers pairs when the average
+// expert holds at least 384 rows (three row tiles), one CTA per tile below.
+// An expert with an odd number of row tiles ends in a pair tile with a ghost
+// half, which still loads its half of B; the pair kernel (with its scale
+// copies on their own thread) loads a third fewer bytes per SM-stage but
+// completes a stage only when both SMs' loads have landed.  Measured on GB300,
+// fused kernel, router routing: DeepSeek-V3 shape at 16384 tokens (512 rows
+// per expert) 6.00 vs 6.08 ms, at 8192 tokens (256) 3.56 vs 3.47 ms, skewed
+// layer with a capped ring 6.55 vs 6.59 ms; Mixtral shape 3.75 vs 3.81 ms.
+// cfg->fused_cta_pairs = MOK_PAIRS_ON / OFF forces either.
 bool fused_uses_pairs(const Dims &dm, const mok_config *cfg)
 {
     if (dm.d % 256 != 0 || cfg->fused_cta_pairs == MOK_PAIRS_OFF) return false;
-    if (cfg->fused_cta_pairs == MOK_PAIRS_AUTO && dm.dtype == MOK_MXFP8) return false;
+    if (cfg->fused_cta_pairs == MOK_PAIRS_AUTO && dm.dtype == MOK_MXFP8 && dm.S < 384LL * dm.E) return false;
     const int64_t ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
     return ring_rows >= dm.rows_pad || ring_rows / 128 >= 4;
 }

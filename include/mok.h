@@ -268,7 +268,8 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
  * start in the gather role, the minibatch (rows per hand-off) and the token
  * ring's rows.  CTA pairs need d a multiple of 256 and an uncapped ring or
  * one of at least 512 rows; cfg->fused_cta_pairs = MOK_PAIRS_ON / OFF forces
- * either where the shape allows, MOK_PAIRS_AUTO takes them for BF16 layers.
+ * either where the shape allows, MOK_PAIRS_AUTO takes them for BF16 layers and
+ * for MXFP8 layers whose experts average at least 384 rows (T*k >= 384 E).
  * A knob the config
  * leaves 0 is chosen from the shape ([kucoin] §03: the right minibatch and
  * number of communication SMs change with the hidden size, top-k and expert

@@ -138,9 +138,10 @@ def test_fused_plan_honours_explicit_knobs():
     # 1 MiB of BF16 rows of 256 elements = 2048 rows; an uncapped ring holds every padded row
     assert q["ring_rows"] == 2048
     assert _plan()["ring_rows"] == mok.max_padded_rows(_cfg())
-    # MXFP8 layers and rings below 512 rows run one CTA per tile by default;
-    # the config forces either where the shape allows
+    # MXFP8 layers whose experts average under 384 rows and rings below 512 rows
+    # run one CTA per tile by default; the config forces either where the shape allows
     assert _plan(dtype=1)["cta_pairs"] == 0
+    assert _plan(dtype=1, T=8 * 384 // 2, top_k=2)["cta_pairs"] == 1
     assert _plan(ring_bytes=256 * 256 * 2, T=4096)["cta_pairs"] == 0
     assert _plan(dtype=1, fused_cta_pairs=mok.MOK_PAIRS_ON)["cta_pairs"] == 1
     assert _plan(fused_cta_pairs=mok.MOK_PAIRS_OFF)["cta_pairs"] == 0
