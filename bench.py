@@ -200,8 +200,14 @@ def _layer_bytes(w):
 # `scale` -- multiplied by `scale` (the weights, activations and staging all
 # grow in proportion), keyed by workload and CTA pairs, with a hash of the
 # kernel's sources at capture time: once the kernel changes, traffic is null.
-FUSED_TRAFFIC = {}
-FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h")
+FUSED_TRAFFIC = {
+    # k_moe_fused_pair<1>, T 2048 / E 32 (1/8 of the tokens and experts), 1.901491 GB
+    # read + 0.416582 GB written
+    ("dsv3_mxfp8", 1): {"bytes_small": 1901491000 + 416581888, "scale": 8,
+                        "case": "T 2048, 32 experts (1/8 of the tokens and experts)",
+                        "src_sha": "17096ffed9cab541"},
+}
+FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h", "mok_gather.cuh")
 
 
 def _fused_src_sha() -> str:

@@ -164,8 +164,10 @@ def test_ring_smaller_than_a_minibatch_is_refused():
 
 
 def test_device_timeout_is_reported_and_context_stays_usable():
+    # one CTA per tile and a split gather: the GEMM role waits for its first
+    # minibatch of rows, a wait that a 1 ns limit cannot survive
     w = CASES["mx_skew_sources"]
-    layer, _ = make_layer(w)
+    layer, _ = make_layer(w, fused_cta_pairs=mok.MOK_PAIRS_OFF, gather_sm_fraction=0.25)
     good = layer.forward().clone()
     torch.cuda.synchronize()
     assert layer.status() == 0
