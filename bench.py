@@ -501,6 +501,11 @@ def main():
             fn()
         return time_flushed(fn, iters, stream, flush)
 
+    def timed_n(fn, n):
+        for _ in range(2):
+            fn()
+        return time_flushed(fn, n, stream, flush)
+
     # the HBM-bound steps on their own (separate kernels, same stream)
     disp_ms = timed(lambda: mok.dispatch(layer.cfg, layer.x_src, R.ids, R.offsets, R.pad_offsets,
                                          R.row_tok, R.row_j, R.xe, R.xs))
@@ -538,6 +543,36 @@ def main():
                               "ms_per_step": sms})
         layer.cfg.c.gather_sm_fraction = 0.0
         layer.cfg.c.minibatch_rows = 0
+
+    # ---------------- macrobatch pipelining: back-to-back calls, each call's
+    # combine inside the next call's fused kernel (two workspaces alternating)
+    chain = None
+    if not args.no_secondary:
+        n_chain = 4
+        ws2 = torch.empty_like(layer.ws)
+        outs = [torch.empty_like(layer.out) for _ in range(n_chain)]
+        wss = [layer.ws if i % 2 == 0 else ws2 for i in range(n_chain)]
+
+        def run_chain():
+            mok.moe_forward_chain(layer.cfg, [layer.x_src] * n_chain, layer.W_r, layer.bias, layer.wstruct,
+                                  outs, wss)
+
+        def run_separate():
+            for i in range(n_chain):
+                mok.moe_forward(layer.cfg, layer.x_src, layer.W_r, layer.bias, layer.wstruct, outs[i], None,
+                                wss[i])
+
+        c_steps = max(3, min(args.steps, 10))
+        chain_ms = timed_n(run_chain, c_steps) / n_chain
+        sep_ms = timed_n(run_separate, c_steps) / n_chain
+        if layer.status() != 0 or mok.get_device_status(ws2) != 0:
+            raise RuntimeError("device status after the chained calls")
+        chain = {"calls": n_chain, "ms_per_call_chained": chain_ms, "ms_per_call_separate": sep_ms,
+                 "saving_ms_per_call": sep_ms - chain_ms,
+                 "value_chained": job_throughput(w.T, world, reduce_max(chain_ms, "cuda")), "unit": "tokens/s",
+                 "how": "mok_moe_forward_chain of 4 calls vs 4 mok_moe_forward calls, L2 flushed between repeats"}
+        del ws2, outs
+        torch.cuda.empty_cache()
 
     # ---------------- end to end through the C ABI with host buffers
     x_host = torch.empty_like(inp["x"], device="cpu").pin_memory()
@@ -640,6 +675,7 @@ def main():
                                "hbm_frac_of_nominal": _layer_bytes(w) / (ms / 1e3) / 1e9 / NOMINAL["hbm_gbs"]},
             "fwd_bwd": fb,
             "expert_load_skewed": skew,
+            "macrobatch_chain": chain,
             "secondary": secondary,
             "e2e": {"value": e2e_val, "unit": "tokens/s",
                     "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2,

@@ -415,28 +415,41 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates, v
                                       static_cast<uint16_t *>(out), static_cast<cudaStream_t>(stream)));
 }
 
-int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float *W_r,
-                    const float *bias, const mok_weights *w, void *out, void *saved_ctx, void *ws,
-                    void *stream)
+namespace {
+
+// The previous call of a chain, whose combine the next call's fused kernel runs.
+struct ChainPrev {
+    const uint16_t *ystage = nullptr;
+    const float *gates = nullptr;
+    uint16_t *out = nullptr;
+    int T = 0;
+};
+
+int check_forward_args(const mok_config *cfg, Dims *dm, const float *W_r, const mok_weights *w,
+                       const void *out, const void *ws)
 {
-    Dims dm;
-    int rc = check_config(cfg, &dm);
+    int rc = check_config(cfg, dm);
     if (rc != MOK_OK) return rc;
     if (!W_r || !w || !out || !ws) return MOK_ERR_INVALID_ARG;
-    const bool mx = dm.dtype == MOK_MXFP8;
+    const bool mx = dm->dtype == MOK_MXFP8;
     if (mx && (!w->q_gate || !w->q_up || !w->q_down || !w->s_gate || !w->s_up || !w->s_down))
         return MOK_ERR_INVALID_ARG;
     if (!mx && (!w->w_gate || !w->w_up || !w->w_down)) return MOK_ERR_INVALID_ARG;
-    Sources src;
-    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
-    {
-        // the token ring must hold at least one minibatch of every size (256 rows)
-        const int64_t ring_rows = fused_ring_rows(dm, cfg->ring_bytes);
-        if (ring_rows < 256) return MOK_ERR_INVALID_ARG;
-        // every CTA gathering first needs a ring that holds every row
-        if (cfg->gather_sm_fraction >= 1.0f && ring_rows < dm.rows_pad) return MOK_ERR_INVALID_ARG;
-    }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // the token ring must hold at least one minibatch of every size (256 rows)
+    const int64_t ring_rows = fused_ring_rows(*dm, cfg->ring_bytes);
+    if (ring_rows < 256) return MOK_ERR_INVALID_ARG;
+    // every CTA gathering first needs a ring that holds every row
+    if (cfg->gather_sm_fraction >= 1.0f && ring_rows < dm->rows_pad) return MOK_ERR_INVALID_ARG;
+    return MOK_OK;
+}
+
+// Router + layout, then the fused kernel; `prev` / `skip_combine` chain calls.
+int forward_impl(const mok_config *cfg, const Dims &dm, const Sources &src, const float *W_r,
+                 const float *bias, const mok_weights *w, void *out, void *saved_ctx, void *ws,
+                 cudaStream_t st, const ChainPrev &prev, bool skip_combine, const float **gates_out,
+                 uint16_t **ystage_out)
+{
+    const bool mx = dm.dtype == MOK_MXFP8;
     FwdWs fw;
     fwd_ws_layout(dm, &fw);
     mok_ctx_layout c;
@@ -447,11 +460,11 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     uint32_t *status = at<uint32_t>(ws, fw.status);
     cudaError_t e = cudaMemsetAsync(status, 0, 4, st);
     if (e != cudaSuccess) return MOK_ERR_CUDA;
-    rc = route_layout_impl(cfg, dm, src, W_r, bias, o, ws, st);
+    int rc = route_layout_impl(cfg, dm, src, W_r, bias, o, ws, st);
     if (rc != MOK_OK) return rc;
     // dispatch, expert FFN and combine: one persistent kernel (role split,
     // token ring, on-GPU hand-off counters)
-    FusedIo io;
+    FusedIo io = {};
     io.ids = o.ids;
     io.counts = o.counts;
     io.offsets = o.offsets;
@@ -470,8 +483,62 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     io.saved_b = saved_ctx ? at<uint16_t>(saved_ctx, c.b) : nullptr;
     io.saved_h = saved_ctx ? at<uint16_t>(saved_ctx, c.h) : nullptr;
     io.counters = at<int>(ws, fw.counters);
-    e = launch_fused(dm, cfg, src, io, w, status, wait_ns(cfg), st);
-    return cuda_status(e);
+    io.prev_ystage = prev.ystage;
+    io.prev_gates = prev.gates;
+    io.prev_out = prev.out;
+    io.prev_T = prev.T;
+    io.skip_combine = skip_combine;
+    if (gates_out) *gates_out = o.gates;
+    if (ystage_out) *ystage_out = ystage;
+    return cuda_status(launch_fused(dm, cfg, src, io, w, status, wait_ns(cfg), st));
+}
+
+}  // namespace
+
+int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float *W_r,
+                    const float *bias, const mok_weights *w, void *out, void *saved_ctx, void *ws,
+                    void *stream)
+{
+    Dims dm;
+    int rc = check_forward_args(cfg, &dm, W_r, w, out, ws);
+    if (rc != MOK_OK) return rc;
+    Sources src;
+    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    return forward_impl(cfg, dm, src, W_r, bias, w, out, saved_ctx, ws, static_cast<cudaStream_t>(stream),
+                        ChainPrev(), false, nullptr, nullptr);
+}
+
+int mok_moe_forward_chain(const mok_config *cfg, int n, const void *const *const *x_src,
+                          const float *W_r, const float *bias, const mok_weights *w,
+                          void *const *out, void *const *ws, void *stream)
+{
+    Dims dm;
+    if (n < 1 || !x_src || !out || !ws) return MOK_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        const int rc = check_forward_args(cfg, &dm, W_r, w, out[i], ws[i]);
+        if (rc != MOK_OK) return rc;
+        Sources src;
+        const int rs = make_sources(cfg, dm, x_src[i], &src);
+        if (rs != MOK_OK) return rs;
+        // call i's combine runs in call i + 1's kernel from call i's workspace
+        if (i > 0 && (ws[i] == ws[i - 1] || out[i] == out[i - 1])) return MOK_ERR_INVALID_ARG;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    ChainPrev prev;
+    for (int i = 0; i < n; ++i) {
+        Sources src;
+        make_sources(cfg, dm, x_src[i], &src);
+        const float *gates = nullptr;
+        uint16_t *ystage = nullptr;
+        const int rc = forward_impl(cfg, dm, src, W_r, bias, w, out[i], nullptr, ws[i], st, prev, i + 1 < n,
+                                    &gates, &ystage);
+        if (rc != MOK_OK) return rc;
+        prev.ystage = ystage;
+        prev.gates = gates;
+        prev.out = static_cast<uint16_t *>(out[i]);
+        prev.T = dm.T;
+    }
+    return MOK_OK;
 }
 
 int mok_fused_plan(const mok_config *cfg, int *ctas, int *cta_pairs, int *gather_ctas,

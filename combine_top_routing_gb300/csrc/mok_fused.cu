@@ -77,6 +77,13 @@ struct FusedArgs {
     int mb;                   // minibatch rows per hand-off (64, 128, 256)
     int n_gather;             // CTAs that start in the gather role
     int prologue;             // 1: every CTA gathers tokens first (gather_all_tokens)
+    // the previous call of a chain: its weighted combine runs here, in chunks
+    // interleaved among this call's FFN1 tiles (prev_chunks = 0: none)
+    const uint16_t *prev_ystage;
+    const float *prev_gates;
+    uint16_t *prev_out;
+    int prev_T, prev_chunks;
+    int skip_combine;         // 1: this call's combine is left to the next call of the chain
     int NT1, NT2, BN2, k1, k2;
     int band1;                // row tiles per band of the FFN1 order (ring-bounded)
     int *counters;            // zeroed: [0] next tile, [1] next minibatch, [2] FFN2 tiles done,
@@ -376,6 +383,67 @@ __device__ __forceinline__ void gather_rows(const FusedArgs &a, const int *s_pad
     }
 }
 
+// Ids in the tile queue: with a previous call to combine, its C combine chunks
+// sit among the FFN1 tiles, one every s = (T1 + C) / C ids (id c*s + s - 1 is
+// chunk c); every other id is GEMM tile `tile` in the usual order.  Returns the
+// chunk index, or -1 with *tile set.
+__device__ __forceinline__ int split_queue_id(int id, int T1, int C, int *tile)
+{
+    if (C > 0) {
+        const int s = (T1 + C) / C;
+        if (id < C * s) {
+            if (id % s == s - 1) return id / s;
+            *tile = id - (id + 1) / s;
+            return -1;
+        }
+        *tile = id - C;
+        return -1;
+    }
+    *tile = id;
+    return -1;
+}
+
+// One token of the weighted combine by one warp: out[t] = BF16 of the fmaf fold
+// over j = 0..k-1 of g_tj * y_tj from 0 -- the separate combine kernel's order
+// and access pattern (16 columns a lane, all 2k slot loads in flight).
+__device__ __forceinline__ void combine_token_warp(const uint16_t *ystage, const float *gates, uint16_t *out,
+                                                   int64_t t, int k, int d, int lane)
+{
+    for (int64_t c = 2 * lane; c < d / 8; c += 64) {
+        uint4 y[MOK_MAX_TOPK][2];
+        float g[MOK_MAX_TOPK];
+#pragma unroll
+        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+            if (j < k) {
+                g[j] = gates[t * k + j];
+                const uint4 *row = reinterpret_cast<const uint4 *>(ystage + (t * k + j) * d) + c;
+                y[j][0] = row[0];
+                y[j][1] = row[1];
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < MOK_MAX_TOPK; ++j) {
+                if (j < k) {
+                    const uint32_t w[4] = {y[j][hh].x, y[j][hh].y, y[j][hh].z, y[j][hh].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = fmaf(g[j], bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
+                        acc[2 * q + 1] = fmaf(g[j], bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
+                    }
+                }
+            }
+            reinterpret_cast<uint4 *>(out + t * d)[c + hh] =
+                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        }
+    }
+}
+
 // Gather prologue (a gather share of 1, uncapped ring): every warp of every
 // CTA pulls whole tokens -- each token's row read once, quantised once
 // (MXFP8), written into its k slot rows of the ring -- then the grid waits
@@ -523,6 +591,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int total_mt = static_cast<int>(pad_end / kBM);
     const int T1 = total_mt * a.NT1;
     const int total_tiles = T1 + total_mt * a.NT2;
+    const int total_ids = total_tiles + a.prev_chunks;  // GEMM tiles and the previous call's combine chunks
     constexpr int kE = MX ? 128 : 64;
 
     // ---------------------------------------------------------- gather role
@@ -537,16 +606,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
             for (;;) {
-                int tile = *abort_flag ? -1 : atomicAdd(next_tile, 1);
-                if (tile >= total_tiles) tile = -1;
+                int qid = *abort_flag ? -1 : atomicAdd(next_tile, 1);
+                if (qid >= total_ids) qid = -1;
                 if (!wait_bar(&tq_empty[qs], qphase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
-                tq[qs] = tile;
+                tq[qs] = qid;
                 mbar_arrive(&tq_full[qs]);
                 if (++qs == kTQ) {
                     qs = 0;
                     qphase ^= 1u;
                 }
-                if (tile < 0) break;
+                if (qid < 0) break;
+                int tile;
+                if (split_queue_id(qid, T1, a.prev_chunks, &tile) >= 0) continue;  // a combine chunk: no loads
                 const bool f1 = tile < T1;
                 const PTile pt = f1 ? decode_phase_tile(tile, s_pad, a.E, a.NT1, a.band1)
                                     : decode_phase_tile(tile - T1, s_pad, a.E, a.NT2, 1 << 30);
@@ -607,13 +678,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const uint64_t bdesc0 = sdesc_k_sw128(smem_u32(sB));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
-                const int tile = tq[qs];
+                const int qid = tq[qs];
                 mbar_arrive(&tq_empty[qs]);
                 if (++qs == kTQ) {
                     qs = 0;
                     qphase ^= 1u;
                 }
-                if (tile < 0) break;
+                if (qid < 0) break;
+                int tile;
+                if (split_queue_id(qid, T1, a.prev_chunks, &tile) >= 0) continue;
                 const bool f1 = tile < T1;
                 const int m = f1 ? decode_phase_tile(tile, s_pad, a.E, a.NT1, a.band1).m : 0;
                 const int BN = f1 ? 256 : a.BN2;
@@ -669,13 +742,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
-                const int tile = tq[qs];
+                const int qid = tq[qs];
                 mbar_arrive(&tq_empty[qs]);
                 if (++qs == kTQ) {
                     qs = 0;
                     qphase ^= 1u;
                 }
-                if (tile < 0) break;
+                if (qid < 0) break;
+                int tile;
+                if (split_queue_id(qid, T1, a.prev_chunks, &tile) >= 0) continue;
                 const bool f1 = tile < T1;
                 const int BN = f1 ? 256 : a.BN2;
                 const int kst = f1 ? a.k1 : a.k2;
@@ -704,14 +779,22 @@ __global__ void __launch_bounds__(kFThreads, 1)
         uint32_t acc_phase = 0, qs = 0, qphase = 0;
         for (;;) {
             if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
-            const int tile = tq[qs];
+            const int qid = tq[qs];
             __syncwarp();
             if (lane == 0) mbar_arrive(&tq_empty[qs]);
             if (++qs == kTQ) {
                 qs = 0;
                 qphase ^= 1u;
             }
-            if (tile < 0) break;
+            if (qid < 0) break;
+            int tile;
+            const int chunk = split_queue_id(qid, T1, a.prev_chunks, &tile);
+            if (chunk >= 0) {
+                // the previous call's combine: one token per epilogue warp
+                const int64_t t = static_cast<int64_t>(chunk) * 4 + (warp - 2);
+                if (t < a.prev_T) combine_token_warp(a.prev_ystage, a.prev_gates, a.prev_out, t, a.k, a.d, lane);
+                continue;
+            }
             const bool f1 = tile < T1;
             const PTile pt = f1 ? decode_phase_tile(tile, s_pad, a.E, a.NT1, a.band1)
                                 : decode_phase_tile(tile - T1, s_pad, a.E, a.NT2, 1 << 30);
@@ -772,7 +855,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
 
     // ----------------------------------------------------- weighted combine
-    combine_tokens(a, ffn2_done, total_mt, abort_flag);
+    if (!a.skip_combine) combine_tokens(a, ffn2_done, total_mt, abort_flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -910,6 +993,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int total_pr = s_pp[a.E];
     const int T1 = total_pr * a.NT1;
     const int total_tiles = T1 + total_pr * a.NT2;
+    const int total_ids = total_tiles + a.prev_chunks;  // pair tiles and the previous call's combine chunks
     constexpr int kE = MX ? 128 : 64;
     const int bandp = a.band1 >= (1 << 29) ? (1 << 30) : (a.band1 / 2 > 0 ? a.band1 / 2 : 1);
 
@@ -954,7 +1038,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (rank == 0) {
                     // scheduler: claim the next pair tile and hand it to both CTAs
                     tile = *abort_flag ? -1 : atomicAdd(next_tile, 1);
-                    if (tile >= total_tiles) tile = -1;
+                    if (tile >= total_ids) tile = -1;
                     if (!wait_bar(&tq_empty[qs], qphase ^ 1u, a.status, a.wait_ns, abort_flag)) tile = -1;
                     tq[qs] = tile;
                     st_shared_cluster(tq_odd + qs * 4, static_cast<uint32_t>(tile));
@@ -970,6 +1054,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     qphase ^= 1u;
                 }
                 if (tile < 0) break;
+                if (split_queue_id(tile, T1, a.prev_chunks, &tile) >= 0) continue;  // a combine chunk: no loads
                 const Job jb = job_of(tile);
                 const int m = jb.m0 + static_cast<int>(rank);
                 if (jb.e < 0 || jb.e >= a.E || m >= total_mt + 1 || jb.n < 0 || jb.n >= (jb.f1 ? a.NT1 : a.NT2)) {
@@ -1030,13 +1115,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const uint64_t tdesc0 = sdesc_k_sw128(smem_u32(sT));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
-                const int tile = tq[qs];
+                int tile = tq[qs];
                 mbar_arrive(&tq_empty[qs]);
                 if (++qs == kTQ) {
                     qs = 0;
                     qphase ^= 1u;
                 }
                 if (tile < 0) break;
+                if (split_queue_id(tile, T1, a.prev_chunks, &tile) >= 0) continue;
                 const Job jb = job_of(tile);
                 const int kst = jb.f1 ? a.k1 : a.k2;
                 const uint32_t idesc = MX ? idesc_mxf8(2 * kBM, 256, 0, 0) : idesc_bf16(2 * kBM, 256);
@@ -1086,13 +1172,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
                 if (!wait_bar(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
-                const int tile = tq[qs];
+                int tile = tq[qs];
                 mbar_arrive(&tq_empty[qs]);
                 if (++qs == kTQ) {
                     qs = 0;
                     qphase ^= 1u;
                 }
                 if (tile < 0) break;
+                if (split_queue_id(tile, T1, a.prev_chunks, &tile) >= 0) continue;
                 const int kst = tile < T1 ? a.k1 : a.k2;
                 for (int ks = 0; ks < kst; ++ks) {
                     if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto copier_done;
@@ -1122,7 +1209,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         uint32_t acc_phase = 0, qs = 0, qphase = 0;
         for (;;) {
             if (!wait_bar_cluster(&tq_full[qs], qphase, a.status, a.wait_ns, abort_flag)) break;
-            const int tile = tq[qs];
+            int tile = tq[qs];
             __syncwarp();
             if (lane == 0) mbar_arrive_remote(tq_empty_even + qs * 8);
             if (++qs == kTQ) {
@@ -1130,6 +1217,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 qphase ^= 1u;
             }
             if (tile < 0) break;
+            const int chunk = split_queue_id(tile, T1, a.prev_chunks, &tile);
+            if (chunk >= 0) {
+                // the previous call's combine: one token per epilogue warp of the pair
+                const int64_t t = static_cast<int64_t>(chunk) * 8 + rank * 4 + (warp - 2);
+                if (t < a.prev_T) combine_token_warp(a.prev_ystage, a.prev_gates, a.prev_out, t, a.k, a.d, lane);
+                continue;
+            }
             const Job jb = job_of(tile);
             const int m = jb.m0 + static_cast<int>(rank);
             const int64_t q = static_cast<int64_t>(m) * kBM + r;  // padded row of this thread
@@ -1182,7 +1276,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
 
     // ----------------------------------------------------- weighted combine
-    combine_tokens(a, ffn2_done, total_mt, abort_flag);
+    if (!a.skip_combine) combine_tokens(a, ffn2_done, total_mt, abort_flag);
 }
 
 template <bool MX>
@@ -1479,6 +1573,13 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
                                        : static_cast<int>(pair ? ring_rows / 128 / 4 * 2 : ring_rows / 128 / 2);
     a.counters = io.counters;
     a.max_mt = static_cast<int>(dm.rows_pad / 128);
+    a.prev_ystage = io.prev_ystage;
+    a.prev_gates = io.prev_gates;
+    a.prev_out = io.prev_out;
+    a.prev_T = io.prev_T;
+    // one token per epilogue warp: four per chunk on one CTA, eight on a pair
+    a.prev_chunks = io.prev_T > 0 ? (io.prev_T + (pair ? 8 : 4) - 1) / (pair ? 8 : 4) : 0;
+    a.skip_combine = io.skip_combine ? 1 : 0;
     a.status = status;
     a.wait_ns = wait_ns;
     FusedPairMaps pm = {};

@@ -162,6 +162,13 @@ struct FusedIo {
     uint32_t *h_scales;
     uint16_t *ystage, *out, *saved_a, *saved_b, *saved_h;
     int *counters;            // fused_counter_ints(dm) ints
+    // chained calls: the previous call's combine (prev_T = 0: none), and whether
+    // this call leaves its own combine to the next call
+    const uint16_t *prev_ystage;
+    const float *prev_gates;
+    uint16_t *prev_out;
+    int prev_T;
+    bool skip_combine;
 };
 int64_t fused_ring_rows(const Dims &dm, size_t ring_bytes);
 // Defaults of the fused forward's knobs when the config leaves them 0.

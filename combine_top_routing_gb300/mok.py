@@ -30,7 +30,7 @@ EXPORTS = [
     "mok_moe_backward",
     "mok_quantize_mx", "mok_transpose_bf16", "mok_reset_device_status", "mok_get_device_status",
     "mok_status_string", "mok_layout_static", "mok_fused_plan", "mok_dispatch_by_token",
-    "mok_bwd_ws_layout", "mok_swiglu_quantize_mx",
+    "mok_bwd_ws_layout", "mok_swiglu_quantize_mx", "mok_moe_forward_chain",
 ]
 
 
@@ -93,6 +93,7 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
         L.mok_combine.argtypes = [cfgp, vp, vp, vp, vp]
         L.mok_moe_fused.argtypes = [cfgp, vp, ctypes.POINTER(MokWeights)] + [vp] * 12
         L.mok_moe_forward.argtypes = [cfgp, vp, vp, vp, ctypes.POINTER(MokWeights), vp, vp, vp, vp]
+        L.mok_moe_forward_chain.argtypes = [cfgp, ctypes.c_int, vp, vp, vp, ctypes.POINTER(MokWeights), vp, vp, vp]
         L.mok_moe_backward.argtypes = [cfgp, vp, vp, vp, vp, ctypes.POINTER(MokWeights), vp,
                                        ctypes.POINTER(MokWeightGrads), vp, vp, vp, vp, vp]
         L.mok_quantize_mx.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp, vp, vp]
@@ -246,6 +247,18 @@ def moe_forward(cfg, x_src, W_r, bias, weights: MokWeights, out, saved_ctx, ws, 
     _check("mok_moe_forward", lib().mok_moe_forward(
         cfg.ref, arr, _ptr(W_r), _ptr(bias), ctypes.byref(weights), _ptr(out), _ptr(saved_ctx),
         _ptr(ws), _stream(stream)))
+
+
+def moe_forward_chain(cfg, x_srcs, W_r, bias, weights: MokWeights, outs, wss, stream=None):
+    """n back-to-back inference calls; call i's combine runs inside call i+1's kernel."""
+    n = len(x_srcs)
+    assert len(outs) == n and len(wss) == n
+    keep = [_src_array(x) for x in x_srcs]
+    srcs = (ctypes.c_void_p * n)(*[ctypes.cast(a, ctypes.c_void_p).value for a in keep])
+    o = (ctypes.c_void_p * n)(*[_ptr(t) for t in outs])
+    ws = (ctypes.c_void_p * n)(*[_ptr(t) for t in wss])
+    _check("mok_moe_forward_chain", lib().mok_moe_forward_chain(
+        cfg.ref, n, srcs, _ptr(W_r), _ptr(bias), ctypes.byref(weights), o, ws, _stream(stream)))
 
 
 def moe_backward(cfg, x_src, W_r, saved_ctx, dY, weights: MokWeights, dX, grads: MokWeightGrads,

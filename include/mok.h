@@ -298,6 +298,26 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
                     void *ws, void *stream);
 
 /*
+ * n independent forward layer calls back to back, inference (macrobatch
+ * pipelining: [kucoin] §02, the token ring lets the combine of one macrobatch
+ * overlap the dispatch and expert work of the next).  Call i computes
+ * out[i] from x_src[i] exactly as mok_moe_forward (the same bits), with its
+ * own workspace ws[i] (fwd_ws bytes).  Call i's weighted combine is not run
+ * at the end of its own fused kernel: call i+1's fused kernel runs it, in
+ * chunks (one token per epilogue warp) spread among its FFN1 tiles, so the
+ * epilogue warps do that HBM-bound work while the same SMs' MMAs run; the
+ * last call combines at the end of its kernel as usual.  Everything is
+ * enqueued on `stream` in call order, so out[i] is complete once call i+1's
+ * kernel has run.  Adjacent calls need different workspaces and outputs (two
+ * workspaces alternating suffice); otherwise MOK_ERR_INVALID_ARG.
+ * x_src  host array [n] of the calls' host source arrays (as mok_moe_forward)
+ * out    host array [n] of device BF16 [T, d];  ws host array [n] of workspaces
+ */
+int mok_moe_forward_chain(const mok_config *cfg, int n, const void *const *const *x_src,
+                          const float *W_r, const float *bias, const mok_weights *w,
+                          void *const *out, void *const *ws, void *stream);
+
+/*
  * Backward of mok_moe_forward ([kucoin] §01: backward runs two more rounds
  * of communication in reverse; §02: pull reverse-combine, push
  * reverse-dispatch).  saved_ctx is the forward's saved context (the forward

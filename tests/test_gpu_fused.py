@@ -196,3 +196,40 @@ def test_moe_fused_entry_equals_forward():
         torch.cuda.synchronize()
         assert layer.status() == 0
         assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("name,pairs", [("bf16", mok.MOK_PAIRS_AUTO), ("bf16", mok.MOK_PAIRS_OFF),
+                                        ("mx_skew_sources", mok.MOK_PAIRS_AUTO),
+                                        ("mx_d384", mok.MOK_PAIRS_AUTO)])
+def test_forward_chain_equals_separate_calls_bit_exact(name, pairs):
+    """Macrobatch pipelining ([kucoin] §02): three back-to-back calls, each
+    call's combine run inside the next call's fused kernel, with two
+    workspaces alternating -- the same bits as three separate forwards."""
+    w = CASES[name]
+    layer, _ = make_layer(w, fused_cta_pairs=pairs)
+    xs = [I.make_inputs(I.scaled(w, seed=w.seed + 100 * i), device="cuda", with_weights=False)["x"]
+          for i in range(3)]
+    srcs = [I.split_sources(x, w.n_sources) if w.n_sources > 1 else [x] for x in xs]
+    wss = [layer.ws, torch.empty_like(layer.ws)]
+    want = []
+    for src in srcs:
+        mok.moe_forward(layer.cfg, src, layer.W_r, layer.bias, layer.wstruct, layer.out, None, layer.ws)
+        want.append(layer.out.clone())
+    outs = [torch.full_like(layer.out, 7) for _ in range(3)]
+    mok.moe_forward_chain(layer.cfg, srcs, layer.W_r, layer.bias, layer.wstruct, outs,
+                          [wss[i % 2] for i in range(3)])
+    torch.cuda.synchronize()
+    for ws in wss:
+        assert mok.get_device_status(ws) == 0
+    for i in range(3):
+        assert torch.equal(outs[i], want[i]), i
+
+
+def test_forward_chain_refuses_a_shared_workspace():
+    w = CASES["bf16"]
+    layer, inp = make_layer(w)
+    outs = [torch.empty_like(layer.out) for _ in range(2)]
+    with pytest.raises(mok.MokError) as ei:
+        mok.moe_forward_chain(layer.cfg, [layer.x_src, layer.x_src], layer.W_r, layer.bias, layer.wstruct,
+                              outs, [layer.ws, layer.ws])
+    assert ei.value.code == mok.MOK_ERR_INVALID_ARG
