@@ -31,6 +31,15 @@
 //     ffn2_done.
 //   * combine: every CTA waits for ffn2_done == all FFN2 tiles, then combines
 //     a share of the tokens in the fixed j order.
+//   * gather prologue (uncapped ring only, chosen by the plan where the split
+//     would give the gather role many SMs): every CTA first pulls whole tokens
+//     (one read per token, written into its k ring rows), a grid-wide arrival
+//     count closes the gather, and every CTA then runs the GEMM role.
+//   * chained calls (macrobatch pipelining): the previous call's weighted
+//     combine runs in this kernel, its tokens in chunks (one token per
+//     epilogue warp) whose queue ids sit evenly among the FFN1 tiles; the
+//     scheduler hands them out like tiles, so they fill the epilogue warps'
+//     gaps while the MMAs of the next tiles run.
 // Each tile is computed by exactly one CTA with the same instruction sequence
 // as the separate-kernel path, so the output is bit-identical to it for every
 // SM split, minibatch and ring size.  Every wait is bounded (wait_ns): on

@@ -31,11 +31,13 @@ __device__ __forceinline__ void dispatch_token(const Sources &src, int64_t t, in
         }
     }
     const uint4 *in = reinterpret_cast<const uint4 *>(source_row(src, static_cast<int>(t), d));
+    // 16 vectors of 16 bytes per lane (8 KB per warp) in flight before any is stored; 8 when
+    // quantising, whose registers also hold the block's codes
     if (!MX) {
-        for (int c0 = 0; c0 < d / 8; c0 += 128) {
-            uint4 v[4];
+        for (int c0 = 0; c0 < d / 8; c0 += 512) {
+            uint4 v[16];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 16; ++u) {
                 const int c = c0 + 32 * u + lane;
                 v[u] = c < d / 8 ? __ldg(in + c) : make_uint4(0, 0, 0, 0);
             }
@@ -44,7 +46,7 @@ __device__ __forceinline__ void dispatch_token(const Sources &src, int64_t t, in
                 if (j < k) {
                     uint4 *out = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(xe) + q[j] * d);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
+                    for (int u = 0; u < 16; ++u) {
                         const int c = c0 + 32 * u + lane;
                         if (c < d / 8) out[c] = v[u];
                     }
@@ -52,16 +54,16 @@ __device__ __forceinline__ void dispatch_token(const Sources &src, int64_t t, in
             }
         }
     } else {
-        for (int c0 = 0; c0 < d; c0 += 1024) {
-            uint4 raw[4];
+        for (int c0 = 0; c0 < d; c0 += 2048) {
+            uint4 raw[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int cu = c0 + 256 * u;
                 const int nvalid = cu >= d ? 0 : (d - cu >= 256 ? 32 : 16);
                 raw[u] = lane < nvalid ? __ldg(in + (cu >> 3) + lane) : make_uint4(0, 0, 0, 0);
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 const int cu = c0 + 256 * u;
                 if (cu >= d) continue;
                 const int nvalid = d - cu >= 256 ? 32 : 16;
