@@ -67,6 +67,25 @@ constexpr int kTQ = 2;  // depth of the tile-id queue from the scheduler thread 
 constexpr int kFThreads = 224;
 constexpr int kScaleWarp = 6;
 
+// Tensor maps of both fused kernels.  ring64 / h64 cover the same tensors as
+// ring / h with 64-row boxes: a row tile whose expert has 64 valid rows or
+// fewer in it loads only those (the rows past an expert's count are padding,
+// whose results are discarded).  The scale-tile maps serve the pair kernel.
+struct FusedMaps {
+    CUtensorMap ring, ring64, g, u, h, h64, dn;   // operands
+    CUtensorMap s_ring, s_g, s_u, s_h, s_dn;      // MX scale tiles (MXFP8, CTA pairs)
+};
+
+// Rows of A a 128-row tile loads: all, its first 64, or none (rows past the
+// expert's count are padding; the MMA reads stale shared memory there, which
+// only reaches the discarded rows of the accumulator).  rel = first row of the
+// tile relative to the expert's first row.
+__device__ __forceinline__ int a_rows_to_load(int count, int64_t rel)
+{
+    const int64_t v = count - rel;
+    return v <= 0 ? 0 : (v <= 64 ? 64 : kBM);
+}
+
 struct FusedArgs {
     int E, T, k, d, F;
     const int32_t *ids, *counts, *offsets, *pad_offsets, *slot_pos, *row_tok;
@@ -531,9 +550,7 @@ __device__ __forceinline__ void combine_tokens(const FusedArgs &a, int *ffn2_don
 
 template <bool MX>
 __global__ void __launch_bounds__(kFThreads, 1)
-    k_moe_fused(const __grid_constant__ CUtensorMap tmRing, const __grid_constant__ CUtensorMap tmG,
-                const __grid_constant__ CUtensorMap tmU, const __grid_constant__ CUtensorMap tmH,
-                const __grid_constant__ CUtensorMap tmD, const __grid_constant__ FusedArgs a)
+    k_moe_fused(const __grid_constant__ FusedMaps pm, const __grid_constant__ FusedArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -581,11 +598,11 @@ __global__ void __launch_bounds__(kFThreads, 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmRing);
-        prefetch_tmap(&tmG);
-        prefetch_tmap(&tmU);
-        prefetch_tmap(&tmH);
-        prefetch_tmap(&tmD);
+        prefetch_tmap(&pm.ring);
+        prefetch_tmap(&pm.g);
+        prefetch_tmap(&pm.u);
+        prefetch_tmap(&pm.h);
+        prefetch_tmap(&pm.dn);
     }
     if (warp == 1) {
         tmem_alloc(tmem_holder, kTmemCols);
@@ -636,12 +653,16 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     break;
                 }
                 const int e = expert_of_row(s_pad, a.E, static_cast<int64_t>(m) * kBM);
+                const int cnt_e = a.counts[e];
                 if (f1 ? !(a.prologue || spin_ge(&ready[m], 2, a, abort_flag))
                        : !spin_ge(&h_done[m], 4 * a.NT1, a, abort_flag))
                     break;
                 fence_proxy_async_global();
                 const int BN = f1 ? 256 : a.BN2;
-                const uint32_t stage_bytes = kAStage + (BN / 128) * 16384 + (MX ? kSfaBytes + (BN / 128) * 512 : 0);
+                // every tile holds at least one of its expert's rows: 64 or 128 to load
+                const int arows = a_rows_to_load(cnt_e, static_cast<int64_t>(m) * kBM - s_pad[e]);
+                const uint32_t stage_bytes =
+                    arows * kBKBytes + (BN / 128) * 16384 + (MX ? kSfaBytes + (BN / 128) * 512 : 0);
                 const int kst = f1 ? a.k1 : a.k2;
                 const int ya = f1 ? static_cast<int>((static_cast<int64_t>(m) * kBM) % a.ring_rows) : m * kBM;
                 const int yb = f1 ? e * a.F + n * 128 : e * a.d + n * BN;
@@ -652,13 +673,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     const int x = ks * kE;
                     mbar_arrive_expect_tx(&full[stage], stage_bytes);
                     if (f1) {
-                        tma_load_2d(dA, &tmRing, &full[stage], x, ya);
-                        tma_load_2d(dB, &tmG, &full[stage], x, yb);
-                        tma_load_2d(dB + 16384, &tmU, &full[stage], x, yb);
+                        tma_load_2d(dA, arows == kBM ? &pm.ring : &pm.ring64, &full[stage], x, ya);
+                        tma_load_2d(dB, &pm.g, &full[stage], x, yb);
+                        tma_load_2d(dB + 16384, &pm.u, &full[stage], x, yb);
                     } else {
-                        tma_load_2d(dA, &tmH, &full[stage], x, ya);
-                        tma_load_2d(dB, &tmD, &full[stage], x, yb);
-                        if (BN == 256) tma_load_2d(dB + 16384, &tmD, &full[stage], x, yb + 128);
+                        tma_load_2d(dA, arows == kBM ? &pm.h : &pm.h64, &full[stage], x, ya);
+                        tma_load_2d(dB, &pm.dn, &full[stage], x, yb);
+                        if (BN == 256) tma_load_2d(dB + 16384, &pm.dn, &full[stage], x, yb + 128);
                     }
                     if constexpr (MX) {
                         uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
@@ -878,9 +899,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
 // ids to both CTAs through a cluster-wide queue; the even CTA issues the MMAs
 // and scale copies; both CTAs run the epilogue of their own rows.  When an
 // expert has an odd number of row tiles its last pair tile has a ghost odd
-// half: the odd CTA loads its A operand from rows past the end of the tensor
-// (TMA fills zeros without reading memory), stores nothing and signals no
-// counter.  Gather CTAs come in pairs and a pair
+// half: the odd CTA loads only its half of B (its A rows in shared memory are
+// stale; their results are discarded), stores nothing and signals no counter.
+// A half with 64 valid rows or fewer loads only those 64 rows of A.  Gather CTAs come in pairs and a pair
 // enters the GEMM role only once both of its CTAs have finished gathering, so
 // a pair never holds a tile while one of its CTAs waits in the gather role.
 // Tiles keep the single-CTA kernel's per-row arithmetic, so results are
@@ -889,10 +910,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
 constexpr int kFPStages = 6;
 constexpr int kFPStage = kAStage + 128 * kBKBytes;  // 32 KB: A rows + one half of B
 
-struct FusedPairMaps {
-    CUtensorMap ring, g, u, h, dn;   // operands (as k_moe_fused)
-    CUtensorMap s_ring, s_g, s_u, s_h, s_dn;  // MX scale tiles (MXFP8 only)
-};
 
 // Pair tile t of one phase (NT N tiles per pair row): expert e, pair row j of
 // that expert (row tiles 2j and 2j + 1 of its segment), N tile n; the same
@@ -923,7 +940,7 @@ __device__ __forceinline__ PPTile decode_pair_tile(int t, const int *s_pp, int E
 
 template <bool MX>
 __global__ void __launch_bounds__(kFThreads, 1)
-    k_moe_fused_pair(const __grid_constant__ FusedPairMaps pm, const __grid_constant__ FusedArgs a)
+    k_moe_fused_pair(const __grid_constant__ FusedMaps pm, const __grid_constant__ FusedArgs a)
 {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1041,7 +1058,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const uint32_t tq_full_odd = mapa_shared(smem_u32(tq_full), 1);
             const uint32_t tq_odd = mapa_shared(smem_u32(tq), 1);
             const uint32_t tq_empty_even = mapa_shared(smem_u32(tq_empty), 0);
-            const uint32_t cta_bytes = kFPStage + (MX ? kSfaBytes + kSfbBytes : 0);
             for (;;) {
                 int tile;
                 if (rank == 0) {
@@ -1070,24 +1086,27 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     report_timeout(a.status, abort_flag);  // a schedule bug: stop, touch nothing
                     break;
                 }
-                // a ghost half waits for the even half's rows and loads its A
-                // operand from rows past the end of the tensor (TMA fills zeros and
-                // reads no memory); its results are discarded
-                const int ma = jb.ghost ? jb.m0 : m;
-                if (jb.f1 ? !(a.prologue || spin_ge(&ready[ma], 2, a, abort_flag))
-                          : !spin_ge(&h_done[ma], 4 * a.NT1, a, abort_flag))
+                // rows of A each half loads (a ghost half none: it only loads its half of
+                // B, and its results are discarded); the even CTA's barrier counts both
+                const int cnt_e = a.counts[jb.e];
+                const int64_t rel0 = static_cast<int64_t>(jb.m0) * kBM - s_pad[jb.e];
+                const int rows0 = a_rows_to_load(cnt_e, rel0), rows1 = a_rows_to_load(cnt_e, rel0 + kBM);
+                const int my_rows = rank ? rows1 : rows0;
+                const uint32_t tx = 2u * (128 * kBKBytes + (MX ? kSfbBytes : 0)) +
+                                    static_cast<uint32_t>((rows0 + rows1) * kBKBytes) +
+                                    (MX ? ((rows0 ? kSfaBytes : 0) + (rows1 ? kSfaBytes : 0)) : 0u);
+                if (my_rows > 0 && (jb.f1 ? !(a.prologue || spin_ge(&ready[m], 2, a, abort_flag))
+                                          : !spin_ge(&h_done[m], 4 * a.NT1, a, abort_flag)))
                     break;
                 fence_proxy_async_global();
                 const int kst = jb.f1 ? a.k1 : a.k2;
                 const int64_t arows = jb.f1 ? a.ring_rows : a.h_rows;
-                const int ya = jb.ghost ? static_cast<int>(arows)
-                               : jb.f1 ? static_cast<int>((static_cast<int64_t>(ma) * kBM) % a.ring_rows) : ma * kBM;
-                // scale tiles of A: (K / 128) x (rows / 128) of them; the ghost's lie past the last
-                const int sfa_end = static_cast<int>(((jb.f1 ? a.d : a.F) >> 7) * (arows >> 7));
+                const int ya = jb.f1 ? static_cast<int>((static_cast<int64_t>(m) * kBM) % a.ring_rows) : m * kBM;
+                const CUtensorMap *amap = jb.f1 ? (my_rows == kBM ? &pm.ring : &pm.ring64)
+                                                : (my_rows == kBM ? &pm.h : &pm.h64);
                 // B rows of this CTA's half, and the first B row of the tile (scales)
                 const int yb_tile = jb.f1 ? jb.e * a.F + jb.n * 128 : jb.e * a.d + jb.n * 256;
                 const int yb = jb.f1 ? yb_tile : yb_tile + static_cast<int>(rank) * 128;
-                const CUtensorMap *amap = jb.f1 ? &pm.ring : &pm.h;
                 const CUtensorMap *bmap = jb.f1 ? (rank ? &pm.u : &pm.g) : &pm.dn;
                 const CUtensorMap *samap = jb.f1 ? &pm.s_ring : &pm.s_h;
                 for (int ks = 0; ks < kst; ++ks) {
@@ -1095,12 +1114,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     uint8_t *dA = sT + stage * kFPStage;
                     const int x = ks * kE;
                     const uint32_t fb = full0 + stage * 8;
-                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * cta_bytes);
-                    tma_load_2d_pair(dA, amap, fb, x, ya);
+                    if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
+                    if (my_rows > 0) tma_load_2d_pair(dA, amap, fb, x, ya);
                     tma_load_2d_pair(dA + kAStage, bmap, fb, x, yb);
                     if constexpr (MX) {
                         uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
-                        tma_load_2d_pair(dS, samap, fb, 0, jb.ghost ? sfa_end : sf_tile(x, ya, arows));
+                        if (my_rows > 0) tma_load_2d_pair(dS, samap, fb, 0, sf_tile(x, ya, arows));
                         if (jb.f1) {
                             tma_load_2d_pair(dS + kSfaBytes, &pm.s_g, fb, 0, sf_tile(x, yb_tile, a.EF));
                             tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_u, fb, 0, sf_tile(x, yb_tile, a.EF));
@@ -1329,7 +1348,7 @@ cudaError_t fused_pair_setup(int *grid_out)
 }
 
 template <bool MX>
-cudaError_t launch_fused_pair_t(const FusedPairMaps &pm, const FusedArgs &args, int grid, cudaStream_t st)
+cudaError_t launch_fused_pair_t(const FusedMaps &pm, const FusedArgs &args, int grid, cudaStream_t st)
 {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
@@ -1354,9 +1373,7 @@ constexpr size_t fused_smem_bytes()
 }
 
 template <bool MX>
-cudaError_t launch_fused_t(const CUtensorMap &ring, const CUtensorMap &g, const CUtensorMap &u,
-                           const CUtensorMap &h, const CUtensorMap &dn, const FusedArgs &args,
-                           cudaStream_t st)
+cudaError_t launch_fused_t(const FusedMaps &pm, const FusedArgs &args, cudaStream_t st)
 {
     constexpr size_t smem = fused_smem_bytes<MX>();
     static std::once_flag once;
@@ -1380,7 +1397,7 @@ cudaError_t launch_fused_t(const CUtensorMap &ring, const CUtensorMap &g, const 
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_moe_fused<MX>, ring, g, u, h, dn, args);
+    return cudaLaunchKernelEx(&cfg, k_moe_fused<MX>, pm, args);
 }
 
 int gather_ctas(int sms, float frac)
@@ -1523,12 +1540,14 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     if (ring_rows < 256) return cudaErrorInvalidValue;
     const uint64_t EF = static_cast<uint64_t>(dm.E) * dm.F;
     const uint64_t Ed = static_cast<uint64_t>(dm.E) * dm.d;
-    CUtensorMap tr, tg, tu, th, td;
-    if (encode_tmap_2d(&tr, io.ring, mx, dm.d, ring_rows, box, kBM) ||
-        encode_tmap_2d(&tg, mx ? static_cast<const void *>(w->q_gate) : w->w_gate, mx, dm.d, EF, box, 128) ||
-        encode_tmap_2d(&tu, mx ? static_cast<const void *>(w->q_up) : w->w_up, mx, dm.d, EF, box, 128) ||
-        encode_tmap_2d(&th, io.h, mx, dm.F, dm.rows_pad, box, kBM) ||
-        encode_tmap_2d(&td, mx ? static_cast<const void *>(w->q_down) : w->w_down, mx, dm.F, Ed, box, 128))
+    FusedMaps pm = {};
+    if (encode_tmap_2d(&pm.ring, io.ring, mx, dm.d, ring_rows, box, kBM) ||
+        encode_tmap_2d(&pm.ring64, io.ring, mx, dm.d, ring_rows, box, 64) ||
+        encode_tmap_2d(&pm.g, mx ? static_cast<const void *>(w->q_gate) : w->w_gate, mx, dm.d, EF, box, 128) ||
+        encode_tmap_2d(&pm.u, mx ? static_cast<const void *>(w->q_up) : w->w_up, mx, dm.d, EF, box, 128) ||
+        encode_tmap_2d(&pm.h, io.h, mx, dm.F, dm.rows_pad, box, kBM) ||
+        encode_tmap_2d(&pm.h64, io.h, mx, dm.F, dm.rows_pad, box, 64) ||
+        encode_tmap_2d(&pm.dn, mx ? static_cast<const void *>(w->q_down) : w->w_down, mx, dm.F, Ed, box, 128))
         return cudaErrorInvalidValue;
     FusedArgs a = {};
     a.E = dm.E;
@@ -1591,13 +1610,7 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     a.skip_combine = io.skip_combine ? 1 : 0;
     a.status = status;
     a.wait_ns = wait_ns;
-    FusedPairMaps pm = {};
     if (pair) {
-        pm.ring = tr;
-        pm.g = tg;
-        pm.u = tu;
-        pm.h = th;
-        pm.dn = td;
         if (mx && (encode_tmap_scales(&pm.s_ring, io.ring_scales, static_cast<uint64_t>(ring_rows), dm.d) ||
                    encode_tmap_scales(&pm.s_g, w->s_gate, EF, dm.d) ||
                    encode_tmap_scales(&pm.s_u, w->s_up, EF, dm.d) ||
@@ -1608,8 +1621,7 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     cudaError_t e = cudaMemsetAsync(io.counters, 0, sizeof(int) * fused_counter_ints(dm), st);
     if (e != cudaSuccess) return e;
     if (pair) return mx ? launch_fused_pair_t<true>(pm, a, grid, st) : launch_fused_pair_t<false>(pm, a, grid, st);
-    return mx ? launch_fused_t<true>(tr, tg, tu, th, td, a, st)
-              : launch_fused_t<false>(tr, tg, tu, th, td, a, st);
+    return mx ? launch_fused_t<true>(pm, a, st) : launch_fused_t<false>(pm, a, st);
 }
 
 }  // namespace mok
