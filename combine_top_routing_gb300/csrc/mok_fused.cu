@@ -837,6 +837,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const int e = expert_of_row(s_pad, a.E, static_cast<int64_t>(m) * kBM);
             const int64_t row_in_e = q - s_pad[e];
             const bool valid = row_in_e < a.counts[e];
+            // FFN2: this row's token slot in ystage, looked up while the tile's MMAs
+            // run (the accumulator is handed back only after the lookup)
+            uint16_t *dst = nullptr;
+            if (!f1 && valid) {
+                const int64_t p = a.offsets[e] + row_in_e;
+                dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k + a.row_j[p]) * a.d + n * a.BN2;
+            }
             if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
             tc_fence_after();
             bool released = false;
@@ -850,12 +857,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 epi_ffn1<MX>(trow, valid, q, n * 128, a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b,
                              a.saved_h, stage_out + (warp - 2) * kStageWords, lane, release);
             } else {
-                uint16_t *dst = nullptr;
-                if (valid) {
-                    const int64_t p = a.offsets[e] + row_in_e;
-                    dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k + a.row_j[p]) * a.d +
-                          n * a.BN2;
-                }
                 epi_rows_bf16(trow, a.BN2, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
                               release);
             }
@@ -1257,6 +1258,12 @@ __global__ void __launch_bounds__(kFThreads, 1)
             const int64_t q = static_cast<int64_t>(m) * kBM + r;  // padded row of this thread
             const int64_t row_in_e = q - s_pad[jb.e];
             const bool valid = !jb.ghost && row_in_e < a.counts[jb.e];
+            // FFN2: this row's token slot in ystage, looked up while the tile's MMAs run
+            uint16_t *dst = nullptr;
+            if (!jb.f1 && valid) {
+                const int64_t p = a.offsets[jb.e] + row_in_e;
+                dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k + a.row_j[p]) * a.d + jb.n * 256;
+            }
             if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
             tc_fence_after();
             bool released = false;
@@ -1270,11 +1277,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 epi_ffn1<MX>(trow, valid, q, jb.n * 128, a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b,
                              a.saved_h, stage_out + (warp - 2) * kStageWords, lane, release);
             } else {
-                uint16_t *dst = nullptr;
-                if (valid) {
-                    const int64_t p = a.offsets[jb.e] + row_in_e;
-                    dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k + a.row_j[p]) * a.d + jb.n * 256;
-                }
                 epi_rows_bf16(trow, 256, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane, release);
             }
             if (!released) release();

@@ -351,6 +351,56 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
             const Tile tl = decode_tile(tile, prefix, groups, a.n_tiles);
+            // What this thread's row needs from global memory is looked up while
+            // the tile's MMAs run, not after the accumulator is full: the expert's
+            // counts and offsets, FFN2's token slot, DGRAD2's first 32 columns of
+            // the saved a, b (the rest prefetched into L2).
+            const int e = tl.group;
+            const int row_in_e = tl.m_blk * kBM + r;
+            bool valid = true;
+            int64_t grow = 0;
+            uint16_t *dst = nullptr;
+            bool empty_k = false;
+            uint4 na[4], nb[4];
+            int c_begin = 0, c_end = 0, f0 = 0;
+            if constexpr (MODE == MODE_FFN1 || MODE == MODE_FFN2 || MODE == MODE_DGRAD2 || MODE == MODE_DGRAD1) {
+                valid = row_in_e < a.counts[e];
+                grow = a.pad_offsets[e] + row_in_e;
+            }
+            if constexpr (MODE == MODE_FFN2) {
+                if (valid) {
+                    const int64_t p = a.offsets[e] + row_in_e;
+                    const int64_t t = a.row_tok[p];
+                    const int64_t j = a.row_j[p];
+                    dst = a.ystage + (t * a.k_top + j) * a.d + tl.n_blk * BN;
+                }
+            } else if constexpr (MODE == MODE_DGRAD1) {
+                dst = a.out_rows + grow * a.d + tl.n_blk * BN;
+            } else if constexpr (MODE == MODE_WGRAD) {
+                empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
+                dst = a.out_rows + (static_cast<int64_t>(e) * a.m_rows + tl.m_blk * kBM + r) * a.out_ld +
+                      tl.n_blk * BN;
+            } else if constexpr (MODE == MODE_DGRAD2) {
+                // warps 2-5 take accumulator columns [0, 128), warps 6-9 [128, 256)
+                // (nothing when BN = 128): whole 128-column MX scale groups each
+                c_begin = ((warp - 2) >> 2) * 128;
+                c_end = min(BN, c_begin + 128);
+                f0 = tl.n_blk * BN + c_begin;
+                if (valid && c_begin < c_end) {
+                    const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + grow * a.F + f0);
+                    const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + grow * a.F + f0);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        na[q] = __ldg(pa + q);
+                        nb[q] = __ldg(pb + q);
+                    }
+                    // the rest of the row's columns: 64-byte pieces, 128-byte lines
+                    for (int c = 64; c < 2 * (c_end - c_begin); c += 128) {
+                        prefetch_l2(reinterpret_cast<const uint8_t *>(a.in_a + grow * a.F + f0) + c);
+                        prefetch_l2(reinterpret_cast<const uint8_t *>(a.in_b + grow * a.F + f0) + c);
+                    }
+                }
+            }
             if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
             tc_fence_after();
             // Hands the accumulator back to the MMA warp; epilogues that first
@@ -382,49 +432,17 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
                     }
                 }
             } else if constexpr (MODE == MODE_FFN1) {
-                const int e = tl.group;
-                const int row_in_e = tl.m_blk * kBM + r;
-                epi_ffn1<MX>(trow, row_in_e < a.counts[e], a.pad_offsets[e] + row_in_e, tl.n_blk * 128,
-                             a.F, a.h, a.h_scales, a.h_rows, a.saved_a, a.saved_b, a.saved_h,
-                             stage_out + (warp - 2) * kStageWords, lane, release);
+                epi_ffn1<MX>(trow, valid, grow, tl.n_blk * 128, a.F, a.h, a.h_scales, a.h_rows, a.saved_a,
+                             a.saved_b, a.saved_h, stage_out + (warp - 2) * kStageWords, lane, release);
             } else if constexpr (MODE == MODE_FFN2) {
-                const int e = tl.group;
-                const int row_in_e = tl.m_blk * kBM + r;
-                const bool valid = row_in_e < a.counts[e];
-                uint16_t *dst = nullptr;
-                if (valid) {
-                    const int64_t p = a.offsets[e] + row_in_e;
-                    const int64_t t = a.row_tok[p];
-                    const int64_t j = a.row_j[p];
-                    dst = a.ystage + (t * a.k_top + j) * a.d + tl.n_blk * BN;
-                }
                 epi_rows_bf16(trow, BN, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
                               release);
             } else if constexpr (MODE == MODE_DGRAD2) {
                 // dh -> SwiGLU backward with the saved (BF16) a, b:
                 //   s = sigmoid(a), da = dh b s (1 + a (1 - s)), db = dh a s
-                const int e = tl.group;
-                const int row_in_e = tl.m_blk * kBM + r;
-                const bool valid = row_in_e < a.counts[e];
-                const int64_t grow = a.pad_offsets[e] + row_in_e;
-                // warps 2-5 take accumulator columns [0, 128), warps 6-9 [128, 256)
-                // (nothing when BN = 128): whole 128-column MX scale groups each
-                const int c_begin = ((warp - 2) >> 2) * 128;
-                const int c_end = min(BN, c_begin + 128);
-                const int f0 = tl.n_blk * BN + c_begin;
+                // (the first 32 columns of a, b are in na / nb; each chunk loads the
+                // next one's while it is processed)
                 uint32_t wa = 0, wb = 0;
-                // the saved a, b of the next 32 columns are loaded while this
-                // chunk is processed (software pipeline over the row's chunks)
-                uint4 na[4], nb[4];
-                if (valid && c_begin < c_end) {
-                    const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + grow * a.F + f0);
-                    const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + grow * a.F + f0);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        na[q] = __ldg(pa + q);
-                        nb[q] = __ldg(pb + q);
-                    }
-                }
                 for (int c = 0; c < c_end - c_begin; c += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32(trow + c_begin + c, v);
@@ -482,19 +500,9 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
                     }
                 }
             } else if constexpr (MODE == MODE_DGRAD1) {
-                const int e = tl.group;
-                const int row_in_e = tl.m_blk * kBM + r;
-                const bool valid = row_in_e < a.counts[e];
-                const int64_t grow = a.pad_offsets[e] + row_in_e;
-                uint16_t *dst = a.out_rows + grow * a.d + tl.n_blk * BN;
                 epi_rows_bf16(trow, BN, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
                               release);
             } else {  // MODE_WGRAD
-                const int e = tl.group;
-                const bool empty_k = a.pad_offsets[e + 1] == a.pad_offsets[e];
-                uint16_t *dst = a.out_rows +
-                                (static_cast<int64_t>(e) * a.m_rows + tl.m_blk * kBM + r) * a.out_ld +
-                                tl.n_blk * BN;
                 epi_rows_bf16(trow, BN, empty_k, true, dst, stage_out + (warp - 2) * kStageWords, lane,
                               release);
             }
@@ -787,6 +795,22 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
         uint32_t acc_phase = 0;
         for (int tile = pair; tile < total; tile += npairs) {
             const Tile tl = locate(tile);
+            const int e = tl.group;
+            const int row_in_e = (2 * tl.m_blk + static_cast<int>(rank)) * kBM + r;
+            // FFN1 / FFN2: the row's counts, offsets and token slot, looked up while
+            // the tile's MMAs run
+            bool valid = true;
+            int64_t grow = 0;
+            uint16_t *dst = nullptr;
+            if constexpr (MODE != MODE_WGRAD) {
+                valid = row_in_e < a.counts[e];
+                grow = a.pad_offsets[e] + row_in_e;
+                if (MODE == MODE_FFN2 && valid) {
+                    const int64_t p = a.offsets[e] + row_in_e;
+                    dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k_top + a.row_j[p]) * a.d +
+                          tl.n_blk * 256;
+                }
+            }
             if (!wait_bar(acc_full, acc_phase, a.status, a.wait_ns, abort_flag)) break;
             tc_fence_after();
             bool released = false;
@@ -796,8 +820,6 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
                 if (lane == 0) mbar_arrive_remote_relaxed(acc_empty_leader);
                 released = true;
             };
-            const int e = tl.group;
-            const int row_in_e = (2 * tl.m_blk + static_cast<int>(rank)) * kBM + r;
             if constexpr (MODE == MODE_WGRAD) {
                 // dW rows (expert e) x this warp's columns; zeros for an expert without rows.
                 // The accumulator is released once it is in registers; the rows go to this
@@ -829,18 +851,9 @@ __global__ void __launch_bounds__(PairShape<MODE>::kThreads, 1)
                     }
                 }
             } else if constexpr (MODE == MODE_FFN1) {
-                const bool valid = row_in_e < a.counts[e];
-                epi_ffn1<MX>(trow, valid, a.pad_offsets[e] + row_in_e, tl.n_blk * 128, a.F, a.h, a.h_scales,
-                             a.h_rows, a.saved_a, a.saved_b, a.saved_h, stage_out + (warp - 2) * kStageWords,
-                             lane, release);
+                epi_ffn1<MX>(trow, valid, grow, tl.n_blk * 128, a.F, a.h, a.h_scales, a.h_rows, a.saved_a,
+                             a.saved_b, a.saved_h, stage_out + (warp - 2) * kStageWords, lane, release);
             } else {
-                const bool valid = row_in_e < a.counts[e];
-                uint16_t *dst = nullptr;
-                if (valid) {
-                    const int64_t p = a.offsets[e] + row_in_e;
-                    dst = a.ystage + (static_cast<int64_t>(a.row_tok[p]) * a.k_top + a.row_j[p]) * a.d +
-                          tl.n_blk * 256;
-                }
                 epi_rows_bf16(trow, 256, false, valid, dst, stage_out + (warp - 2) * kStageWords, lane,
                               release);
             }
