@@ -50,6 +50,11 @@ namespace {
 #endif
 constexpr int kCluster = MOK_GEMM_CLUSTER;  // CTAs per cluster of the GEMM launch
 enum { MODE_ROUTER = 0, MODE_FFN1, MODE_FFN2, MODE_DGRAD2, MODE_DGRAD1, MODE_WGRAD };
+// Epilogue staging: four warps of 32 rows x 33 words, or DGRAD2's eight warps
+// of 32 rows x 17 words (64-byte row segments)
+constexpr int kD2StageWords = 32 * 17;
+constexpr size_t kGemmStageBytes =
+    kStageBytes > 8 * kD2StageWords * 4 ? kStageBytes : static_cast<size_t>(8 * kD2StageWords * 4);
 
 template <int NA>
 struct AMaps {
@@ -362,6 +367,8 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
             uint16_t *dst = nullptr;
             bool empty_k = false;
             uint4 na[4], nb[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) na[q] = nb[q] = make_uint4(0, 0, 0, 0);
             int c_begin = 0, c_end = 0, f0 = 0;
             if constexpr (MODE == MODE_FFN1 || MODE == MODE_FFN2 || MODE == MODE_DGRAD2 || MODE == MODE_DGRAD1) {
                 valid = row_in_e < a.counts[e];
@@ -442,60 +449,70 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
                 //   s = sigmoid(a), da = dh b s (1 + a (1 - s)), db = dh a s
                 // (the first 32 columns of a, b are in na / nb; each chunk loads the
                 // next one's while it is processed)
+                // Every lane computes (rows past the expert's count on zeros) and
+                // takes part in the staged stores, which write whole row segments;
+                // only valid rows are stored.
                 uint32_t wa = 0, wb = 0;
+                uint32_t *stg = stage_out + (warp - 2) * kD2StageWords;
                 for (int c = 0; c < c_end - c_begin; c += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32(trow + c_begin + c, v);
                     tmem_ld_wait();
-                    if (valid) {
-                        const int64_t off = grow * a.F + f0 + c;
-                        float av[32], bv[32], da[32], db[32];
+                    const int64_t off = grow * a.F + f0 + c;
+                    float av[32], bv[32], da[32], db[32];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint32_t ua[4] = {na[q].x, na[q].y, na[q].z, na[q].w};
+                        const uint32_t ub[4] = {nb[q].x, nb[q].y, nb[q].z, nb[q].w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            av[8 * q + 2 * i] = bf16_bits_to_float(ua[i] & 0xFFFFu);
+                            av[8 * q + 2 * i + 1] = bf16_bits_to_float(ua[i] >> 16);
+                            bv[8 * q + 2 * i] = bf16_bits_to_float(ub[i] & 0xFFFFu);
+                            bv[8 * q + 2 * i + 1] = bf16_bits_to_float(ub[i] >> 16);
+                        }
+                    }
+                    if (valid && c + 32 < c_end - c_begin) {
+                        const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + off + 32);
+                        const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + off + 32);
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            const uint32_t ua[4] = {na[q].x, na[q].y, na[q].z, na[q].w};
-                            const uint32_t ub[4] = {nb[q].x, nb[q].y, nb[q].z, nb[q].w};
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                av[8 * q + 2 * i] = bf16_bits_to_float(ua[i] & 0xFFFFu);
-                                av[8 * q + 2 * i + 1] = bf16_bits_to_float(ua[i] >> 16);
-                                bv[8 * q + 2 * i] = bf16_bits_to_float(ub[i] & 0xFFFFu);
-                                bv[8 * q + 2 * i + 1] = bf16_bits_to_float(ub[i] >> 16);
-                            }
+                            na[q] = __ldg(pa + q);
+                            nb[q] = __ldg(pb + q);
                         }
-                        if (c + 32 < c_end - c_begin) {
-                            const uint4 *pa = reinterpret_cast<const uint4 *>(a.in_a + off + 32);
-                            const uint4 *pb = reinterpret_cast<const uint4 *>(a.in_b + off + 32);
+                    }
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                na[q] = __ldg(pa + q);
-                                nb[q] = __ldg(pb + q);
-                            }
-                        }
+                    for (int i = 0; i < 32; ++i) {
+                        const float dh = __uint_as_float(v[i]);
+                        const float s = 1.0f / (1.0f + __expf(-av[i]));
+                        da[i] = dh * bv[i] * s * (1.0f + av[i] * (1.0f - s));
+                        db[i] = dh * av[i] * s;
+                    }
+                    uint32_t pk[16];
+                    pack_bf16x32(da, pk);
+                    store_rows_staged_n<16>(pk, valid ? a.out_da + off : nullptr, stg, lane);
+                    pack_bf16x32(db, pk);
+                    store_rows_staged_n<16>(pk, valid ? a.out_db + off : nullptr, stg, lane);
+                    if constexpr (MX) {
+                        // quantise the BF16-rounded values (the stored da, db)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) {
-                            const float dh = __uint_as_float(v[i]);
-                            const float s = 1.0f / (1.0f + __expf(-av[i]));
-                            da[i] = dh * bv[i] * s * (1.0f + av[i] * (1.0f - s));
-                            db[i] = dh * av[i] * s;
+                            da[i] = bf16_bits_to_float(float_to_bf16_bits(da[i]));
+                            db[i] = bf16_bits_to_float(float_to_bf16_bits(db[i]));
                         }
-                        store_bf16x32(a.out_da + off, da);
-                        store_bf16x32(a.out_db + off, db);
-                        if constexpr (MX) {
-                            // quantise the BF16-rounded values (the stored da, db)
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) {
-                                da[i] = bf16_bits_to_float(float_to_bf16_bits(da[i]));
-                                db[i] = bf16_bits_to_float(float_to_bf16_bits(db[i]));
-                            }
-                            const int sh = 8 * ((c >> 5) & 3);
-                            wa |= quant_mx32(da, a.q_da + off) << sh;
-                            wb |= quant_mx32(db, a.q_db + off) << sh;
-                            if ((c & 127) == 96) {
+                        const int sh = 8 * ((c >> 5) & 3);
+                        uint32_t qc[8];
+                        wa |= mx_block32(da, qc) << sh;
+                        store_rows_staged_n<8>(qc, valid ? a.q_da + off : nullptr, stg, lane);
+                        wb |= mx_block32(db, qc) << sh;
+                        store_rows_staged_n<8>(qc, valid ? a.q_db + off : nullptr, stg, lane);
+                        if ((c & 127) == 96) {
+                            if (valid) {
                                 const int64_t wi = scale_word_row((f0 + c) >> 7, grow, a.h_rows);
                                 a.s_da[wi] = wa;
                                 a.s_db[wi] = wb;
-                                wa = wb = 0;
                             }
+                            wa = wb = 0;
                         }
                     }
                 }
@@ -926,7 +943,7 @@ template <bool MX>
 constexpr size_t smem_bytes()
 {
     return 1024 + kStages * (kAStage + kBStage) + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0) +
-           (2 * kStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+           (2 * kStages + 2) * 8 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kGemmStageBytes;
 }
 
 template <int MODE, bool MX>
