@@ -562,7 +562,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     uint64_t *full = bars;
     uint64_t *empty = bars + kStages;
     uint64_t *sf_ready = bars + 2 * kStages;  // MXFP8: the stage's scales are in TMEM
-    uint64_t *acc_full = bars + 3 * kStages;
+    uint64_t *sf_full = bars + 3 * kStages;   // MXFP8: the stage's scale bytes have landed
+    uint64_t *acc_full = bars + 4 * kStages;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *tq_full = acc_empty + 1;
     uint64_t *tq_empty = tq_full + kTQ;
@@ -587,6 +588,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 1);
+            mbar_init(&sf_full[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
@@ -661,8 +663,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const int BN = f1 ? 256 : a.BN2;
                 // every tile holds at least one of its expert's rows: 64 or 128 to load
                 const int arows = a_rows_to_load(cnt_e, static_cast<int64_t>(m) * kBM - s_pad[e]);
-                const uint32_t stage_bytes =
-                    arows * kBKBytes + (BN / 128) * 16384 + (MX ? kSfaBytes + (BN / 128) * 512 : 0);
+                const uint32_t stage_bytes = arows * kBKBytes + (BN / 128) * 16384;
+                const uint32_t sf_bytes = kSfaBytes + (BN / 128) * 512;
                 const int kst = f1 ? a.k1 : a.k2;
                 const int ya = f1 ? static_cast<int>((static_cast<int64_t>(m) * kBM) % a.ring_rows) : m * kBM;
                 const int yb = f1 ? e * a.F + n * 128 : e * a.d + n * BN;
@@ -671,6 +673,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     uint8_t *dA = sA + stage * kAStage;
                     uint8_t *dB = sB + stage * kBStage;
                     const int x = ks * kE;
+                    if constexpr (MX) {
+                        // the scales first, on their own barrier: the copier copies them
+                        // into TMEM as soon as they land, so the copies (which the tensor
+                        // pipe runs in order with the MMAs already issued) are done before
+                        // the stage's operands arrive
+                        uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
+                        mbar_arrive_expect_tx(&sf_full[stage], sf_bytes);
+                        if (f1) {
+                            bulk_load(dS, a.ring_scales + scale_word(x, ya, a.ring_rows), kSfaBytes, &sf_full[stage]);
+                            bulk_load(dS + kSfaBytes, a.s_gate + scale_word(x, yb, a.EF), 512, &sf_full[stage]);
+                            bulk_load(dS + kSfaBytes + 512, a.s_up + scale_word(x, yb, a.EF), 512, &sf_full[stage]);
+                        } else {
+                            bulk_load(dS, a.h_scales + scale_word(x, ya, a.h_rows), kSfaBytes, &sf_full[stage]);
+                            bulk_load(dS + kSfaBytes, a.s_down + scale_word(x, yb, a.Ed), (BN / 128) * 512,
+                                      &sf_full[stage]);
+                        }
+                    }
                     mbar_arrive_expect_tx(&full[stage], stage_bytes);
                     if (f1) {
                         tma_load_2d(dA, arows == kBM ? &pm.ring : &pm.ring64, &full[stage], x, ya);
@@ -680,18 +699,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
                         tma_load_2d(dA, arows == kBM ? &pm.h : &pm.h64, &full[stage], x, ya);
                         tma_load_2d(dB, &pm.dn, &full[stage], x, yb);
                         if (BN == 256) tma_load_2d(dB + 16384, &pm.dn, &full[stage], x, yb + 128);
-                    }
-                    if constexpr (MX) {
-                        uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
-                        if (f1) {
-                            bulk_load(dS, a.ring_scales + scale_word(x, ya, a.ring_rows), kSfaBytes, &full[stage]);
-                            bulk_load(dS + kSfaBytes, a.s_gate + scale_word(x, yb, a.EF), 512, &full[stage]);
-                            bulk_load(dS + kSfaBytes + 512, a.s_up + scale_word(x, yb, a.EF), 512, &full[stage]);
-                        } else {
-                            bulk_load(dS, a.h_scales + scale_word(x, ya, a.h_rows), kSfaBytes, &full[stage]);
-                            bulk_load(dS + kSfaBytes, a.s_down + scale_word(x, yb, a.Ed), (BN / 128) * 512,
-                                      &full[stage]);
-                        }
                     }
                     if (++stage == kStages) {
                         stage = 0;
@@ -726,10 +733,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kst; ++ks) {
-                    // MXFP8: sf_ready (the scale copier waited for the loads, then
-                    // copied the stage's scales into TMEM); BF16: the loads
-                    if (!wait_bar(MX ? &sf_ready[stage] : &full[stage], phase, a.status, a.wait_ns, abort_flag))
-                        goto mma_done;
+                    // the operands, and (MXFP8) the stage's scales in TMEM (sf_ready)
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    if (MX && !wait_bar(&sf_ready[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
                     tc_fence_after();
                     if (f1 && ks == kst - 1) {
                         // every ring row of row tile m this tile needs is now in shared memory
@@ -765,9 +771,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
         if (MX && lane == 0) {
             // ------------------------------------------------ scale copier
             // the same tile and stage sequence as the MMA issuer: once a stage's
-            // loads have landed, copy its A and B scales into the stage's TMEM
-            // columns and commit to sf_ready (a scale slot is refilled only after
-            // empty[stage], i.e. after the MMAs that read it have completed)
+            // scale bytes have landed (sf_full), copy its A and B scales into the
+            // stage's TMEM columns and commit to sf_ready (a scale slot is refilled
+            // only after empty[stage], i.e. after the MMAs that read it completed)
             uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
             const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
@@ -785,7 +791,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const int BN = f1 ? 256 : a.BN2;
                 const int kst = f1 ? a.k1 : a.k2;
                 for (int ks = 0; ks < kst; ++ks) {
-                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto copier_done;
+                    if (!wait_bar(&sf_full[stage], phase, a.status, a.wait_ns, abort_flag)) goto copier_done;
                     tc_fence_after();
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
@@ -952,7 +958,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     uint64_t *full = bars;
     uint64_t *empty = bars + kFPStages;
     uint64_t *sf_ready = bars + 2 * kFPStages;  // MXFP8, even CTA: the stage's scales are in TMEM
-    uint64_t *acc_full = bars + 3 * kFPStages;
+    uint64_t *sf_full = bars + 3 * kFPStages;   // MXFP8, even CTA: both CTAs' scale bytes have landed
+    uint64_t *acc_full = bars + 4 * kFPStages;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *tq_full = acc_empty + 1;
     uint64_t *tq_empty = tq_full + kTQ;
@@ -979,6 +986,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sf_ready[s], 1);
+            mbar_init(&sf_full[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);  // four epilogue warps of each CTA
@@ -1051,6 +1059,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         return jb;
     };
     const uint32_t full0 = mapa_shared(smem_u32(full), 0);
+    const uint32_t sf_full0 = mapa_shared(smem_u32(sf_full), 0);
 
     // ------------------------------------------------------------ GEMM role
     if (warp == 0) {
@@ -1093,9 +1102,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 const int64_t rel0 = static_cast<int64_t>(jb.m0) * kBM - s_pad[jb.e];
                 const int rows0 = a_rows_to_load(cnt_e, rel0), rows1 = a_rows_to_load(cnt_e, rel0 + kBM);
                 const int my_rows = rank ? rows1 : rows0;
-                const uint32_t tx = 2u * (128 * kBKBytes + (MX ? kSfbBytes : 0)) +
-                                    static_cast<uint32_t>((rows0 + rows1) * kBKBytes) +
-                                    (MX ? ((rows0 ? kSfaBytes : 0) + (rows1 ? kSfaBytes : 0)) : 0u);
+                const uint32_t tx = 2u * 128 * kBKBytes + static_cast<uint32_t>((rows0 + rows1) * kBKBytes);
+                const uint32_t tx_sf = 2u * kSfbBytes + (rows0 ? kSfaBytes : 0) + (rows1 ? kSfaBytes : 0);
                 if (my_rows > 0 && (jb.f1 ? !(a.prologue || spin_ge(&ready[m], 2, a, abort_flag))
                                           : !spin_ge(&h_done[m], 4 * a.NT1, a, abort_flag)))
                     break;
@@ -1115,20 +1123,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
                     uint8_t *dA = sT + stage * kFPStage;
                     const int x = ks * kE;
                     const uint32_t fb = full0 + stage * 8;
+                    if constexpr (MX) {
+                        // the scales first, on their own barrier (see k_moe_fused)
+                        const uint32_t sfb = sf_full0 + stage * 8;
+                        uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
+                        if (rank == 0) mbar_arrive_expect_tx(&sf_full[stage], tx_sf);
+                        if (my_rows > 0) tma_load_2d_pair(dS, samap, sfb, 0, sf_tile(x, ya, arows));
+                        if (jb.f1) {
+                            tma_load_2d_pair(dS + kSfaBytes, &pm.s_g, sfb, 0, sf_tile(x, yb_tile, a.EF));
+                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_u, sfb, 0, sf_tile(x, yb_tile, a.EF));
+                        } else {
+                            tma_load_2d_pair(dS + kSfaBytes, &pm.s_dn, sfb, 0, sf_tile(x, yb_tile, a.Ed));
+                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_dn, sfb, 0, sf_tile(x, yb_tile + 128, a.Ed));
+                        }
+                    }
                     if (rank == 0) mbar_arrive_expect_tx(&full[stage], tx);
                     if (my_rows > 0) tma_load_2d_pair(dA, amap, fb, x, ya);
                     tma_load_2d_pair(dA + kAStage, bmap, fb, x, yb);
-                    if constexpr (MX) {
-                        uint8_t *dS = sSF + stage * (kSfaBytes + kSfbBytes);
-                        if (my_rows > 0) tma_load_2d_pair(dS, samap, fb, 0, sf_tile(x, ya, arows));
-                        if (jb.f1) {
-                            tma_load_2d_pair(dS + kSfaBytes, &pm.s_g, fb, 0, sf_tile(x, yb_tile, a.EF));
-                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_u, fb, 0, sf_tile(x, yb_tile, a.EF));
-                        } else {
-                            tma_load_2d_pair(dS + kSfaBytes, &pm.s_dn, fb, 0, sf_tile(x, yb_tile, a.Ed));
-                            tma_load_2d_pair(dS + kSfaBytes + 512, &pm.s_dn, fb, 0, sf_tile(x, yb_tile + 128, a.Ed));
-                        }
-                    }
                     if (++stage == kFPStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -1158,9 +1169,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (!wait_bar(acc_empty, acc_phase ^ 1u, a.status, a.wait_ns, abort_flag)) break;
                 tc_fence_after();
                 for (int ks = 0; ks < kst; ++ks) {
-                    // MXFP8: sf_ready (loads landed, scales copied); BF16: the loads
-                    if (!wait_bar(MX ? &sf_ready[stage] : &full[stage], phase, a.status, a.wait_ns, abort_flag))
-                        goto mma_done;
+                    // both CTAs' operands, and (MXFP8) the stage's scales in TMEM
+                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
+                    if (MX && !wait_bar(&sf_ready[stage], phase, a.status, a.wait_ns, abort_flag)) goto mma_done;
                     tc_fence_after();
                     if (jb.f1 && ks == kst - 1) {
                         // every ring row of the pair's row tiles is now in shared memory
@@ -1195,8 +1206,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     } else if (warp == kScaleWarp) {
         if (MX && lane == 0 && rank == 0) {
             // ---------------------------------- even CTA: scale copier for the pair
-            // once a stage's loads (both CTAs') have landed, copy the stage's
-            // scales into both CTAs' TMEM and commit to sf_ready (see k_moe_fused)
+            // once a stage's scale bytes (both CTAs') have landed, copy them into
+            // both CTAs' TMEM and commit to sf_ready (see k_moe_fused)
             uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
             const uint64_t sfdesc0 = sdesc_sf(smem_u32(sSF));
             for (;;) {
@@ -1211,7 +1222,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
                 if (split_queue_id(tile, T1, a.prev_chunks, &tile) >= 0) continue;
                 const int kst = tile < T1 ? a.k1 : a.k2;
                 for (int ks = 0; ks < kst; ++ks) {
-                    if (!wait_bar(&full[stage], phase, a.status, a.wait_ns, abort_flag)) goto copier_done;
+                    if (!wait_bar(&sf_full[stage], phase, a.status, a.wait_ns, abort_flag)) goto copier_done;
                     tc_fence_after();
                     const uint32_t sfa_col = tmem + kSfCol + stage * 16;
                     const uint32_t sfb_col = sfa_col + 4;
@@ -1313,7 +1324,7 @@ template <bool MX>
 constexpr size_t fused_pair_smem_bytes()
 {
     return 1024 + kFPStages * kFPStage + (MX ? kFPStages * (kSfaBytes + kSfbBytes) : 0) +
-           (3 * kFPStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + 2 * (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+           (4 * kFPStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + 2 * (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
 }
 
 // Launch configuration of the pair kernel: its attributes are set once and its
@@ -1371,7 +1382,7 @@ template <bool MX>
 constexpr size_t fused_smem_bytes()
 {
     return 1024 + kStages * (kAStage + kBStage) + (MX ? kStages * (kSfaBytes + kSfbBytes) : 0) +
-           (3 * kStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
+           (4 * kStages + 2 + 2 * kTQ) * 8 + kTQ * 4 + 16 + (MOK_MAX_EXPERTS + 4) * 4 + kStageBytes;
 }
 
 template <bool MX>
