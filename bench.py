@@ -202,11 +202,11 @@ def _layer_bytes(w):
 # kernel's sources at capture time (comments and blank lines left out): once
 # the kernel's code changes, traffic is null.
 FUSED_TRAFFIC = {
-    # k_moe_fused_pair<1>, T 2048 / E 32 (1/8 of the tokens and experts), 1.897091 GB
-    # read + 0.416860 GB written
-    ("dsv3_mxfp8", 1): {"bytes_small": 1897090816 + 416859904, "scale": 8,
+    # k_moe_fused_pair<1>, T 2048 / E 32 (1/8 of the tokens and experts), 1.880735 GB
+    # read + 0.418315 GB written
+    ("dsv3_mxfp8", 1): {"bytes_small": 1880735488 + 418315008, "scale": 8,
                         "case": "T 2048, 32 experts (1/8 of the tokens and experts)",
-                        "src_sha": "2eeff147b880777e"},
+                        "src_sha": "ced4fd59b12f88d5"},
 }
 FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h", "mok_gather.cuh")
 
