@@ -669,7 +669,7 @@ def main():
                          "unit": "TFLOP/s", "frac": fused_tflops / peak_tc,
                          "traffic": None, "traffic_unit": "DRAM bytes per launch",
                          "kernel": ("k_moe_fused_pair" if plan["cta_pairs"] else "k_moe_fused")
-                                   + " (pull dispatch + FFN1 + FFN2 + combine)",
+                                   + " (pull dispatch + FFN1 + FFN2) + k_combine, one mok_moe_fused call",
                          "algorithmic": "6*S*d*F flops per launch",
                          "peak_source": f"{peak_src} bf16 burst"
                                         + (" x2 (nominal fp8:bf16 ratio)" if mx else ""),

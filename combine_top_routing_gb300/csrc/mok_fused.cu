@@ -27,10 +27,10 @@
 //     waits for ready[m], loads A from the ring, and signals consumed[m] once
 //     its loads have landed; its epilogue writes h and bumps h_done[m] (once
 //     per epilogue warp).  An FFN2 tile waits until all FFN1 N tiles of m are
-//     in h and pushes y rows to their token slots (ystage), then bumps
-//     ffn2_done.
-//   * combine: every CTA waits for ffn2_done == all FFN2 tiles, then combines
-//     a share of the tokens in the fixed j order.
+//     in h and pushes y rows to their token slots (ystage).
+//   * combine: the separate combine kernel, launched right after this one on
+//     the same stream (with seven warps per SM this kernel's threads did the
+//     same reads 1.4x slower than the combine kernel at full occupancy).
 //   * gather prologue (uncapped ring only, chosen by the plan where the split
 //     would give the gather role many SMs): every CTA first pulls whole tokens
 //     (one read per token, written into its k ring rows), a grid-wide arrival
@@ -111,7 +111,6 @@ struct FusedArgs {
     const float *prev_gates;
     uint16_t *prev_out;
     int prev_T, prev_chunks;
-    int skip_combine;         // 1: this call's combine is left to the next call of the chain
     int NT1, NT2, BN2, k1, k2;
     int band1;                // row tiles per band of the FFN1 order (ring-bounded)
     int *counters;            // zeroed: [0] next tile, [1] next minibatch, [2] FFN2 tiles done,
@@ -497,57 +496,6 @@ __device__ __forceinline__ void gather_all_tokens(const FusedArgs &a, int *arriv
     __syncthreads();
 }
 
-// Weighted combine of the fused forward: once every FFN2 tile has pushed its
-// rows (ffn2_done), all threads of all CTAs walk the (token, 16-column) pieces
-// of the output, each with its 2k slot loads in flight before the (ordered)
-// accumulation -- the access pattern of the separate combine kernel.  Every
-// thread of the CTA calls it.
-__device__ __forceinline__ void combine_tokens(const FusedArgs &a, int *ffn2_done, int total_mt,
-                                               volatile int *abort_flag)
-{
-    if (threadIdx.x == 0 && !*abort_flag) spin_ge(ffn2_done, 4 * total_mt * a.NT2, a, abort_flag);
-    __syncthreads();
-    if (*abort_flag) return;
-    const int64_t vec_per_tok = a.d / 16;
-    const int64_t n = static_cast<int64_t>(a.T) * vec_per_tok;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t t = i / vec_per_tok;
-        const int64_t c = (i % vec_per_tok) * 2;
-        uint4 y[MOK_MAX_TOPK][2];
-        float g[MOK_MAX_TOPK];
-#pragma unroll
-        for (int j = 0; j < MOK_MAX_TOPK; ++j) {
-            if (j < a.k) {
-                g[j] = a.gates[t * a.k + j];
-                const uint4 *row = reinterpret_cast<const uint4 *>(a.ystage + (t * a.k + j) * a.d) + c;
-                y[j][0] = row[0];
-                y[j][1] = row[1];
-            }
-        }
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float acc[8];
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-#pragma unroll
-            for (int j = 0; j < MOK_MAX_TOPK; ++j) {
-                if (j < a.k) {
-                    const uint32_t w[4] = {y[j][hh].x, y[j][hh].y, y[j][hh].z, y[j][hh].w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        acc[2 * q] = fmaf(g[j], bf16_bits_to_float(w[q] & 0xFFFFu), acc[2 * q]);
-                        acc[2 * q + 1] = fmaf(g[j], bf16_bits_to_float(w[q] >> 16), acc[2 * q + 1]);
-                    }
-                }
-            }
-            reinterpret_cast<uint4 *>(a.out + t * a.d)[c + hh] =
-                make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                           pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-        }
-    }
-}
-
 template <bool MX>
 __global__ void __launch_bounds__(kFThreads, 1)
     k_moe_fused(const __grid_constant__ FusedMaps pm, const __grid_constant__ FusedArgs a)
@@ -578,7 +526,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int lane = threadIdx.x & 31;
     int *next_tile = a.counters;
     int *next_unit = a.counters + 1;
-    int *ffn2_done = a.counters + 2;
     int *ready = a.counters + 3;
     int *consumed = ready + a.max_mt;
     int *h_done = consumed + a.max_mt;
@@ -868,14 +815,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             if (!released) release();
             acc_phase ^= 1u;
-            // publish this warp's quarter of the tile (h rows for FFN2 tiles, ystage
-            // rows for the combine); each epilogue warp counts for itself, so no
-            // barrier ties the four warps together
-            fence_proxy_async_global();
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence();
-                red_release_gpu_add(f1 ? &h_done[m] : ffn2_done, 1);
+            // an FFN1 tile publishes this warp's quarter of its h rows for the FFN2
+            // tiles (TMA reads them); each epilogue warp counts for itself, so no
+            // barrier ties the four warps together.  FFN2 tiles' ystage rows are read
+            // by the combine kernel that follows this one on the stream.
+            if (f1) {
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence();
+                    red_release_gpu_add(&h_done[m], 1);
+                }
             }
         }
     }
@@ -891,8 +841,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
         tmem_dealloc(tmem, kTmemCols);
     }
 
-    // ----------------------------------------------------- weighted combine
-    if (!a.skip_combine) combine_tokens(a, ffn2_done, total_mt, abort_flag);
 }
 
 // ---------------------------------------------------------------------------
@@ -976,7 +924,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t rank = cluster_ctarank();
     int *next_tile = a.counters;
     int *next_unit = a.counters + 1;
-    int *ffn2_done = a.counters + 2;
     int *ready = a.counters + 3;
     int *consumed = ready + a.max_mt;
     int *h_done = consumed + a.max_mt;
@@ -1292,13 +1239,14 @@ __global__ void __launch_bounds__(kFThreads, 1)
             }
             if (!released) release();
             acc_phase ^= 1u;
-            // publish this warp's quarter of the row tile (a ghost half has none)
-            if (!jb.ghost) {
+            // an FFN1 tile publishes this warp's quarter of its h rows (a ghost half
+            // has none); FFN2 tiles' ystage rows go to the combine kernel that follows
+            if (jb.f1 && !jb.ghost) {
                 fence_proxy_async_global();
                 __syncwarp();
                 if (lane == 0) {
                     __threadfence();
-                    red_release_gpu_add(jb.f1 ? &h_done[m] : ffn2_done, 1);
+                    red_release_gpu_add(&h_done[m], 1);
                 }
             }
         }
@@ -1316,8 +1264,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
         tmem_dealloc_pair(tmem, kTmemCols);
     }
 
-    // ----------------------------------------------------- weighted combine
-    if (!a.skip_combine) combine_tokens(a, ffn2_done, total_mt, abort_flag);
 }
 
 template <bool MX>
@@ -1620,7 +1566,6 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     a.prev_T = io.prev_T;
     // one token per epilogue warp: four per chunk on one CTA, eight on a pair
     a.prev_chunks = io.prev_T > 0 ? (io.prev_T + (pair ? 8 : 4) - 1) / (pair ? 8 : 4) : 0;
-    a.skip_combine = io.skip_combine ? 1 : 0;
     a.status = status;
     a.wait_ns = wait_ns;
     if (pair) {
@@ -1633,8 +1578,11 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     }
     cudaError_t e = cudaMemsetAsync(io.counters, 0, sizeof(int) * fused_counter_ints(dm), st);
     if (e != cudaSuccess) return e;
-    if (pair) return mx ? launch_fused_pair_t<true>(pm, a, grid, st) : launch_fused_pair_t<false>(pm, a, grid, st);
-    return mx ? launch_fused_t<true>(pm, a, st) : launch_fused_t<false>(pm, a, st);
+    e = pair ? (mx ? launch_fused_pair_t<true>(pm, a, grid, st) : launch_fused_pair_t<false>(pm, a, grid, st))
+             : (mx ? launch_fused_t<true>(pm, a, st) : launch_fused_t<false>(pm, a, st));
+    if (e != cudaSuccess || io.skip_combine) return e;
+    // the weighted combine of this call's tokens, by the separate combine kernel
+    return launch_combine(dm, io.ystage, io.gates, io.out, st);
 }
 
 }  // namespace mok

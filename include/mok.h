@@ -235,7 +235,7 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates,
                 void *out, void *stream);
 
 /*
- * A3-A6 as ONE persistent cooperative kernel ([kucoin] §02: the megakernel
+ * A3-A5 as ONE persistent cooperative kernel, then A6 ([kucoin] §02: the megakernel
  * splits the SMs between dispatch/combine/state and the expert FFN, hands
  * minibatches over through on-GPU counters and reuses a fixed-size token ring
  * buffer as soon as the experts are done with it).  From a layout made by
@@ -243,8 +243,9 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates,
  * shape, see mok_fused_plan) start pulling rows (quantised when MXFP8) into a
  * token ring of cfg->ring_bytes (0: no cap; it must hold 256 rows) in
  * minibatches of cfg->minibatch_rows (0: chosen from the shape);
- * the other SMs run the FFN1 and FFN2 tiles as rows arrive; finally every SM
- * combines.  The result is bit-identical to mok_dispatch + mok_expert_ffn +
+ * the other SMs run the FFN1 and FFN2 tiles as rows arrive; the weighted
+ * combine follows as the mok_combine kernel on the same stream (launched by
+ * this call).  The result is bit-identical to mok_dispatch + mok_expert_ffn +
  * mok_combine for every split, minibatch and ring size.  With a gather share
  * of 1 (uncapped ring only) every CTA first pulls whole tokens -- each row
  * read once and quantised once, written into its k slot rows, as
@@ -303,10 +304,10 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
  * overlap the dispatch and expert work of the next).  Call i computes
  * out[i] from x_src[i] exactly as mok_moe_forward (the same bits), with its
  * own workspace ws[i] (fwd_ws bytes).  Call i's weighted combine is not run
- * at the end of its own fused kernel: call i+1's fused kernel runs it, in
- * chunks (one token per epilogue warp) spread among its FFN1 tiles, so the
- * epilogue warps do that HBM-bound work while the same SMs' MMAs run; the
- * last call combines at the end of its kernel as usual.  Everything is
+ * after its own fused kernel: call i+1's fused kernel runs it, in chunks (one
+ * token per epilogue warp) spread among its FFN1 tiles, so the epilogue warps
+ * do that HBM-bound work while the same SMs' MMAs run; the last call's combine
+ * follows its kernel as in mok_moe_forward.  Everything is
  * enqueued on `stream` in call order, so out[i] is complete once call i+1's
  * kernel has run.  Adjacent calls need different workspaces and outputs (two
  * workspaces alternating suffice); otherwise MOK_ERR_INVALID_ARG.
