@@ -194,21 +194,25 @@ def _layer_bytes(w):
     return weights + x + xe + h + ystage + out
 
 
-# DRAM bytes (read + write) per launch of the fused kernel, from one ncu capture
-# (`--metrics dram__bytes_read.sum,dram__bytes_write.sum`) of a case small enough
-# to capture -- the same per-expert shape with the tokens and experts cut by
-# `scale` -- multiplied by `scale` (the weights, activations and staging all
-# grow in proportion), keyed by workload and CTA pairs, with a hash of the
-# kernel's sources at capture time (comments and blank lines left out): once
-# the kernel's code changes, traffic is null.
+# DRAM bytes (read + write) of one mok_moe_fused call -- the dispatch kernel (when
+# the plan gathers first), the fused kernel and the combine kernel -- from one ncu
+# capture (`--metrics dram__bytes_read.sum,dram__bytes_write.sum`) of a case small
+# enough to capture: the same per-expert shape with the tokens and experts cut by
+# `scale`, multiplied by `scale` (the weights, activations and staging all grow in
+# proportion).  Keyed by workload and CTA pairs, with a hash of the kernels'
+# sources at capture time (comments and blank lines left out): once their code
+# changes, traffic is null.
 FUSED_TRAFFIC = {
-    # k_moe_fused_pair<1>, T 2048 / E 32 (1/8 of the tokens and experts), 1.880735 GB
-    # read + 0.418315 GB written
-    ("dsv3_mxfp8", 1): {"bytes_small": 1880735488 + 418315008, "scale": 8,
-                        "case": "T 2048, 32 experts (1/8 of the tokens and experts)",
-                        "src_sha": "ced4fd59b12f88d5"},
+    # T 2048 / E 32 (1/8 of the tokens and experts): k_dispatch_by_token<1> 29.709 MB
+    # read + 60.419 MB written, k_moe_fused_pair<1> 1628.526 + 244.993 MB,
+    # k_combine<8> 234.963 + 17.933 MB
+    ("dsv3_mxfp8", 1): {"bytes_small": 29708800 + 60418816 + 1628526080 + 244992512 + 234963200 + 17933312,
+                        "scale": 8,
+                        "case": "T 2048, 32 experts (1/8 of the tokens and experts); dispatch, fused and "
+                                "combine kernels",
+                        "src_sha": "3372b4c2db070173"},
 }
-FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h", "mok_gather.cuh")
+FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h", "mok_gather.cuh", "mok_move.cu")
 
 
 def _fused_src_sha() -> str:
@@ -531,7 +535,9 @@ def main():
                                            R.ystage, layer.out, layer.ws))
     ffn_ms = timed(lambda: _ffn(layer, R))
     fused_tflops = flops / (fused_ms / 1e3) / 1e12
-    launches_per_step = 8  # router split, router GEMM, top-k, 4 layout passes, fused kernel
+    # router split, router GEMM, top-k, 4 layout passes, the fused kernel and the
+    # combine kernel, and the dispatch kernel when the plan gathers first
+    launches_per_step = 9 + (1 if plan["gather_ctas"] >= plan["ctas"] else 0)
 
     sweep = None
     if args.sweep:
@@ -704,7 +710,7 @@ def main():
         if tr is not None:
             line["roofline"]["traffic"] = tr["bytes"]
             line["roofline"]["traffic_how"] = (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of one "
-                                               f"launch at {tr['captured']}, x{tr['scale']}")
+                                               f"mok_moe_fused call at {tr['captured']}, x{tr['scale']}")
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

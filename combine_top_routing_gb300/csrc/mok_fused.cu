@@ -31,10 +31,12 @@
 //   * combine: the separate combine kernel, launched right after this one on
 //     the same stream (with seven warps per SM this kernel's threads did the
 //     same reads 1.4x slower than the combine kernel at full occupancy).
-//   * gather prologue (uncapped ring only, chosen by the plan where the split
-//     would give the gather role many SMs): every CTA first pulls whole tokens
-//     (one read per token, written into its k ring rows), a grid-wide arrival
-//     count closes the gather, and every CTA then runs the GEMM role.
+//   * gather first (uncapped ring only, chosen by the plan where the split
+//     would give the gather role many SMs): the by-token dispatch kernel pulls
+//     whole tokens into their k ring rows (one read per token) right before
+//     this kernel on the same stream, and every CTA runs the GEMM role from
+//     the start.  (A gather prologue inside this kernel, seven warps per SM,
+//     took 0.30 ms where the dispatch kernel at full occupancy takes 0.24.)
 //   * chained calls (macrobatch pipelining): the previous call's weighted
 //     combine runs in this kernel, its tokens in chunks (one token per
 //     epilogue warp) whose queue ids sit evenly among the FFN1 tiles; the
@@ -52,7 +54,6 @@
 
 #include <mutex>
 
-#include "mok_gather.cuh"
 #include "mok_internal.h"
 #include "mok_ptx.cuh"
 #include "mok_tc.cuh"
@@ -104,7 +105,7 @@ struct FusedArgs {
     uint16_t *saved_a, *saved_b, *saved_h;
     int mb;                   // minibatch rows per hand-off (64, 128, 256)
     int n_gather;             // CTAs that start in the gather role
-    int prologue;             // 1: every CTA gathers tokens first (gather_all_tokens)
+    int prologue;             // 1: the rows are in the ring already (gathered by the dispatch kernel)
     // the previous call of a chain: its weighted combine runs here, in chunks
     // interleaved among this call's FFN1 tiles (prev_chunks = 0: none)
     const uint16_t *prev_ystage;
@@ -471,31 +472,6 @@ __device__ __forceinline__ void combine_token_warp(const uint16_t *ystage, const
     }
 }
 
-// Gather prologue (a gather share of 1, uncapped ring): every warp of every
-// CTA pulls whole tokens -- each token's row read once, quantised once
-// (MXFP8), written into its k slot rows of the ring -- then the grid waits
-// until every CTA has arrived (bounded; all CTAs are resident), so every FFN1
-// tile finds its rows in place.  Every thread of the CTA calls it.
-template <bool MX>
-__device__ __forceinline__ void gather_all_tokens(const FusedArgs &a, int *arrived, volatile int *abort_flag,
-                                                  int warp, int lane)
-{
-    const int nw = kFThreads / 32;
-    for (int64_t t = static_cast<int64_t>(blockIdx.x) * nw + warp; t < a.T;
-         t += static_cast<int64_t>(gridDim.x) * nw)
-        dispatch_token<MX>(a.src, t, a.d, a.k, a.ids, a.slot_pos, a.offsets, a.pad_offsets, a.ring,
-                           a.ring_scales, a.ring_rows, lane);
-    // the rows are read by TMA (async proxy) after the barrier
-    fence_proxy_async_global();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        red_release_gpu_add(arrived, 1);
-        spin_ge(arrived, static_cast<int>(gridDim.x), a, abort_flag);
-    }
-    __syncthreads();
-}
-
 template <bool MX>
 __global__ void __launch_bounds__(kFThreads, 1)
     k_moe_fused(const __grid_constant__ FusedMaps pm, const __grid_constant__ FusedArgs a)
@@ -570,9 +546,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     constexpr int kE = MX ? 128 : 64;
 
     // ---------------------------------------------------------- gather role
-    if (a.prologue)
-        gather_all_tokens<MX>(a, next_unit, abort_flag, warp, lane);
-    else if (static_cast<int>(blockIdx.x) < a.n_gather)
+    if (!a.prologue && static_cast<int>(blockIdx.x) < a.n_gather)
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
                         kFThreads / 32, smem, kStages * (kAStage + kBStage));
 
@@ -980,9 +954,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const int bandp = a.band1 >= (1 << 29) ? (1 << 30) : (a.band1 / 2 > 0 ? a.band1 / 2 : 1);
 
     // ---------------------------------------------------------- gather role
-    if (a.prologue) {
-        gather_all_tokens<MX>(a, next_unit, abort_flag, warp, lane);
-    } else if (static_cast<int>(blockIdx.x) < a.n_gather) {
+    if (!a.prologue && static_cast<int>(blockIdx.x) < a.n_gather) {
         gather_rows<MX>(a, s_pad, pad_end, s_unit, abort_flag, next_unit, ready, consumed, warp, lane,
                         kFThreads / 32, smem, kFPStages * kFPStage);
         cluster_sync_all();  // the pair joins the GEMM role together
@@ -1578,6 +1550,13 @@ cudaError_t launch_fused(const Dims &dm, const mok_config *cfg, const Sources &s
     }
     cudaError_t e = cudaMemsetAsync(io.counters, 0, sizeof(int) * fused_counter_ints(dm), st);
     if (e != cudaSuccess) return e;
+    if (a.prologue) {
+        // gather first: every token's row read once, quantised once, placed into
+        // its k rows of the (uncapped) ring, by the dispatch kernel
+        e = launch_dispatch_by_token(dm, src, io.ids, io.slot_pos, io.offsets, io.pad_offsets, io.ring,
+                                     io.ring_scales, st);
+        if (e != cudaSuccess) return e;
+    }
     e = pair ? (mx ? launch_fused_pair_t<true>(pm, a, grid, st) : launch_fused_pair_t<false>(pm, a, grid, st))
              : (mx ? launch_fused_t<true>(pm, a, st) : launch_fused_t<false>(pm, a, st));
     if (e != cudaSuccess || io.skip_combine) return e;

@@ -247,10 +247,9 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates,
  * combine follows as the mok_combine kernel on the same stream (launched by
  * this call).  The result is bit-identical to mok_dispatch + mok_expert_ffn +
  * mok_combine for every split, minibatch and ring size.  With a gather share
- * of 1 (uncapped ring only) every CTA first pulls whole tokens -- each row
- * read once and quantised once, written into its k slot rows, as
- * mok_dispatch_by_token -- and the GEMM role starts on every CTA once all of
- * them have arrived.  ids/gates/counts/offsets/pad_offsets/slot_pos/row_tok/
+ * of 1 (uncapped ring only) the call first runs the mok_dispatch_by_token
+ * kernel -- each row read once and quantised once, written into its k slot
+ * rows -- and the fused kernel then runs the GEMM role on every CTA.  ids/gates/counts/offsets/pad_offsets/slot_pos/row_tok/
  * row_j as produced by mok_route_layout; ystage: device BF16 [T,k,d]; out:
  * device BF16 [T,d]; ws: fwd_ws bytes.  A ring below 256 rows, or a gather
  * share of 1 with a capped ring, returns MOK_ERR_INVALID_ARG; a bounded device
