@@ -1418,15 +1418,15 @@ int fused_ctas(const Dims &dm, const mok_config *cfg, int sms)
 }
 
 // ctas: the CTAs of the launch (for the pair kernel, its grid)
-// A gather share of 1 (every CTA pulls whole tokens first, then every CTA runs
-// the GEMM role) when the config asks for it, or automatically when the ring
-// is uncapped and the split rule would give the gather role at least 1/8 of
-// the CTAs: the split keeps that share away from the GEMM role for as long as
-// it takes a fraction of the SMs to pull the rows (one read per slot), the
-// prologue takes every SM for the time the whole GPU needs to pull them (one
-// read per token).  Measured on GB300 (DeepSeek-V3 MXFP8 shape, 38 of 152 CTAs
-// by the split rule): 6.43 -> 6.09 ms; Mixtral shape (10 of 152): 3.66 vs
-// 3.68 ms, so the split stays there.
+// A gather share of 1 (every token pulled first, by the dispatch kernel, then
+// every CTA of the fused kernel runs the GEMM role) when the config asks for
+// it, or automatically when the ring is uncapped and the split rule would give
+// the gather role at least 1/8 of the CTAs: the split keeps that share away
+// from the GEMM role for as long as it takes a fraction of the SMs to pull the
+// rows (one read per slot); gathering first takes every SM for the time the
+// whole GPU needs to pull them (one read per token).  Measured on GB300
+// (DeepSeek-V3 MXFP8 shape, 38 of 152 CTAs by the split rule): 6.43 -> 6.09
+// ms; Mixtral shape (10 of 152): 3.66 vs 3.68 ms, so the split stays there.
 bool fused_gathers_first(const Dims &dm, const mok_config *cfg, int ctas)
 {
     if (fused_ring_rows(dm, cfg->ring_bytes) < dm.rows_pad) return false;

@@ -4,7 +4,8 @@
 // own expert order, with MXFP8 quantisation fused in): one warp reads token
 // t's row from its source once, quantises it once (MXFP8) and writes it into
 // each of the token's k slot rows of the expert-ordered buffer.  Shared by the
-// by-token dispatch kernel and the fused forward's gather prologue.
+// by-token dispatch kernel (which the fused forward also runs first when its
+// plan gathers every token before the GEMM role).
 #pragma once
 
 #include "mok_internal.h"
