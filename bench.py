@@ -420,6 +420,41 @@ def _layer_line(w, layer, stream, steps, flush, peaks):
                 "hbm_frac": _layer_bytes(w) / (ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6800.0)}
 
 
+def _skewed_layer(w, stream, flush, peaks, world):
+    """The Zipf-skewed, 64-source, 256 MB-ring layer: its forward with the
+    automatic plan, and the gather share x minibatch sweep of the split gather,
+    each point's output compared bit for bit with the automatic plan's."""
+    import torch
+
+    from combine_top_routing_gb300 import inputs as I
+    from combine_top_routing_gb300 import mok
+    from combine_top_routing_gb300.layer import MoELayer
+    rank = int(os.environ.get("RANK", "0"))
+    inp = I.make_inputs(I.scaled(w, seed=w.seed + 1000 * rank), device="cuda")
+    layer = MoELayer(w, inp)
+    ms, lr = _layer_line(w, layer, stream, 10, flush, peaks)
+    ms = reduce_max(ms, "cuda")
+    plan = mok.fused_plan(layer.cfg)
+    ref = layer.out.clone()
+    sweep = []
+    for frac in (0.125, 0.25, 1 / 3):
+        for mb in (64, 128, 256):
+            layer.cfg.c.gather_sm_fraction = frac
+            layer.cfg.c.minibatch_rows = mb
+            layer.forward()
+            torch.cuda.synchronize()
+            same = bool(torch.equal(layer.out.view(torch.int16), ref.view(torch.int16)))
+            sms = time_flushed(layer.forward, 5, stream, flush)
+            if layer.status() != 0:
+                raise RuntimeError("device status in the skewed sweep: " + mok.status_string(layer.status()))
+            sweep.append({"gather_sm_fraction": round(frac, 4), "minibatch_rows": mb, "ms_per_step": sms,
+                          "bit_identical_to_automatic_plan": same})
+    out = {"forward_ms": ms, "value": job_throughput(w.T, world, ms), "unit": "tokens/s",
+           "layer_roofline": lr, "fused_plan": plan, "sweep": sweep}
+    del layer, inp, ref
+    return out
+
+
 def _tc_peak(w, peaks):
     """Measured dense tensor peak for the layer's GEMM dtype: the BF16 burst
     figure, x2 (the nominal FP8:BF16 ratio) for MXFP8."""
@@ -633,11 +668,15 @@ def main():
                                         NOMINAL["mxfp8_tflops" if wf.dtype == "mxfp8" else "bf16_tflops"],
               "steps": fb_steps, "l2": "flushed between timed steps"}
 
-    # ---------------- skewed layer's achieved load, secondary BF16 layer
+    # ---------------- skewed layer (load, forward, the gather-share x minibatch
+    # sweep with its outputs compared bit for bit), secondary BF16 layer
     skew = secondary = None
     if not args.no_secondary:
         skew = _expert_load(I.WORKLOADS["dsv3_skew_ep"])
         torch.cuda.empty_cache()
+        if w.name != "dsv3_skew_ep":
+            skew.update(_skewed_layer(I.WORKLOADS["dsv3_skew_ep"], stream, flush, peaks, world))
+            torch.cuda.empty_cache()
         if w.name != SECONDARY:
             w2 = I.WORKLOADS[SECONDARY]
             inp2 = I.make_inputs(I.scaled(w2, seed=w2.seed + 1000 * rank), device="cuda")

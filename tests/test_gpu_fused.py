@@ -127,10 +127,10 @@ def test_full_size_skewed_layer_bit_identical_across_repeats_splits_minibatches(
 
 
 @pytest.mark.parametrize("name", ["mx_skew_sources", "bf16"])
-def test_gather_prologue_equals_split_gather_bit_exact(name):
-    """A gather share of 1: every CTA pulls whole tokens first (one read per
-    token), then every CTA runs the GEMM role -- the same bits as the split
-    gather, on one CTA per tile and on CTA pairs."""
+def test_gather_first_equals_split_gather_bit_exact(name):
+    """A gather share of 1: the dispatch kernel pulls whole tokens first (one
+    read per token), then every CTA of the fused kernel runs the GEMM role --
+    the same bits as the split gather, on one CTA per tile and on CTA pairs."""
     w = CASES[name]
     layer, _ = make_layer(w)
     ref = layer.forward().clone()
@@ -145,7 +145,7 @@ def test_gather_prologue_equals_split_gather_bit_exact(name):
         assert torch.equal(out, ref), pairs
 
 
-def test_gather_prologue_needs_an_uncapped_ring():
+def test_gather_first_needs_an_uncapped_ring():
     w = CASES["bf16"]
     layer, _ = make_layer(w, gather_sm_fraction=1.0)
     layer.cfg.c.ring_bytes = 512 * w.d * 2
