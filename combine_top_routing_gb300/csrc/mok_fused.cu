@@ -114,7 +114,7 @@ struct FusedArgs {
     int prev_T, prev_chunks;
     int NT1, NT2, BN2, k1, k2;
     int band1;                // row tiles per band of the FFN1 order (ring-bounded)
-    int *counters;            // zeroed: [0] next tile, [1] next minibatch, [2] FFN2 tiles done,
+    int *counters;            // zeroed: [0] next tile, [1] next minibatch, [2] unused,
                               // then ready[mt], consumed[mt], h_done[mt]
     int max_mt;
     uint32_t *status;
