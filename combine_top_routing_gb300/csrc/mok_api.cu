@@ -25,7 +25,10 @@ int check_config(const mok_config *cfg, Dims *dm)
 {
     if (!cfg) return MOK_ERR_INVALID_ARG;
     const int T = cfg->T, d = cfg->d_model, E = cfg->n_experts, k = cfg->top_k, F = cfg->d_ff;
-    if (T < 1 || d < 1 || E < 1 || k < 1 || F < 1) return MOK_ERR_INVALID_ARG;
+    // T = 0 is an empty batch: every call is then a no-op apart from the
+    // per-expert outputs it defines (see empty_layout and mok_moe_backward)
+    if (T < 0 || d < 1 || E < 1 || k < 1 || F < 1) return MOK_ERR_INVALID_ARG;
+    if (T == 0 && cfg->n_sources != 1) return MOK_ERR_INVALID_ARG;
     if (cfg->router != MOK_ROUTER_SOFTMAX && cfg->router != MOK_ROUTER_SIGMOID) return MOK_ERR_INVALID_ARG;
     if (cfg->dtype != MOK_BF16 && cfg->dtype != MOK_MXFP8) return MOK_ERR_INVALID_ARG;
     if (cfg->n_sources < 1 || cfg->n_sources > MOK_MAX_SOURCES) return MOK_ERR_INVALID_ARG;
@@ -226,6 +229,16 @@ static uint64_t wait_ns(const mok_config *cfg)
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA; }
 
+// The layout of an empty batch: no expert has a row, every offset is 0.
+int empty_layout(const Dims &dm, int32_t *counts, int32_t *offsets, int32_t *pad_offsets, cudaStream_t st)
+{
+    if (!counts || !offsets || !pad_offsets) return MOK_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(counts, 0, static_cast<size_t>(dm.E) * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, static_cast<size_t>(dm.E + 1) * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(pad_offsets, 0, static_cast<size_t>(dm.E + 1) * 4, st);
+    return e == cudaSuccess ? MOK_OK : MOK_ERR_CUDA;
+}
+
 template <typename T>
 static T *at(void *base, size_t off)
 {
@@ -320,6 +333,7 @@ int mok_route_layout(const mok_config *cfg, const void *const *x_src, const floa
     Dims dm;
     int rc = check_config(cfg, &dm);
     if (rc != MOK_OK) return rc;
+    if (dm.T == 0) return empty_layout(dm, counts, offsets, pad_offsets, static_cast<cudaStream_t>(stream));
     if (!W_r || !ids || !gates || !counts || !offsets || !pad_offsets || !slot_pos || !row_tok ||
         !row_j || !ws)
         return MOK_ERR_INVALID_ARG;
@@ -349,7 +363,7 @@ int mok_dispatch(const mok_config *cfg, const void *const *x_src, const int32_t 
 {
     Dims dm;
     int rc = check_config(cfg, &dm);
-    if (rc != MOK_OK) return rc;
+    if (rc != MOK_OK || dm.T == 0) return rc;
     if (!ids || !offsets || !pad_offsets || !row_tok || !row_j || !xe) return MOK_ERR_INVALID_ARG;
     if (dm.dtype == MOK_MXFP8 && !xe_scales) return MOK_ERR_INVALID_ARG;
     Sources src;
@@ -364,7 +378,7 @@ int mok_dispatch_by_token(const mok_config *cfg, const void *const *x_src, const
 {
     Dims dm;
     int rc = check_config(cfg, &dm);
-    if (rc != MOK_OK) return rc;
+    if (rc != MOK_OK || dm.T == 0) return rc;
     if (!ids || !slot_pos || !offsets || !pad_offsets || !xe) return MOK_ERR_INVALID_ARG;
     if (dm.dtype == MOK_MXFP8 && !xe_scales) return MOK_ERR_INVALID_ARG;
     Sources src;
@@ -380,7 +394,7 @@ int mok_expert_ffn(const mok_config *cfg, const void *xe, const uint32_t *xe_sca
 {
     Dims dm;
     int rc = check_config(cfg, &dm);
-    if (rc != MOK_OK) return rc;
+    if (rc != MOK_OK || dm.T == 0) return rc;
     if (!xe || !w || !offsets || !pad_offsets || !row_tok || !row_j || !ystage || !ws)
         return MOK_ERR_INVALID_ARG;
     const bool mx = dm.dtype == MOK_MXFP8;
@@ -409,7 +423,7 @@ int mok_combine(const mok_config *cfg, const void *ystage, const float *gates, v
 {
     Dims dm;
     const int rc = check_config(cfg, &dm);
-    if (rc != MOK_OK) return rc;
+    if (rc != MOK_OK || dm.T == 0) return rc;
     if (!ystage || !gates || !out) return MOK_ERR_INVALID_ARG;
     return cuda_status(launch_combine(dm, static_cast<const uint16_t *>(ystage), gates,
                                       static_cast<uint16_t *>(out), static_cast<cudaStream_t>(stream)));
@@ -430,7 +444,7 @@ int check_forward_args(const mok_config *cfg, Dims *dm, const float *W_r, const 
 {
     int rc = check_config(cfg, dm);
     if (rc != MOK_OK) return rc;
-    if (!W_r || !w || !out || !ws) return MOK_ERR_INVALID_ARG;
+    if (!W_r || !w || (!out && dm->T > 0) || !ws) return MOK_ERR_INVALID_ARG;
     const bool mx = dm->dtype == MOK_MXFP8;
     if (mx && (!w->q_gate || !w->q_up || !w->q_down || !w->s_gate || !w->s_up || !w->s_down))
         return MOK_ERR_INVALID_ARG;
@@ -460,6 +474,10 @@ int forward_impl(const mok_config *cfg, const Dims &dm, const Sources &src, cons
     uint32_t *status = at<uint32_t>(ws, fw.status);
     cudaError_t e = cudaMemsetAsync(status, 0, 4, st);
     if (e != cudaSuccess) return MOK_ERR_CUDA;
+    if (gates_out) *gates_out = o.gates;
+    if (ystage_out) *ystage_out = ystage;
+    // an empty batch: the saved routing says that no expert has a row
+    if (dm.T == 0) return saved_ctx ? empty_layout(dm, o.counts, o.offsets, o.pad_offsets, st) : MOK_OK;
     int rc = route_layout_impl(cfg, dm, src, W_r, bias, o, ws, st);
     if (rc != MOK_OK) return rc;
     // dispatch, expert FFN and combine: one persistent kernel (role split,
@@ -488,8 +506,6 @@ int forward_impl(const mok_config *cfg, const Dims &dm, const Sources &src, cons
     io.prev_out = prev.out;
     io.prev_T = prev.T;
     io.skip_combine = skip_combine;
-    if (gates_out) *gates_out = o.gates;
-    if (ystage_out) *ystage_out = ystage;
     return cuda_status(launch_fused(dm, cfg, src, io, w, status, wait_ns(cfg), st));
 }
 
@@ -502,8 +518,8 @@ int mok_moe_forward(const mok_config *cfg, const void *const *x_src, const float
     Dims dm;
     int rc = check_forward_args(cfg, &dm, W_r, w, out, ws);
     if (rc != MOK_OK) return rc;
-    Sources src;
-    if ((rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
+    Sources src = {};
+    if (dm.T > 0 && (rc = make_sources(cfg, dm, x_src, &src)) != MOK_OK) return rc;
     return forward_impl(cfg, dm, src, W_r, bias, w, out, saved_ctx, ws, static_cast<cudaStream_t>(stream),
                         ChainPrev(), false, nullptr, nullptr);
 }
@@ -518,16 +534,16 @@ int mok_moe_forward_chain(const mok_config *cfg, int n, const void *const *const
         const int rc = check_forward_args(cfg, &dm, W_r, w, out[i], ws[i]);
         if (rc != MOK_OK) return rc;
         Sources src;
-        const int rs = make_sources(cfg, dm, x_src[i], &src);
+        const int rs = dm.T > 0 ? make_sources(cfg, dm, x_src[i], &src) : MOK_OK;
         if (rs != MOK_OK) return rs;
         // call i's combine runs in call i + 1's kernel from call i's workspace
-        if (i > 0 && (ws[i] == ws[i - 1] || out[i] == out[i - 1])) return MOK_ERR_INVALID_ARG;
+        if (i > 0 && (ws[i] == ws[i - 1] || (dm.T > 0 && out[i] == out[i - 1]))) return MOK_ERR_INVALID_ARG;
     }
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     ChainPrev prev;
     for (int i = 0; i < n; ++i) {
-        Sources src;
-        make_sources(cfg, dm, x_src[i], &src);
+        Sources src = {};
+        if (dm.T > 0) make_sources(cfg, dm, x_src[i], &src);
         const float *gates = nullptr;
         uint16_t *ystage = nullptr;
         const int rc = forward_impl(cfg, dm, src, W_r, bias, w, out[i], nullptr, ws[i], st, prev, i + 1 < n,
@@ -567,6 +583,13 @@ int mok_moe_fused(const mok_config *cfg, const void *const *x_src, const mok_wei
     Dims dm;
     int rc = check_config(cfg, &dm);
     if (rc != MOK_OK) return rc;
+    if (dm.T == 0) {
+        // an empty batch: nothing to move or compute; the status word reads OK
+        if (!ws) return MOK_ERR_INVALID_ARG;
+        FwdWs fw;
+        fwd_ws_layout(dm, &fw);
+        return cuda_status(cudaMemsetAsync(at<uint32_t>(ws, fw.status), 0, 4, static_cast<cudaStream_t>(stream)));
+    }
     if (!w || !ids || !gates || !counts || !offsets || !pad_offsets || !slot_pos || !row_tok ||
         !row_j || !ystage || !out || !ws)
         return MOK_ERR_INVALID_ARG;
@@ -611,6 +634,19 @@ int mok_moe_backward(const mok_config *cfg, const void *const *x_src, const floa
     Dims dm;
     int rc = check_config(cfg, &dm);
     if (rc != MOK_OK) return rc;
+    if (dm.T == 0) {
+        // an empty batch: every weight gradient is an empty sum, so zero
+        if (!dw || !dw->d_gate || !dw->d_up || !dw->d_down || !dW_r || !ws) return MOK_ERR_INVALID_ARG;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        BwdWs bw;
+        bwd_ws_layout(dm, &bw);
+        const size_t wbytes = static_cast<size_t>(dm.E) * dm.F * dm.d * 2;
+        cudaError_t e = cudaMemsetAsync(at<uint32_t>(ws, bw.status), 0, 4, st);
+        for (void *g : {dw->d_gate, dw->d_up, dw->d_down})
+            if (e == cudaSuccess) e = cudaMemsetAsync(g, 0, wbytes, st);
+        if (e == cudaSuccess) e = cudaMemsetAsync(dW_r, 0, static_cast<size_t>(dm.E) * dm.d * 4, st);
+        return cuda_status(e);
+    }
     if (!W_r || !saved_ctx || !dY || !w || !dX || !dw || !dw->d_gate || !dw->d_up || !dw->d_down ||
         !dgates || !dW_r || !ws)
         return MOK_ERR_INVALID_ARG;

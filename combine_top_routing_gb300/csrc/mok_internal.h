@@ -72,6 +72,8 @@ struct BwdWs {
 };
 
 int check_config(const mok_config *cfg, Dims *dm);
+// counts = 0, offsets = pad_offsets = 0 on st (the layout of an empty batch)
+int empty_layout(const Dims &dm, int32_t *counts, int32_t *offsets, int32_t *pad_offsets, cudaStream_t st);
 void bwd_ws_layout(const Dims &dm, BwdWs *w);
 void fwd_ws_layout(const Dims &dm, FwdWs *w);
 void ctx_layout(const Dims &dm, mok_ctx_layout *c);

@@ -59,6 +59,7 @@ extern "C" int mok_layout_static(const mok_config *cfg, const int32_t *ids, int3
     Dims dm;
     const int rc = check_config(cfg, &dm);
     if (rc != MOK_OK) return rc;
+    if (dm.T == 0) return empty_layout(dm, counts, offsets, pad_offsets, static_cast<cudaStream_t>(stream));
     if (!ids || !counts || !offsets || !pad_offsets || !slot_pos || !row_tok || !row_j)
         return MOK_ERR_INVALID_ARG;
     const int64_t words = 2 * static_cast<int64_t>(dm.nchunks) * dm.E;

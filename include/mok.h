@@ -70,11 +70,20 @@ enum { MOK_PAIRS_AUTO = 0, MOK_PAIRS_ON = 1, MOK_PAIRS_OFF = 2 };
 #define MOK_MAX_TOPK 8
 
 /*
- * Layer configuration.  Supported: 1 <= T, 1 <= E <= MOK_MAX_EXPERTS,
+ * Layer configuration.  Supported: 0 <= T, 1 <= E <= MOK_MAX_EXPERTS,
  * 1 <= k <= min(E, MOK_MAX_TOPK), d and F multiples of 128 (the MXFP8 block
  * of 32 and the 128-wide tiles), S + 128 E < 2^31, and for n_sources > 1 every
  * source_rows[s] a multiple of 128 (one router row tile never spans two
  * sources).  Anything else returns MOK_ERR_UNSUPPORTED.
+ *
+ * T = 0 is an empty batch (n_sources must be 1): every call returns MOK_OK
+ * and launches no kernel, and pointers to arrays with T (or T*k) rows may be
+ * NULL.  What is still written follows from the definitions with no tokens:
+ * mok_route_layout, mok_layout_static and a training mok_moe_forward (into
+ * its saved context) set counts to 0 and offsets, pad_offsets to 0;
+ * mok_moe_backward sets the three weight gradients and dW_r to 0 (empty
+ * sums); the forward, fused and backward calls clear their workspace's status
+ * word.  Nothing is enqueued but those memsets.
  */
 typedef struct {
     int T, d_model, n_experts, top_k, d_ff;

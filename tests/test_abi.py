@@ -46,8 +46,19 @@ def test_workspace_size_valid_and_monotone():
     assert mok.max_padded_rows(_cfg()) == 512 + 8 * 128
 
 
+def test_empty_batch_is_a_valid_config():
+    """T = 0 (no tokens) is accepted: the workspaces still hold the per-expert
+    layout and the status word; T = 0 spread over several sources is not a
+    layout of sources (each holds at least one 128-row piece)."""
+    assert all(s > 0 for s in mok.workspace_size(_cfg(T=0)))
+    assert mok.max_padded_rows(_cfg(T=0)) == 8 * 128
+    with pytest.raises(mok.MokError) as ei:
+        mok.workspace_size(_cfg(T=0, n_sources=2, source_rows=[128, 128]))
+    assert ei.value.code == mok.MOK_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("kw,code", [
-    (dict(T=0), mok.MOK_ERR_INVALID_ARG),
+    (dict(T=-1), mok.MOK_ERR_INVALID_ARG),
     (dict(top_k=9, n_experts=16), mok.MOK_ERR_UNSUPPORTED),
     (dict(top_k=4, n_experts=2), mok.MOK_ERR_UNSUPPORTED),
     (dict(n_experts=2048), mok.MOK_ERR_UNSUPPORTED),
