@@ -48,6 +48,10 @@ SMALL = {
                             router="softmax", seed=48),
     "mx_one_expert": I.Workload("mx_one_expert", T=384, d=256, E=1, k=1, F=256, dtype="mxfp8",
                                 router="sigmoid", seed=49),
+    # the largest expert count and top-k (1024, 8): most experts have a few
+    # rows or none, every weight gradient of an expert without rows is zero
+    "mx_max_experts": I.Workload("mx_max_experts", T=384, d=256, E=1024, k=8, F=256,
+                                 dtype="mxfp8", router="sigmoid", seed=40),
 }
 
 

@@ -34,6 +34,13 @@ SMALL = {
                                      dtype="bf16", router="softmax", seed=36),
     "mx_top1": I.Workload("mx_top1", T=257, d=256, E=4, k=1, F=128, dtype="mxfp8",
                           router="sigmoid", seed=37),
+    # the largest expert count and top-k the library takes (1024, 8): about
+    # three rows per expert, so nearly every row tile is a ragged tail, and the
+    # kernels' per-expert tables are full (BF16 on CTA pairs, MXFP8 on single CTAs)
+    "bf16_max_experts": I.Workload("bf16_max_experts", T=384, d=256, E=1024, k=8, F=256,
+                                   dtype="bf16", router="softmax", seed=38),
+    "mx_max_experts": I.Workload("mx_max_experts", T=384, d=256, E=1024, k=8, F=256,
+                                 dtype="mxfp8", router="sigmoid", seed=39),
 }
 
 
