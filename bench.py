@@ -210,12 +210,12 @@ FUSED_TRAFFIC = {
                         "scale": 8,
                         "case": "T 2048, 32 experts (1/8 of the tokens and experts); dispatch, fused and "
                                 "combine kernels",
-                        "src_sha": "ad5aa6dd350f6181"},
+                        "src_sha": "ca1272697b0c8c80"},
     # full size (a few GB on the device): k_moe_fused_pair<0> 4407.417 MB read + 764.237 MB
     # written, k_combine<2> 134.295 + 30.839 MB (the split gather is inside the fused kernel)
     ("mixtral_bf16", 1): {"bytes_small": 4407416576 + 764236800 + 134294784 + 30838528, "scale": 1,
                           "case": "full size; fused and combine kernels",
-                          "src_sha": "ad5aa6dd350f6181"},
+                          "src_sha": "ca1272697b0c8c80"},
 }
 FUSED_SOURCES = ("mok_fused.cu", "mok_tc.cuh", "mok_ptx.cuh", "mok_internal.h", "mok_gather.cuh", "mok_move.cu")
 

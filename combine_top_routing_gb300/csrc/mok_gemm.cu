@@ -359,7 +359,9 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
             // What this thread's row needs from global memory is looked up while
             // the tile's MMAs run, not after the accumulator is full: the expert's
             // counts and offsets, FFN2's token slot, DGRAD2's first 32 columns of
-            // the saved a, b (the rest prefetched into L2).
+            // the saved a, b.  (Prefetching the rest of the row into L2 here read
+            // it from DRAM twice -- the K loop's weights evict it before the
+            // epilogue -- and bought no time.)
             const int e = tl.group;
             const int row_in_e = tl.m_blk * kBM + r;
             bool valid = true;
@@ -400,11 +402,6 @@ __global__ void __launch_bounds__(GemmShape<MODE>::kThreads, 1)
                     for (int q = 0; q < 4; ++q) {
                         na[q] = __ldg(pa + q);
                         nb[q] = __ldg(pb + q);
-                    }
-                    // the rest of the row's columns: 64-byte pieces, 128-byte lines
-                    for (int c = 64; c < 2 * (c_end - c_begin); c += 128) {
-                        prefetch_l2(reinterpret_cast<const uint8_t *>(a.in_a + grow * a.F + f0) + c);
-                        prefetch_l2(reinterpret_cast<const uint8_t *>(a.in_b + grow * a.F + f0) + c);
                     }
                 }
             }

@@ -184,12 +184,6 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr
 
 // ---------------------------------------------------------------- TMA
 
-// Brings the 128-byte line holding p into L2 (no register result).
-__device__ __forceinline__ void prefetch_l2(const void *p)
-{
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
