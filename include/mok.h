@@ -20,6 +20,9 @@
  *     "host" are read before the call returns.  The library never allocates,
  *     never frees and never synchronises the host inside a call: work is
  *     enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     So the layer calls can be captured into a CUDA graph and replayed,
+ *     once each kind of call has run outside the capture (the first call
+ *     of a kind sets its kernels' launch attributes, once per process).
  *   - Return value: MOK_OK, or a host-detectable error code (nothing was
  *     enqueued).  Errors found on the device (a bounded wait that ran out)
  *     land in the status word of the workspace; read them with
