@@ -718,8 +718,12 @@ def main():
             "roofline": {"bound": "tensor", "achieved": fused_tflops, "peak": peak_tc,
                          "unit": "TFLOP/s", "frac": fused_tflops / peak_tc,
                          "traffic": None, "traffic_unit": "DRAM bytes per launch",
-                         "kernel": ("k_moe_fused_pair" if plan["cta_pairs"] else "k_moe_fused")
-                                   + " (pull dispatch + FFN1 + FFN2) + k_combine, one mok_moe_fused call",
+                         "kernel": (("k_dispatch_by_token (pull dispatch) + " if plan["gather_ctas"] >= plan["ctas"]
+                                     else "")
+                                    + ("k_moe_fused_pair" if plan["cta_pairs"] else "k_moe_fused")
+                                    + (" (FFN1 + FFN2)" if plan["gather_ctas"] >= plan["ctas"]
+                                       else " (pull dispatch by its gather CTAs + FFN1 + FFN2)")
+                                    + " + k_combine, one mok_moe_fused call"),
                          "algorithmic": "6*S*d*F flops per launch",
                          "peak_source": f"{peak_src} bf16 burst"
                                         + (" x2 (nominal fp8:bf16 ratio)" if mx else ""),
