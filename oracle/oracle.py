@@ -509,7 +509,10 @@ def backward(fwd, dY, x, Wr, get_expert, *, E, k, kind, mode, rss=False):
     dx_rows = np.zeros((S, d))
     off = lay["offsets"]
     grads = {}
-    F = next(iter(fwd["experts"].values()))["a"].shape[1] if fwd["experts"] else 0
+    # d_ff from an expert that has rows, else from the weights themselves (a
+    # call in which no expert has a row still owes every expert a zero dW)
+    F = (next(iter(fwd["experts"].values()))["a"].shape[1] if fwd["experts"]
+         else get_expert(0)[0].shape[0])
     for e in range(E):
         lo, hi = int(off[e]), int(off[e + 1])
         if hi == lo:

@@ -196,6 +196,26 @@ def test_backward_matches_finite_differences(kind):
             close(fd(Wd, (e,) + idx), gr["dWd"][idx])
 
 
+@pytest.mark.parametrize("mode", ["exact", "bf16", "mxfp8"])
+def test_empty_batch_gives_empty_outputs_and_zero_weight_gradients(mode):
+    """No tokens: the layout is empty, there is no output row, and every
+    gradient that sums over tokens (dW of each expert, dW_r) is the zero
+    matrix of its weight's shape -- an empty sum, whatever the weights."""
+    _, Wr, b, Wg, Wu, Wd = _tiny(41, T=1, d=32, E=4, k=2, F=64)
+    x = np.zeros((0, 32))
+    ge = lambda e: (Wg[e], Wu[e], Wd[e])
+    f = O.forward(x, Wr, b, ge, E=4, k=2, kind=O.SIGMOID, mode=mode)
+    assert f["out"].shape == (0, 32)
+    assert np.array_equal(f["layout"]["counts"], np.zeros(4)) and np.array_equal(f["layout"]["offsets"], np.zeros(5))
+    g = O.backward(f, np.zeros((0, 32)), x, Wr, ge, E=4, k=2, kind=O.SIGMOID, mode=mode, rss=True)
+    assert g["dX"].shape == (0, 32) and g["dgates"].shape == (0, 2)
+    assert g["dWr"].shape == (4, 32) and not g["dWr"].any()
+    for e in range(4):
+        assert g["experts"][e]["dWg"].shape == (64, 32) and not g["experts"][e]["dWg"].any()
+        assert g["experts"][e]["dWu"].shape == (64, 32) and not g["experts"][e]["dWu"].any()
+        assert g["experts"][e]["dWd"].shape == (32, 64) and not g["experts"][e]["dWd"].any()
+
+
 def test_softmax_logit_grad_sums_to_zero_and_gate_grad_closed_form():
     x, Wr, b, Wg, Wu, Wd = _tiny(30, T=12)
     dY = np.random.default_rng(1).standard_normal(x.shape)
